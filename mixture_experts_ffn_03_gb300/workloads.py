@@ -1,0 +1,116 @@
+"""Seeded synthetic workloads for the MoE FFN layer.
+
+This module only draws random inputs; it holds none of the layer's arithmetic.
+Both the CUDA path (through the tests and the benchmark) and the CPU oracle read
+the tensors it returns, byte for byte.
+
+Shapes follow the Qwen3.5-style MoE block described in
+"Add Qwen3.5-35B-A3B (support vision and text input)" (Description: 256 routed
+experts, top-8, one sigmoid-gated shared expert) and the wider 512-expert /
+top-10 family member named in the FastAFD pull request ("What the model needed").
+
+Recipe (fixed draw order, one ``torch.randn`` call per tensor or per expert):
+
+1. hidden      [T, H]      N(0, 1)     -> bf16 (round to nearest even)
+2. logits      [T, E]      N(0, 1)     fp32; the skewed workload adds
+                                       b_e = fp32(-2 ln(e + 1)) to column e
+3. W_gate_up   E x [2I, H] N(0, 0.02)  -> bf16, rows [0, I) gate, [I, 2I) up
+4. W_down      E x [H, I]  N(0, 0.02)  -> bf16
+5. Ws_gate_up  [2I_s, H]   N(0, 0.02)  -> bf16
+6. Ws_down     [H, I_s]    N(0, 0.02)  -> bf16
+7. w_g         [H]         N(0, 0.02)  -> bf16
+
+The generator runs on ``device`` ("cpu" or "cuda"); the two devices give
+different streams for the same seed, so a workload is named by
+(config, seed, generator device).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+SOFTMAX = 0
+SIGMOID = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEConfig:
+    name: str
+    T: int
+    H: int
+    E: int
+    k: int
+    I: int
+    I_s: int
+    score_fn: int
+    skew: bool = False
+
+    def dims(self):
+        return dict(T=self.T, H=self.H, E=self.E, k=self.k, I=self.I, I_s=self.I_s,
+                    score_fn=self.score_fn)
+
+    def with_tokens(self, T: int) -> "MoEConfig":
+        return dataclasses.replace(self, T=T)
+
+
+# The five workloads: tiny correctness case, decode-shaped, prefill-shaped,
+# wide-expert (512 experts, top-10) and Zipf-skewed routing.
+CONFIGS = {
+    "tiny": MoEConfig("tiny", T=16, H=128, E=16, k=4, I=64, I_s=64, score_fn=SOFTMAX),
+    "decode": MoEConfig("decode", T=64, H=2048, E=256, k=8, I=512, I_s=512, score_fn=SIGMOID),
+    "prefill": MoEConfig("prefill", T=4096, H=2048, E=256, k=8, I=512, I_s=512, score_fn=SOFTMAX),
+    "wide": MoEConfig("wide", T=2048, H=4096, E=512, k=10, I=1024, I_s=1024, score_fn=SIGMOID),
+    "skewed": MoEConfig("skewed", T=8192, H=2048, E=256, k=8, I=512, I_s=512, score_fn=SOFTMAX,
+                        skew=True),
+}
+CONFIG_ORDER = ["tiny", "decode", "prefill", "wide", "skewed"]
+
+
+def skew_bias(E: int) -> torch.Tensor:
+    """Per-expert logit bias of the skewed workload: fp32(-2 ln(rank)), rank = e + 1."""
+    return torch.tensor([-2.0 * math.log(e + 1.0) for e in range(E)], dtype=torch.float64).to(
+        torch.float32)
+
+
+def _bf16(x: torch.Tensor, scale: float) -> torch.Tensor:
+    if scale != 1.0:
+        x = x * scale
+    return x.to(torch.bfloat16)
+
+
+def make_inputs(cfg: MoEConfig, seed: int = 0, device: str = "cpu",
+                weights_device: str | None = None) -> dict:
+    """Draw one workload. Returns a dict of tensors on ``weights_device``
+    (default: ``device``). All tensors are contiguous row-major."""
+    dev = torch.device(device)
+    out_dev = torch.device(weights_device) if weights_device is not None else dev
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    T, H, E, I, I_s = cfg.T, cfg.H, cfg.E, cfg.I, cfg.I_s
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
+
+    hidden = _bf16(randn(T, H), 1.0).to(out_dev)
+    logits = randn(T, E)
+    if cfg.skew:
+        logits = logits + skew_bias(E).to(dev)
+    logits = logits.to(out_dev)
+    w_gate_up = torch.empty(E, 2 * I, H, dtype=torch.bfloat16, device=out_dev)
+    for e in range(E):
+        w_gate_up[e].copy_(_bf16(randn(2 * I, H), 0.02))
+    w_down = torch.empty(E, H, I, dtype=torch.bfloat16, device=out_dev)
+    for e in range(E):
+        w_down[e].copy_(_bf16(randn(H, I), 0.02))
+    ws_gate_up = _bf16(randn(2 * I_s, H), 0.02).to(out_dev)
+    ws_down = _bf16(randn(H, I_s), 0.02).to(out_dev)
+    w_g = _bf16(randn(H), 0.02).to(out_dev)
+    return dict(hidden=hidden, logits=logits.contiguous(), w_gate_up=w_gate_up, w_down=w_down,
+                ws_gate_up=ws_gate_up, ws_down=ws_down, w_g=w_g)
+
+
+def bf16_bits(t: torch.Tensor):
+    """bf16 tensor -> numpy uint16 array of its bit patterns (host copy)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")

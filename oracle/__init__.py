@@ -1,0 +1,147 @@
+"""CPU fp64 oracle of the MoE FFN layer (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package. The library it wraps (``moe_oracle.c``) is plain C,
+compiled with gcc; it shares no code with the CUDA path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+_lib = None
+
+SOFTMAX = 0
+SIGMOID = 1
+
+
+def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math)."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", src, "-o", out + ".tmp",
+               "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(out + ".tmp", out)
+    return out
+
+
+def _load(path: str | None = None):
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    i = ctypes.c_int
+    lib.oracle_route.argtypes = [i, i, i, i, P, P, P]
+    lib.oracle_route.restype = i
+    lib.oracle_expert_counts.argtypes = [i, i, i, P, P]
+    lib.oracle_expert_counts.restype = None
+    lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i] + [P] * 8 + [i] + [P] * 5 + [i]
+    lib.oracle_moe_forward.restype = i
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    """Accept a torch bf16 tensor or a numpy uint16 array of bf16 bits."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+        return a.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def _f32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().contiguous().cpu().numpy()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def route(logits, k: int, score_fn: int, lib_path: str | None = None):
+    """Routing of every token: (ids [T,k] int32, weights [T,k] fp64)."""
+    lib = _load(lib_path)
+    lg = _f32(logits)
+    T, E = lg.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    bad = lib.oracle_route(T, E, k, score_fn, _ptr(lg), _ptr(ids), _ptr(w))
+    assert bad == 0, f"{bad} tokens: fp64 score order contradicts the logit order"
+    return ids, w
+
+
+def expert_counts(ids, E: int, lib_path: str | None = None) -> np.ndarray:
+    lib = _load(lib_path)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, dtype=np.int32)
+    lib.oracle_expert_counts(T, E, k, _ptr(ids), _ptr(counts))
+    return counts
+
+
+def moe_forward(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=None,
+                n_threads: int | None = None, lib_path: str | None = None):
+    """Evaluate the layer in fp64 for ``tokens`` (default: all tokens).
+
+    ``inputs`` holds hidden, logits, w_gate_up, w_down, ws_gate_up, ws_down,
+    w_g (torch tensors or numpy bf16-bit arrays). Returns a dict with
+    out [n,H] fp64, ids [n,k], weights [n,k] fp64 and gate [n] fp64.
+    """
+    lib = _load(lib_path)
+    hidden = _u16(inputs["hidden"])
+    logits = _f32(inputs["logits"])
+    wgu = _u16(inputs["w_gate_up"])
+    wd = _u16(inputs["w_down"])
+    wsgu = _u16(inputs["ws_gate_up"])
+    wsd = _u16(inputs["ws_down"])
+    wg = _u16(inputs["w_g"])
+    T, H = hidden.shape
+    E = logits.shape[1]
+    I = wgu.shape[1] // 2
+    I_s = wsgu.shape[0] // 2
+    assert wgu.shape == (E, 2 * I, H) and wd.shape == (E, H, I)
+    assert wsgu.shape == (2 * I_s, H) and wsd.shape == (H, I_s) and wg.shape == (H,)
+    if tokens is None:
+        tok = None
+        n = T
+    else:
+        tok = np.ascontiguousarray(tokens, dtype=np.int64)
+        n = tok.shape[0]
+        assert n == 0 or (tok.min() >= 0 and tok.max() < T)
+    go = None if gate_override is None else np.ascontiguousarray(gate_override, dtype=np.float64)
+    if go is not None:
+        assert go.shape == (n,)
+    out = np.empty((n, H), dtype=np.float64)
+    ids = np.empty((n, k), dtype=np.int32)
+    w = np.empty((n, k), dtype=np.float64)
+    gate = np.empty((n,), dtype=np.float64)
+    if n == 0:
+        return dict(out=out, ids=ids, weights=w, gate=gate)
+    bad = lib.oracle_moe_forward(T, H, E, k, I, I_s, score_fn, _ptr(hidden), _ptr(logits),
+                                 _ptr(wgu), _ptr(wd), _ptr(wsgu), _ptr(wsd), _ptr(wg), _ptr(tok),
+                                 n, _ptr(go), _ptr(out), _ptr(ids), _ptr(w), _ptr(gate),
+                                 n_threads or default_threads())
+    assert bad == 0, f"{bad} tokens: fp64 score order contradicts the logit order"
+    return dict(out=out, ids=ids, weights=w, gate=gate)
