@@ -1,0 +1,366 @@
+"""Benchmark of the MoE FFN layer on GB300: tokens/s and roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step = one moe_forward (route, permute, gate_up GEMM, down GEMM, shared
+expert, combine) over the workload's T tokens, inputs resident in HBM. Each
+timed step is bracketed by CUDA events on the launching stream, with a 256 MB
+write between steps to flush L2. Per-kernel times come from events the
+library records around each of its kernels on the same stream. Prints one
+JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded token sample per step), with the same metric and workload.
+Multi-GPU runs (torchrun) are independent replicas: the layer does not shard.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+DEFAULT_CONFIG = "decode"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        hbm = float(p.get("hbm_gbs"))
+        tf = float(p.get("bf16_tflops"))
+        tfs = float(p.get("bf16_tflops_sustained", tf))
+        return dict(hbm_gbs=hbm, bf16_tflops=tf, bf16_tflops_sustained=tfs, source="measured")
+    except Exception:
+        return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS,
+                    bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_name(cfg):
+    sf = "softmax" if cfg.score_fn == 0 else "sigmoid"
+    return (f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} I={cfg.I} I_s={cfg.I_s} "
+            f"{sf}+renorm{', zipf-skewed logits' if cfg.skew else ''}")
+
+
+def algorithmic_work(cfg, counts):
+    """Layer FLOPs and touched bytes from the actual routing (counts per expert)."""
+    T, H, E, k, I, I_s = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_s
+    touched = int(sum(1 for c in counts if c > 0))
+    flops = 6.0 * H * I * T * k + 6.0 * H * I_s * T + 2.0 * H * T
+    w_routed = touched * 6.0 * I * H
+    w_shared = 6.0 * I_s * H
+    act = 2.0 * T * H + 4.0 * T * E + 2.0 * T * H
+    bytes_total = w_routed + w_shared + 2.0 * H + act
+    gate_up_bytes = touched * 4.0 * I * H + 4.0 * I_s * H + 2.0 * T * H
+    gate_up_flops = 4.0 * H * I * T * k + 4.0 * H * I_s * T
+    down_bytes = touched * 2.0 * I * H + 2.0 * I_s * H
+    down_flops = 2.0 * H * I * T * k + 2.0 * H * I_s * T
+    return dict(touched=touched, flops=flops, bytes=bytes_total, gate_up_bytes=gate_up_bytes,
+                gate_up_flops=gate_up_flops, down_bytes=down_bytes, down_flops=down_flops)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        time.sleep(0.06)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+def read_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
+    summary was taken on the current kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in ("moe_gemm.cu", "ptx.cuh", "moe_internal.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_ffn_03_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            key, _, v = line.strip()[2:].partition(":")
+            vals[key.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != h.hexdigest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from mixture_experts_ffn_03_gb300 import workloads as wl
+    inp = wl.make_inputs(cfg, seed=0)
+    threads = oracle.default_threads()
+    # Size the per-step token sample for about 1-3 s of oracle work per step.
+    probe = oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=np.arange(min(cfg.T, threads)),
+                               n_threads=threads)
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=np.arange(min(cfg.T, threads)),
+                       n_threads=threads)
+    per_batch = time.perf_counter() - t0
+    n_tok = int(max(threads, min(cfg.T, threads * max(1, int(2.0 / max(per_batch, 1e-3))))))
+    toks = np.arange(n_tok) % cfg.T
+    for _ in range(args.warmup):
+        oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=toks[:threads], n_threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=toks, n_threads=threads)
+        times.append(time.perf_counter() - t0)
+    del probe
+    total = sum(times)
+    value = n_tok * len(times) / total
+    sample = f"{n_tok} of {cfg.T} tokens per step, fp64, all routed + shared experts"
+    line = dict(impl="reference", metric="MoE-layer tokens/s", value=value, unit="tokens/s",
+                n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=1e3 * total / len(times), higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=workload_name(cfg), seed=0),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=threads, kind="oracle",
+                                  sample=sample),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_cpu_baseline(cfg, inp_cpu, budget_s=12.0):
+    import numpy as np
+    import oracle
+    threads = oracle.default_threads()
+    n = min(cfg.T, threads)
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp_cpu, cfg.k, cfg.score_fn, tokens=np.arange(n), n_threads=threads)
+    dt = time.perf_counter() - t0
+    reps = max(1, int(budget_s / max(dt, 1e-3)))
+    n_tok = min(cfg.T * 4, n * reps)
+    toks = np.arange(n_tok) % cfg.T
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp_cpu, cfg.k, cfg.score_fn, tokens=toks, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return dict(value=n_tok / dt, unit="tokens/s", cores=threads, kind="oracle",
+                sample=f"{n_tok} tokens of the {cfg.name} workload (token t mod {cfg.T}), fp64, "
+                       f"{dt:.1f} s")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from mixture_experts_ffn_03_gb300 import workloads as wl
+    cfg = wl.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import numpy as np
+    import torch
+    import mixture_experts_ffn_03_gb300 as moe
+
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    moe.load_library()
+
+    inp = wl.make_inputs(cfg, seed=0, device=str(dev))
+    layer = moe.MoELayer(inp["w_gate_up"], inp["w_down"], inp["ws_gate_up"], inp["ws_down"],
+                         inp["w_g"], cfg.k, cfg.score_fn)
+    T = cfg.T
+    stream = torch.cuda.Stream(dev)
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            layer.forward(inp["hidden"], inp["logits"], out=out, counts=counts, stream=stream)
+    st = moe.device_status(layer.workspace(T), stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.status_string(st))
+    work = algorithmic_work(cfg, counts.cpu().tolist())
+
+    K = args.steps
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
+                for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            moe.set_stage_events(stage_ev[i])
+            step_ev[i][0].record(stream)
+            layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
+            step_ev[i][1].record(stream)
+    moe.set_stage_events(None)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    st = moe.device_status(layer.workspace(T), stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.status_string(st))
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    total_ms = sum(step_ms)
+    stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev]
+                for j in range(moe.NUM_STAGES)]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # End to end through the public API: pinned host inputs in, output back.
+    h_host = inp["hidden"].cpu().pin_memory()
+    l_host = inp["logits"].cpu().pin_memory()
+    o_host = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            layer.forward_from_host(h_host, l_host, o_host, stream=stream)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            e2e_ev[i][0].record(stream)
+            layer.forward_from_host(h_host, l_host, o_host, stream=stream)
+            e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = load_peaks()
+    value = world * T * K / (total_ms / 1e3)
+    ms_step = total_ms / K
+    gu_ms = statistics.mean(stage_ms[3])
+    dn_ms = statistics.mean(stage_ms[4])
+    hbm_bound = work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (
+        peaks["bf16_tflops_sustained"] * 1e12)
+    if hbm_bound:
+        achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
+        roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=achieved / peaks["hbm_gbs"],
+                    traffic=read_traffic("moe_gate_up", cfg.name),
+                    kernel="moe gate_up grouped GEMM", peak_source=peaks["source"])
+    else:
+        achieved = work["gate_up_flops"] / (gu_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
+                    frac=achieved / peak, traffic=read_traffic("moe_gate_up", cfg.name),
+                    kernel="moe gate_up grouped GEMM", peak_source=peaks["source"])
+    t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 work["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
+    layer_roof = dict(bound="hbm" if hbm_bound else "tensor", roofline_ms=t_roof * 1e3,
+                      frac=t_roof * 1e3 / ms_step, bytes=work["bytes"], flops=work["flops"],
+                      experts_touched=work["touched"],
+                      frac_vs_nominal_8tbs=(work["bytes"] / 8e12 * 1e3) / ms_step)
+    kernels = {n: round(statistics.mean(v) * 1e3, 2) for n, v in zip(moe.STAGE_NAMES, stage_ms)}
+    h2d = T * cfg.H * 2 + T * cfg.E * 4
+    d2h = T * cfg.H * 2
+    line = dict(
+        metric="MoE-layer tokens/s", value=value, unit="tokens/s", n_gpus=world, steps=K,
+        warmup=args.warmup, ms_per_step=ms_step, higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="bf16", data="synthetic",
+        config=dict(workload=workload_name(cfg), seed=0, parallelism="replicas" if world > 1 else "1gpu",
+                    l2="flushed: 256 MB write between timed steps", launch="stream",
+                    wall_s=round(wall, 3)),
+        roofline=roof, layer_roofline=layer_roof, kernel_us=kernels,
+        down_gbs=work["down_bytes"] / (dn_ms / 1e3) / 1e9,
+        e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
+                 d2h_bytes_per_step=d2h),
+        gpu_launches=moe.NUM_STAGES * K, clocks=clocks)
+    if world == 1 and not args.no_cpu_baseline:
+        inp_cpu = {n: t.cpu() for n, t in inp.items()}
+        line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,149 @@
+/*
+ * libmoe: the FFN-side Mixture-of-Experts layer of a Qwen3.5-style hybrid
+ * model on one Blackwell (sm_103a) GPU, behind a plain C ABI.
+ *
+ * The layer sits at the attention-to-experts boundary described in
+ * "[RFC] Experimental Qwen3.5 MoE AFD support: CUDA correctness baseline"
+ * (Proposed plugin boundary): it receives the hidden states and one fp32
+ * router-logit row per token, runs the routed experts and the shared expert,
+ * and returns the expert output. The residual add stays with the caller.
+ *
+ * Per token t with hidden row x (bf16, length H) and logit row l (fp32,
+ * length E):
+ *   1. score   s_e = softmax_e(l) or sigmoid(l_e)          (selectable)
+ *   2. select  the k experts with the largest logits, ties to the lower
+ *              expert index, ordered by descending logit
+ *   3. weight  w_j = s_{e_j} / sum_j' s_{e_j'}             (top-k renorm)
+ *   4. expert  y_j = W_down[e_j] (silu(G x) * (U x)),  G = W_gate_up[e_j][0:I],
+ *              U = W_gate_up[e_j][I:2I]                     (SwiGLU)
+ *   5. shared  y_s = Ws_down (silu(Gs x) * (Us x)), gated by sigmoid(x . w_g)
+ *   6. output  out = bf16( sum_j w_j y_j + sigmoid(x . w_g) y_s )
+ * Sources: "Add Qwen3.5-35B-A3B (support vision and text input)":
+ * Description (top-8 of 256 experts, per-token sigmoid-gated shared expert,
+ * stacked 3D expert weights), Model Information (sigmoid routing) and
+ * Additional Information (router in fp32, softmax score, normalize top-k
+ * affinities).
+ *
+ * Conventions for every entry point:
+ *   - Tensor arguments are DEVICE pointers to contiguous row-major arrays,
+ *     owned by the caller, 16-byte aligned. The library keeps no pointer
+ *     after a call returns and allocates no device memory.
+ *   - bf16 arrays are passed as void* (IEEE bfloat16 bit patterns).
+ *   - Work is enqueued on the caller's CUDA stream (cudaStream_t passed as
+ *     void*; NULL = legacy default stream) without a host synchronisation;
+ *     results are valid once the stream has reached that point.
+ *   - Calls that share one workspace must not overlap on the GPU.
+ */
+#ifndef LIBMOE_MOE_H
+#define LIBMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_SCORE_SOFTMAX = 0, /* softmax over all E logits of the token */
+    MOE_SCORE_SIGMOID = 1  /* independent sigmoid of each logit */
+} moe_score_fn;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,   /* H, I or I_s not a multiple of 64 */
+    MOE_ERR_WORKSPACE = 3,     /* workspace null or smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
+    MOE_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up waiting on an internal pipeline
+                                  barrier and returned early; outputs are invalid */
+} moe_status;
+
+/* Problem sizes. T tokens, hidden size H, E routed experts, top-k, expert
+ * intermediate size I, shared-expert intermediate size I_s, and the score
+ * function (a moe_score_fn value).
+ * Limits: 0 <= T <= 2^22; 1 <= k <= E <= 1024; k <= 32; H, I, I_s in
+ * [64, 65536] and multiples of 64 (else MOE_ERR_UNSUPPORTED). */
+typedef struct {
+    int32_t T, H, E, k, I, I_s;
+    int32_t score_fn;
+} moe_dims;
+
+/* Bytes of device workspace moe_forward needs for these sizes (0 if the
+ * sizes are invalid). The workspace holds the routing results, the
+ * per-expert token lists, the SwiGLU activations and the per-slot expert
+ * outputs; its size grows as T * (k + 1) * H * 4 bytes plus lower-order
+ * terms. */
+size_t moe_workspace_size(const moe_dims* d);
+
+/*
+ * Run the layer.
+ *   hidden        [T, H]       bf16   normed hidden states
+ *   router_logits [T, E]       fp32   router logits (computed upstream)
+ *   w_gate_up     [E, 2I, H]   bf16   rows [0, I) gate, rows [I, 2I) up
+ *   w_down        [E, H, I]    bf16
+ *   ws_gate_up    [2I_s, H]    bf16   shared expert, same row convention
+ *   ws_down       [H, I_s]     bf16
+ *   w_g           [H]          bf16   shared-expert gate vector
+ *   out           [T, H]       bf16   expert output (written)
+ *   topk_ids_out  [T, k]       int32  selected experts, in ranking order (NULL: not returned)
+ *   topk_w_out    [T, k]       fp32   renormalised weights (NULL: not returned)
+ *   expert_counts_out [E]      int32  tokens routed to each expert (NULL: not returned)
+ *   workspace     device buffer of at least moe_workspace_size(d) bytes,
+ *                 256-byte aligned; its contents need no initialisation
+ *   cuda_stream   cudaStream_t as void*
+ * Returns MOE_OK after enqueueing every kernel. T = 0 returns MOE_OK and
+ * enqueues nothing. Errors detected on the host return before anything is
+ * enqueued. Non-finite logits give an unspecified (but in-range) routing.
+ * Device-side pipeline timeouts are reported by moe_device_status().
+ */
+moe_status moe_forward(const moe_dims* d, const void* hidden, const float* router_logits,
+                       const void* w_gate_up, const void* w_down, const void* ws_gate_up,
+                       const void* ws_down, const void* w_g, void* out, int32_t* topk_ids_out,
+                       float* topk_w_out, int32_t* expert_counts_out, void* workspace,
+                       size_t workspace_bytes, void* cuda_stream);
+
+/* Synchronise cuda_stream, then report MOE_ERR_DEVICE_TIMEOUT if the last
+ * moe_forward that used this workspace hit a pipeline timeout, MOE_ERR_CUDA
+ * on a CUDA error, else MOE_OK. */
+moe_status moe_device_status(const void* workspace, void* cuda_stream);
+
+/* Static, human-readable name of a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Byte offsets of the intermediate arrays inside the workspace, for
+ * inspection after a call (all arrays row-major):
+ *   topk_ids  [T, k] int32, topk_w [T, k] fp32, gate_logit [T] fp32 (x . w_g),
+ *   counts [E] int32, offsets [E + 1] int32 (exclusive prefix of counts),
+ *   perm [T k] int32 (slot t*k+j at its position in expert-sorted order,
+ *   tokens ascending within an expert), inv [T k] int32 (position of slot
+ *   t*k+j), h_hi / h_lo [T k, I] bf16 (SwiGLU activation of each routed slot
+ *   in sorted order, as a high + low bf16 pair), hs_hi / hs_lo [T, I_s] bf16
+ *   (shared expert activation), y [T k + T, H] fp32 (rows [0, T k): routed
+ *   expert outputs in sorted order; rows T k + t: gated shared output). */
+typedef struct {
+    size_t topk_ids, topk_w, gate_logit, counts, offsets, perm, inv;
+    size_t h_hi, h_lo, hs_hi, hs_lo, y;
+    size_t total;
+} moe_workspace_layout_t;
+
+moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layout);
+
+/* Number of kernels one moe_forward enqueues (route, count/scan, scatter,
+ * gate_up GEMM, down GEMM, combine). */
+#define MOE_NUM_STAGES 6
+
+/* Optional per-kernel timing. `events` points to MOE_NUM_STAGES + 1
+ * cudaEvent_t handles (passed as void*) created by the caller; while set,
+ * every moe_forward issued from the calling host thread records events[i]
+ * on its stream just before kernel i and events[MOE_NUM_STAGES] after the
+ * last one, so kernel i runs between events[i] and events[i + 1]. Pass NULL
+ * (n_events = 0) to stop. The library does not own the events. Returns
+ * MOE_ERR_INVALID_ARG unless n_events is 0 or MOE_NUM_STAGES + 1. */
+moe_status moe_set_stage_events(void* const* events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMOE_MOE_H */

@@ -1,0 +1,195 @@
+"""Python binding of libmoe, the sm_103a MoE FFN layer (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. Importing
+this package loads ``libmoe.so`` from this directory and fails loudly if it
+has not been built (``python -m mixture_experts_ffn_03_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+SOFTMAX = 0
+SIGMOID = 1
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT"}
+
+EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
+            "moe_workspace_layout", "moe_set_stage_events"]
+NUM_STAGES = 6
+STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
+
+
+class MoEDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("I", ctypes.c_int32), ("I_s", ctypes.c_int32),
+                ("score_fn", ctypes.c_int32)]
+
+
+class MoEWorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("topk_ids", "topk_w", "gate_logit", "counts", "offsets", "perm", "inv", "h_hi",
+                 "h_lo", "hs_hi", "hs_lo", "y", "total")]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmoe.so (once). Raises if the CUDA library has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmoe.so not found at {path}; build it first "
+                           "(python -m mixture_experts_ffn_03_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    lib.moe_workspace_size.argtypes = [ctypes.POINTER(MoEDims)]
+    lib.moe_workspace_size.restype = ctypes.c_size_t
+    lib.moe_forward.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 11 + [P, ctypes.c_size_t, P]
+    lib.moe_forward.restype = ctypes.c_int
+    lib.moe_device_status.argtypes = [P, P]
+    lib.moe_device_status.restype = ctypes.c_int
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_workspace_layout.argtypes = [ctypes.POINTER(MoEDims), ctypes.POINTER(MoEWorkspaceLayout)]
+    lib.moe_workspace_layout.restype = ctypes.c_int
+    lib.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+    lib.moe_set_stage_events.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def make_dims(T, H, E, k, I, I_s, score_fn) -> MoEDims:
+    return MoEDims(int(T), int(H), int(E), int(k), int(I), int(I_s), int(score_fn))
+
+
+def workspace_size(dims: MoEDims) -> int:
+    return int(load_library().moe_workspace_size(ctypes.byref(dims)))
+
+
+def workspace_layout(dims: MoEDims) -> MoEWorkspaceLayout:
+    out = MoEWorkspaceLayout()
+    st = load_library().moe_workspace_layout(ctypes.byref(dims), ctypes.byref(out))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_workspace_layout")
+    return out
+
+
+def status_string(status: int) -> str:
+    return load_library().moe_status_string(int(status)).decode()
+
+
+def set_stage_events(events) -> None:
+    """Record torch.cuda.Event objects around each kernel of subsequent
+    moe_forward calls from this thread (NUM_STAGES + 1 events), or stop (None)."""
+    lib = load_library()
+    if events is None:
+        st = lib.moe_set_stage_events(None, 0)
+    else:
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        st = lib.moe_set_stage_events(arr, len(events))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_set_stage_events")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def forward_raw(dims: MoEDims, hidden, logits, w_gate_up, w_down, ws_gate_up, ws_down, w_g, out,
+                workspace, topk_ids_out=None, topk_w_out=None, counts_out=None,
+                stream=None) -> int:
+    """Direct call of moe_forward on tensors (or None); returns the status code."""
+    lib = load_library()
+    return int(lib.moe_forward(ctypes.byref(dims), _ptr(hidden), _ptr(logits), _ptr(w_gate_up),
+                               _ptr(w_down), _ptr(ws_gate_up), _ptr(ws_down), _ptr(w_g),
+                               _ptr(out), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(counts_out),
+                               _ptr(workspace),
+                               ctypes.c_size_t(0 if workspace is None else workspace.numel()),
+                               _stream_handle(stream)))
+
+
+def device_status(workspace, stream=None) -> int:
+    return int(load_library().moe_device_status(_ptr(workspace), _stream_handle(stream)))
+
+
+class MoELayer:
+    """The layer's weights plus a reusable workspace on one CUDA device.
+
+    ``forward(hidden, logits)`` enqueues one moe_forward on the current
+    stream; outputs are allocated by PyTorch unless ``out`` is given."""
+
+    def __init__(self, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int, score_fn: int):
+        import torch
+        self.w_gate_up, self.w_down = w_gate_up, w_down
+        self.ws_gate_up, self.ws_down, self.w_g = ws_gate_up, ws_down, w_g
+        self.E, two_i, self.H = w_gate_up.shape
+        self.I = two_i // 2
+        self.I_s = ws_gate_up.shape[0] // 2
+        self.k, self.score_fn = int(k), int(score_fn)
+        self.device = w_gate_up.device
+        self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+        self._ws_T = -1
+
+    def dims(self, T: int) -> MoEDims:
+        return make_dims(T, self.H, self.E, self.k, self.I, self.I_s, self.score_fn)
+
+    def workspace(self, T: int):
+        import torch
+        need = workspace_size(self.dims(T))
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, hidden, logits, out=None, topk_ids=None, topk_w=None, counts=None,
+                stream=None):
+        import torch
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        ws = self.workspace(T)
+        st = forward_raw(self.dims(T), hidden, logits, self.w_gate_up, self.w_down,
+                         self.ws_gate_up, self.ws_down, self.w_g, out, ws, topk_ids, topk_w,
+                         counts, stream)
+        if st != MOE_OK:
+            raise MoEError(st, "moe_forward")
+        return out
+
+    def forward_from_host(self, hidden_host, logits_host, out_host, stream=None):
+        """End-to-end call from pinned host buffers: copy hidden and logits in,
+        run the layer, copy the output back (all on one stream)."""
+        import torch
+        T = hidden_host.shape[0]
+        if not hasattr(self, "_io") or self._io[0].shape[0] != T:
+            self._io = (torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device),
+                        torch.empty(T, self.E, dtype=torch.float32, device=self.device),
+                        torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device))
+        h, l, o = self._io
+        s = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            h.copy_(hidden_host, non_blocking=True)
+            l.copy_(logits_host, non_blocking=True)
+            self.forward(h, l, out=o, stream=s)
+            out_host.copy_(o, non_blocking=True)
+        return out_host

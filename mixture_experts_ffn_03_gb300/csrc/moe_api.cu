@@ -1,0 +1,313 @@
+// C ABI of libmoe: argument checks, workspace carving, TMA descriptors and
+// the launch sequence route -> count/scan -> scatter -> gate_up -> down ->
+// combine on the caller's stream. See include/moe.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "moe.h"
+#include "moe_internal.cuh"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    size_t meta, topk_ids, topk_w, gate_logit, counts, offsets, perm, inv, blockhist;
+    size_t rt_gu, rt_dn, h_hi, h_lo, hs_hi, hs_lo, y, total;
+};
+
+bool dims_valid(const moe_dims* d) {
+    if (!d) return false;
+    if (d->T < 0 || d->T > (1 << 22)) return false;
+    if (d->E < 1 || d->E > 1024) return false;
+    if (d->k < 1 || d->k > 32 || d->k > d->E) return false;
+    if (d->H < 1 || d->H > 65536 || d->I < 1 || d->I > 65536 || d->I_s < 1 || d->I_s > 65536)
+        return false;
+    if (d->score_fn != MOE_SCORE_SOFTMAX && d->score_fn != MOE_SCORE_SIGMOID) return false;
+    return true;
+}
+
+bool dims_supported(const moe_dims* d) {
+    return d->H % 64 == 0 && d->I % 64 == 0 && d->I_s % 64 == 0 && d->H >= 64 && d->I >= 64 &&
+           d->I_s >= 64;
+}
+
+// Upper bound on the routed row tiles of a GEMM with tile width bn.
+size_t max_row_tiles(size_t tk, size_t E, size_t bn) { return tk / bn + (tk < E ? tk : E) + 1; }
+
+Layout layout_of(const moe_dims& d) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + (bytes ? bytes : 1), kAlign);
+        return o;
+    };
+    const size_t T = d.T, H = d.H, E = d.E, I = d.I, Is = d.I_s, tk = T * d.k;
+    const size_t nb = (T + kCountTokens - 1) / kCountTokens;
+    L.meta = take(META_WORDS * sizeof(int));
+    L.topk_ids = take(tk * 4);
+    L.topk_w = take(tk * 4);
+    L.gate_logit = take(T * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take(tk * 4);
+    L.inv = take(tk * 4);
+    L.blockhist = take(nb * E * 4);
+    L.rt_gu = take(max_row_tiles(tk, E, 16) * sizeof(int2));
+    L.rt_dn = take(max_row_tiles(tk, E, 16) * sizeof(int2));
+    L.h_hi = take(tk * I * 2);
+    L.h_lo = take(tk * I * 2);
+    L.hs_hi = take(T * Is * 2);
+    L.hs_lo = take(T * Is * 2);
+    L.y = take((tk + T) * H * 4);
+    L.total = off;
+    return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [outer, inner] read in boxes of 64 x box_rows with
+// the 128-byte swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Tokens per tile: the smallest supported width >= 1.25x the mean group size.
+int pick_bn(size_t tk, int E, int cap) {
+    const double mean = static_cast<double>(tk) / E;
+    int bn = 16;
+    while (bn < cap && bn < 1.25 * mean) bn *= 2;
+    return bn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Caller-owned timing events of this host thread (moe_set_stage_events).
+thread_local cudaEvent_t tl_stage_events[MOE_NUM_STAGES + 1];
+thread_local bool tl_stage_events_on = false;
+
+void mark_stage(int i, cudaStream_t st) {
+    if (tl_stage_events_on) cudaEventRecord(tl_stage_events[i], st);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_workspace_size(const moe_dims* d) {
+    if (!dims_valid(d)) return 0;
+    return layout_of(*d).total;
+}
+
+MOE_API moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* out) {
+    if (!dims_valid(d) || !out) return MOE_ERR_INVALID_ARG;
+    const Layout L = layout_of(*d);
+    out->topk_ids = L.topk_ids;
+    out->topk_w = L.topk_w;
+    out->gate_logit = L.gate_logit;
+    out->counts = L.counts;
+    out->offsets = L.offsets;
+    out->perm = L.perm;
+    out->inv = L.inv;
+    out->h_hi = L.h_hi;
+    out->h_lo = L.h_lo;
+    out->hs_hi = L.hs_hi;
+    out->hs_lo = L.hs_lo;
+    out->y = L.y;
+    out->total = L.total;
+    return MOE_OK;
+}
+
+MOE_API const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size (H, I and I_s must be multiples of 64)";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const float* router_logits,
+                               const void* w_gate_up, const void* w_down, const void* ws_gate_up,
+                               const void* ws_down, const void* w_g, void* out,
+                               int32_t* topk_ids_out, float* topk_w_out,
+                               int32_t* expert_counts_out, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream) {
+    if (!dims_valid(d)) return MOE_ERR_INVALID_ARG;
+    if (!dims_supported(d)) return MOE_ERR_UNSUPPORTED;
+    if (d->T == 0) return MOE_OK;
+    const void* required[] = {hidden, router_logits, w_gate_up, w_down, ws_gate_up,
+                              ws_down, w_g, out};
+    for (const void* p : required)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const void* optional[] = {topk_ids_out, topk_w_out, expert_counts_out};
+    for (const void* p : optional)
+        if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
+    const Layout L = layout_of(*d);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return MOE_ERR_WORKSPACE;
+
+    const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->I, Is = d->I_s;
+    const size_t tk = static_cast<size_t>(T) * k;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    char* ws = static_cast<char*>(workspace);
+    int* meta = reinterpret_cast<int*>(ws + L.meta);
+    int* topk_ids = reinterpret_cast<int*>(ws + L.topk_ids);
+    float* topk_w = reinterpret_cast<float*>(ws + L.topk_w);
+    float* gate_logit = reinterpret_cast<float*>(ws + L.gate_logit);
+    int* counts = reinterpret_cast<int*>(ws + L.counts);
+    int* offsets = reinterpret_cast<int*>(ws + L.offsets);
+    int* perm = reinterpret_cast<int*>(ws + L.perm);
+    int* inv = reinterpret_cast<int*>(ws + L.inv);
+    int* blockhist = reinterpret_cast<int*>(ws + L.blockhist);
+    int2* rt_gu = reinterpret_cast<int2*>(ws + L.rt_gu);
+    int2* rt_dn = reinterpret_cast<int2*>(ws + L.rt_dn);
+    auto* h_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.h_hi);
+    auto* h_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.h_lo);
+    auto* hs_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_hi);
+    auto* hs_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_lo);
+    float* y = reinterpret_cast<float*>(ws + L.y);
+
+    const int bn_gu = pick_bn(tk, E, 256);
+    const int bn_dn = pick_bn(tk, E, 128);
+    const int num_sms = sm_count();
+    if (num_sms <= 0) return MOE_ERR_CUDA;
+
+    GemmMaps gu{}, dn{};
+    bool ok = make_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E) * 2 * I, kGemmBM) &&
+              make_map(&gu.ws, ws_gate_up, H, static_cast<uint64_t>(2) * Is, kGemmBM) &&
+              make_map(&dn.w, w_down, I, static_cast<uint64_t>(E) * H, kGemmBM) &&
+              make_map(&dn.ws, ws_down, Is, H, kGemmBM) &&
+              make_map(&dn.h_hi, h_hi, I, tk, bn_dn) && make_map(&dn.h_lo, h_lo, I, tk, bn_dn) &&
+              make_map(&dn.hs_hi, hs_hi, Is, T, bn_dn) && make_map(&dn.hs_lo, hs_lo, Is, T, bn_dn);
+    if (!ok) return MOE_ERR_CUDA;
+
+    GemmArgs ga{};
+    ga.T = T;
+    ga.H = H;
+    ga.E = E;
+    ga.k = k;
+    ga.I = I;
+    ga.I_s = Is;
+    ga.hidden = static_cast<const __nv_bfloat16*>(hidden);
+    ga.perm = perm;
+    ga.counts = counts;
+    ga.offsets = offsets;
+    ga.meta = meta;
+    ga.gate_logit = gate_logit;
+    ga.h_hi = h_hi;
+    ga.h_lo = h_lo;
+    ga.hs_hi = hs_hi;
+    ga.hs_lo = hs_lo;
+    ga.y = y;
+    ga.err = reinterpret_cast<unsigned*>(meta + META_ERR);
+    GemmArgs gd = ga;
+    ga.rowtiles = rt_gu;
+    gd.rowtiles = rt_dn;
+
+    const size_t routed_min = tk < static_cast<size_t>(E) ? tk : static_cast<size_t>(E);
+    const int F_gu = (I + kGemmBM - 1) / kGemmBM, F_s = (Is + kGemmBM - 1) / kGemmBM;
+    const int F_dn = (H + kGemmBM - 1) / kGemmBM;
+    const size_t max_gu = (tk / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
+    const size_t max_dn = (tk / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
+    const int cap = 1 << 30;
+
+    mark_stage(0, st);
+    if ((launch_route(T, H, E, k, d->score_fn, router_logits,
+                          static_cast<const __nv_bfloat16*>(hidden),
+                          static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w, gate_logit,
+                          topk_ids_out, topk_w_out, meta, st)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark_stage(1, st);
+    if ((launch_count_scan(T, E, k, bn_gu, bn_dn, topk_ids, blockhist, counts, offsets, rt_gu,
+                               rt_dn, meta, expert_counts_out, st)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark_stage(2, st);
+    if ((launch_scatter(T, E, k, topk_ids, blockhist, offsets, perm, inv, st)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark_stage(3, st);
+    if ((launch_gate_up(bn_gu, gu, ga, static_cast<int>(max_gu < cap ? max_gu : cap), num_sms,
+                            st)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark_stage(4, st);
+    if ((launch_down(bn_dn, dn, gd, static_cast<int>(max_dn < cap ? max_dn : cap), num_sms,
+                         st)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark_stage(5, st);
+    if ((launch_combine(T, H, k, y, topk_w, inv, static_cast<__nv_bfloat16*>(out), st)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark_stage(6, st);
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_set_stage_events(void* const* events, int n_events) {
+    if (n_events == 0 || events == nullptr) {
+        tl_stage_events_on = false;
+        return MOE_OK;
+    }
+    if (n_events != MOE_NUM_STAGES + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i) {
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+        tl_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    tl_stage_events_on = true;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_device_status(const void* workspace, void* cuda_stream) {
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    unsigned flags = 0;
+    if (cudaMemcpy(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return flags ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}

@@ -1,0 +1,592 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA, persistent and warp-specialised.
+//
+// Both GEMMs put the weights on the MMA's M side (128 output features per
+// tile, one TMEM lane each) and the tokens of one expert on the N side (up to
+// BN per tile). Decode-sized groups (a few tokens per expert) then cost one
+// pass over the touched expert weights, and the same kernel serves prefill
+// with BN up to 256. Tiles come from a device-built list of (expert, first
+// row) pairs, so empty experts cost nothing and no host synchronisation is
+// needed; the shared expert is one more group appended to the list.
+//
+// gate_up: for the tile's 128 intermediate features f..f+127 of expert e,
+//   G = W_gate_up[e][f.., :] X^T and U = W_gate_up[e][I+f.., :] X^T go to two
+//   TMEM accumulators that share the B operand X (the gathered hidden rows of
+//   the expert's tokens), and the epilogue writes h = silu(G) * U as a bf16
+//   high/low pair (h_hi = bf16(h), h_lo = bf16(h - h_hi)).
+// down: y = W_down[e][f.., :] [h_hi | h_lo]^T, both halves accumulated into
+//   one TMEM accumulator against the same weight tile; fp32 rows of y are
+//   written per (token, slot); the shared expert's rows are scaled by the
+//   per-token gate sigmoid(x . w_g) in the epilogue.
+// Sources: "Add Qwen3.5-35B-A3B (support vision and text input)", Description
+// (stacked 3D expert weights; per-token sigmoid-gated shared expert); the
+// SwiGLU expert FFN is the plain reading of the stacked gate/up layout.
+//
+// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs, warps 2-3 gather hidden rows with cp.async (gate_up only),
+// warps 4-7 drain TMEM in the epilogue (warp w reads TMEM lanes 32*(w%4)..).
+// Every wait on a pipeline barrier gives up after a time limit, sets an error
+// bit in the workspace status word and lets the CTA finish cleanly.
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448;
+
+template <int BN, bool GU>
+struct Cfg {
+    static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;  // 16 KB weight tile
+    static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
+    static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : (A_BYTES + 2 * B_BYTES);
+    static constexpr int STAGES_FIT = (220 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    static constexpr int ACC_COLS = GU ? 2 * BN : BN;  // TMEM columns per accumulator set
+    static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+    static constexpr int TMEM_USED = ACC_COLS * ACC_STAGES;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                     : TMEM_USED <= 64  ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256
+                                                        : 512;
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int ROWTAB_BYTES = GU ? (BN / 8) * 64 * 4 : 0;  // gather row table
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + CTL_BYTES + ROWTAB_BYTES;
+    static constexpr int CHUNK = BN >= 32 ? 32 : 16;  // TMEM columns per epilogue load
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(SMEM <= kSmemLimit, "shared memory budget");
+    static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
+};
+
+struct Ctl {
+    uint64_t full_a[kMaxStages];  // TMA bytes landed
+    uint64_t full_b[kMaxStages];  // gathered rows landed (gate_up)
+    uint64_t empty[kMaxStages];   // MMAs reading the stage completed
+    uint64_t tfull[2];            // accumulator ready for the epilogue
+    uint64_t tempty[2];           // accumulator drained
+    uint64_t drain;               // MMA completion on the abort path
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct Tile {
+    int shared;  // 1: shared-expert tile
+    int e;       // routed expert
+    int m0;      // first row inside the group
+    int n_rows;  // valid token rows in this tile (1..BN)
+    int p0;      // first row in the sorted slot order (routed) or token index (shared)
+    int f;       // 128-row block of output features
+};
+
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(int tile, int routed_tiles, int F, int F_s,
+                                            const GemmArgs& a) {
+    Tile ti;
+    if (tile < routed_tiles) {
+        const int rt = tile / F;
+        ti.f = tile - rt * F;
+        const int2 r = a.rowtiles[rt];
+        ti.shared = 0;
+        ti.e = r.x;
+        ti.m0 = r.y;
+        ti.n_rows = min(BN, a.counts[r.x] - r.y);
+        ti.p0 = a.offsets[r.x] + r.y;
+    } else {
+        const int t2 = tile - routed_tiles;
+        const int rt = t2 / F_s;
+        ti.f = t2 - rt * F_s;
+        ti.shared = 1;
+        ti.e = 0;
+        ti.m0 = rt * BN;
+        ti.n_rows = min(BN, a.T - ti.m0);
+        ti.p0 = ti.m0;
+    }
+    return ti;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned* err, unsigned code) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for phase `parity` of `bar`; false if the CTA is aborting or the wait
+// timed out (which starts the abort).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* err, unsigned code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, err, code);
+}
+
+// Abort-path wait that ignores the abort flag, bounded by the time limit.
+__device__ __noinline__ void wait_bounded(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t* b) { return ptx::smem_u32(b); }
+
+// Common set-up: barriers, TMEM allocation. Returns the TMEM base address.
+template <int BN, bool GU>
+__device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp) {
+    using C = Cfg<BN, GU>;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(bar_addr(&ctl->full_a[s]), 1);
+            ptx::mbar_init(bar_addr(&ctl->full_b[s]), 64);
+            ptx::mbar_init(bar_addr(&ctl->empty[s]), 1);
+        }
+        for (int s = 0; s < C::ACC_STAGES; ++s) {
+            ptx::mbar_init(bar_addr(&ctl->tfull[s]), 1);
+            ptx::mbar_init(bar_addr(&ctl->tempty[s]), 4);
+        }
+        ptx::mbar_init(bar_addr(&ctl->drain), 1);
+        ctl->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    return ctl->tmem_base;
+}
+
+template <int BN, bool GU>
+__device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, int warp) {
+    using C = Cfg<BN, GU>;
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Abort path of the TMA producer: wait (bounded) until the last load armed on
+// every stage has landed, so no copy is in flight when the CTA exits.
+template <int STAGES>
+__device__ __forceinline__ void drain_tma(Ctl* ctl, uint32_t armed, uint32_t parity_bits) {
+    for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) wait_bounded(bar_addr(&ctl->full_a[s]), (parity_bits >> s) & 1u);
+}
+
+// ================================================================ gate_up
+template <int BN>
+__global__ void __launch_bounds__(256, 1)
+gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    using C = Cfg<BN, true>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE_BYTES);
+    int* rowtab = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::CTL_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&maps.w);
+        ptx::prefetch_tmap(&maps.ws);
+    }
+    const uint32_t tmem_base = gemm_setup<BN, true>(ctl, warp);
+
+    const int R = a.meta[META_RT_GU];
+    const int F = (a.I + kGemmBM - 1) / kGemmBM, F_s = (a.I_s + kGemmBM - 1) / kGemmBM;
+    const int routed_tiles = R * F;
+    const int num_tiles = routed_tiles + ((a.T + BN - 1) / BN) * F_s;
+    const int ksteps = a.H / kGemmBK;
+    volatile int* abort_flag = &ctl->abort;
+    unsigned* err = a.err;
+    const unsigned code = ERR_GATE_UP_TIMEOUT;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------------------------- TMA producer
+            const uint64_t pol = ptx::policy_evict_normal();
+            int s = 0;
+            uint32_t ph = 0, armed = 0, parity_bits = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+                const CUtensorMap* tm = ti.shared ? &maps.ws : &maps.w;
+                const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
+                const int row_u = row_g + (ti.shared ? a.I_s : a.I);
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint32_t fb = bar_addr(&ctl->full_a[s]);
+                    ptx::mbar_arrive_expect_tx(fb, 2 * C::A_BYTES);
+                    ptx::tma_load_2d(sa, tm, fb, ks * kGemmBK, row_g, pol);
+                    ptx::tma_load_2d(sa + C::A_BYTES, tm, fb, ks * kGemmBK, row_u, pol);
+                    armed |= 1u << s;
+                    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) drain_tma<C::STAGES>(ctl, armed, parity_bits);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------------------------- MMA issuer
+            int s = 0, as = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+                const int n_mma = max(16, (ti.n_rows + 15) & ~15);
+                const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, n_mma);
+                if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_gate = tmem_base + as * C::ACC_COLS;
+                const uint32_t d_up = d_gate + BN;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code) ||
+                        !wait_bar(bar_addr(&ctl->full_b[s]), ph, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::fence_proxy_async_smem();  // gathered rows were written by cp.async
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint64_t da0 = ptx::smem_desc_sw128(sa);
+                    const uint64_t da1 = ptx::smem_desc_sw128(sa + C::A_BYTES);
+                    const uint64_t db = ptx::smem_desc_sw128(sa + 2 * C::A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+                        const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
+                        // +32 bytes of K per step, in 16-byte descriptor units
+                        ptx::mma_bf16_ss(d_gate, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+                        ptx::mma_bf16_ss(d_up, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+                    }
+                    ptx::mma_commit(bar_addr(&ctl->empty[s]));
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar_addr(&ctl->tfull[as]));
+                if (++as == C::ACC_STAGES) {
+                    as = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) {
+                ptx::mma_commit(bar_addr(&ctl->drain));
+                wait_bounded(bar_addr(&ctl->drain), 0);
+            }
+        }
+    } else if (warp < 4) {  // ------------------------------ row gather (64 threads)
+        const int gl = (warp - 2) * 32 + lane;
+        const int c = gl & 7;          // 16-byte chunk of the 128-byte row
+        const int r_first = gl >> 3;   // rows r_first, r_first + 8, ...
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+            // Token row of each row this thread copies (thread-private table).
+            for (int r = r_first, j = 0; r < ti.n_rows; r += 8, ++j) {
+                const int t = ti.shared ? ti.m0 + r : a.perm[ti.p0 + r] / a.k;
+                rowtab[j * 64 + gl] = t;
+            }
+            for (int ks = 0; ks < ksteps; ++ks) {
+                if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + 2 * C::A_BYTES);
+                for (int r = r_first, j = 0; r < ti.n_rows; r += 8, ++j) {
+                    const __nv_bfloat16* src = a.hidden +
+                                               static_cast<size_t>(rowtab[j * 64 + gl]) * a.H +
+                                               ks * kGemmBK + c * 8;
+                    // 128-byte swizzle: chunk c of row r lands at chunk c ^ (r % 8)
+                    ptx::cp_async_16(sb + r * 128 + ((c ^ (r & 7)) << 4), src);
+                }
+                ptx::cp_async_arrive_noinc(bar_addr(&ctl->full_b[s]));
+                if (++s == C::STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        ptx::cp_async_wait_all();
+    } else {  // -------------------------------------------- epilogue (warps 4-7)
+        const int q = warp & 3;
+        int as = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+            if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
+            ptx::tc_fence_after();
+            const int n_feat = ti.shared ? a.I_s : a.I;
+            const int i = ti.f * kGemmBM + q * 32 + lane;
+            const bool valid_i = i < n_feat;
+            __nv_bfloat16* dhi = ti.shared ? a.hs_hi : a.h_hi;
+            __nv_bfloat16* dlo = ti.shared ? a.hs_lo : a.h_lo;
+            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
+            for (int c0 = 0; c0 < ti.n_rows; c0 += C::CHUNK) {
+                uint32_t g[C::CHUNK], u[C::CHUNK];
+                if constexpr (C::CHUNK == 32) {
+                    ptx::tmem_ld_32x32b_x32(tb + c0, g);
+                    ptx::tmem_ld_32x32b_x32(tb + BN + c0, u);
+                } else {
+                    ptx::tmem_ld_32x32b_x16(tb + c0, g);
+                    ptx::tmem_ld_32x32b_x16(tb + BN + c0, u);
+                }
+                ptx::tmem_ld_wait();
+                if (valid_i) {
+#pragma unroll
+                    for (int n = 0; n < C::CHUNK; ++n) {
+                        if (c0 + n < ti.n_rows) {
+                            const float gv = __uint_as_float(g[n]);
+                            const float uv = __uint_as_float(u[n]);
+                            const float h = gv / (1.f + __expf(-gv)) * uv;
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                            const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+                            const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * n_feat + i;
+                            dhi[o] = hi;
+                            dlo[o] = lo;
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
+            if (++as == C::ACC_STAGES) {
+                as = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+    gemm_teardown<BN, true>(tmem_base, warp);
+}
+
+// =================================================================== down
+template <int BN>
+__global__ void __launch_bounds__(256, 1)
+down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    using C = Cfg<BN, false>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&maps.w);
+        ptx::prefetch_tmap(&maps.ws);
+        ptx::prefetch_tmap(&maps.h_hi);
+        ptx::prefetch_tmap(&maps.h_lo);
+        ptx::prefetch_tmap(&maps.hs_hi);
+        ptx::prefetch_tmap(&maps.hs_lo);
+    }
+    const uint32_t tmem_base = gemm_setup<BN, false>(ctl, warp);
+
+    const int R = a.meta[META_RT_DN];
+    const int F = (a.H + kGemmBM - 1) / kGemmBM;
+    const int routed_tiles = R * F;
+    const int num_tiles = routed_tiles + ((a.T + BN - 1) / BN) * F;
+    volatile int* abort_flag = &ctl->abort;
+    unsigned* err = a.err;
+    const unsigned code = ERR_DOWN_TIMEOUT;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------------------------- TMA producer
+            const uint64_t pol_w = ptx::policy_evict_normal();
+            const uint64_t pol_h = ptx::policy_evict_first();
+            int s = 0;
+            uint32_t ph = 0, armed = 0, parity_bits = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F, a);
+                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
+                const CUtensorMap* thi = ti.shared ? &maps.hs_hi : &maps.h_hi;
+                const CUtensorMap* tlo = ti.shared ? &maps.hs_lo : &maps.h_lo;
+                const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * kGemmBM;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint32_t fb = bar_addr(&ctl->full_a[s]);
+                    ptx::mbar_arrive_expect_tx(fb, C::A_BYTES + 2 * C::B_BYTES);
+                    ptx::tma_load_2d(sa, tw, fb, ks * kGemmBK, row_w, pol_w);
+                    ptx::tma_load_2d(sa + C::A_BYTES, thi, fb, ks * kGemmBK, ti.p0, pol_h);
+                    ptx::tma_load_2d(sa + C::A_BYTES + C::B_BYTES, tlo, fb, ks * kGemmBK, ti.p0,
+                                     pol_h);
+                    armed |= 1u << s;
+                    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) drain_tma<C::STAGES>(ctl, armed, parity_bits);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------------------------- MMA issuer
+            int s = 0, as = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F, a);
+                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const int n_mma = max(16, (ti.n_rows + 15) & ~15);
+                const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, n_mma);
+                if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + as * C::ACC_COLS;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint64_t da = ptx::smem_desc_sw128(sa);
+                    const uint64_t dhi = ptx::smem_desc_sw128(sa + C::A_BYTES);
+                    const uint64_t dlo = ptx::smem_desc_sw128(sa + C::A_BYTES + C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+                        const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
+                        ptx::mma_bf16_ss(d, da + 2 * kk, dhi + 2 * kk, idesc, acc);
+                        ptx::mma_bf16_ss(d, da + 2 * kk, dlo + 2 * kk, idesc, 1u);
+                    }
+                    ptx::mma_commit(bar_addr(&ctl->empty[s]));
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar_addr(&ctl->tfull[as]));
+                if (++as == C::ACC_STAGES) {
+                    as = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) {
+                ptx::mma_commit(bar_addr(&ctl->drain));
+                wait_bounded(bar_addr(&ctl->drain), 0);
+            }
+        }
+    } else if (warp >= 4) {  // ------------------------------ epilogue
+        const int q = warp & 3;
+        int as = 0;
+        uint32_t aph = 0;
+        const size_t shared_row0 = static_cast<size_t>(a.T) * a.k;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F, a);
+            if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
+            ptx::tc_fence_after();
+            const int hf = ti.f * kGemmBM + q * 32 + lane;
+            const bool valid = hf < a.H;
+            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
+            for (int c0 = 0; c0 < ti.n_rows; c0 += C::CHUNK) {
+                uint32_t v[C::CHUNK];
+                if constexpr (C::CHUNK == 32) {
+                    ptx::tmem_ld_32x32b_x32(tb + c0, v);
+                } else {
+                    ptx::tmem_ld_32x32b_x16(tb + c0, v);
+                }
+                ptx::tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int n = 0; n < C::CHUNK; ++n) {
+                        if (c0 + n < ti.n_rows) {
+                            const float val = __uint_as_float(v[n]);
+                            if (!ti.shared) {
+                                a.y[static_cast<size_t>(ti.p0 + c0 + n) * a.H + hf] = val;
+                            } else {
+                                const int t = ti.m0 + c0 + n;
+                                const float gate = 1.f / (1.f + expf(-a.gate_logit[t]));
+                                a.y[(shared_row0 + t) * a.H + hf] = gate * val;
+                            }
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
+            if (++as == C::ACC_STAGES) {
+                as = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+    gemm_teardown<BN, false>(tmem_base, warp);
+}
+
+template <int BN, bool GU>
+cudaError_t launch_bn(const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
+                      cudaStream_t st) {
+    using C = Cfg<BN, GU>;
+    auto kern = GU ? gate_up_kernel<BN> : down_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = max_tiles < num_sms ? max_tiles : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, 256, C::SMEM, st>>>(maps, a);
+    return cudaGetLastError();
+}
+
+template <bool GU>
+cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
+                     cudaStream_t st) {
+    switch (bn) {
+        case 16: return launch_bn<16, GU>(maps, a, max_tiles, num_sms, st);
+        case 32: return launch_bn<32, GU>(maps, a, max_tiles, num_sms, st);
+        case 64: return launch_bn<64, GU>(maps, a, max_tiles, num_sms, st);
+        case 128: return launch_bn<128, GU>(maps, a, max_tiles, num_sms, st);
+        case 256: return launch_bn<256, GU>(maps, a, max_tiles, num_sms, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool gemm_bn_supported(int bn) {
+    return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
+}
+
+cudaError_t launch_gate_up(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
+                           int num_sms, cudaStream_t st) {
+    return dispatch<true>(bn, maps, a, max_tiles, num_sms, st);
+}
+
+cudaError_t launch_down(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
+                        int num_sms, cudaStream_t st) {
+    return dispatch<false>(bn, maps, a, max_tiles, num_sms, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,90 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every entry point
+declared in include/moe.h, and rejects bad arguments on the host before any
+CUDA call (none of these tests touches a GPU)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_ffn_03_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    import mixture_experts_ffn_03_gb300 as moe
+    return moe.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    import mixture_experts_ffn_03_gb300 as moe
+    names = declared_functions()
+    assert set(moe.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size_and_layout():
+    import mixture_experts_ffn_03_gb300 as moe
+    from mixture_experts_ffn_03_gb300.workloads import CONFIGS
+    for cfg in CONFIGS.values():
+        d = moe.make_dims(**cfg.dims())
+        n = moe.workspace_size(d)
+        L = moe.workspace_layout(d)
+        assert n == L.total > 0
+        tk = cfg.T * cfg.k
+        assert L.y + (tk + cfg.T) * cfg.H * 4 <= n
+        offs = [L.topk_ids, L.topk_w, L.gate_logit, L.counts, L.offsets, L.perm, L.inv, L.h_hi,
+                L.h_lo, L.hs_hi, L.hs_lo, L.y]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert moe.workspace_size(moe.make_dims(16, 128, 16, 17, 64, 64, 0)) == 0  # k > E
+
+
+def _call(lib, dims, **kw):
+    import mixture_experts_ffn_03_gb300 as moe
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: the checks below fail first
+    args = dict(hidden=fake, logits=fake, wgu=fake, wd=fake, wsgu=fake, wsd=fake, wg=fake,
+                out=fake, ids=None, w=None, counts=None, ws=fake, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return lib.moe_forward(ctypes.byref(dims), args["hidden"], args["logits"], args["wgu"],
+                           args["wd"], args["wsgu"], args["wsd"], args["wg"], args["out"],
+                           args["ids"], args["w"], args["counts"], args["ws"],
+                           ctypes.c_size_t(args["ws_bytes"]), args["stream"])
+
+
+def test_host_validation(lib):
+    import mixture_experts_ffn_03_gb300 as moe
+    ok = moe.make_dims(16, 128, 16, 4, 64, 64, 0)
+    assert _call(lib, moe.make_dims(16, 128, 16, 0, 64, 64, 0)) == 1      # k < 1
+    assert _call(lib, moe.make_dims(16, 128, 16, 17, 64, 64, 0)) == 1     # k > E
+    assert _call(lib, moe.make_dims(16, 128, 2048, 4, 64, 64, 0)) == 1    # E > 1024
+    assert _call(lib, moe.make_dims(16, 128, 64, 33, 64, 64, 0)) == 1     # k > 32
+    assert _call(lib, moe.make_dims(-1, 128, 16, 4, 64, 64, 0)) == 1      # T < 0
+    assert _call(lib, moe.make_dims(16, 128, 16, 4, 64, 64, 2)) == 1      # score fn
+    assert _call(lib, moe.make_dims(16, 96, 16, 4, 64, 64, 0)) == 2       # H % 64
+    assert _call(lib, moe.make_dims(16, 128, 16, 4, 80, 64, 0)) == 2      # I % 64
+    assert _call(lib, moe.make_dims(16, 128, 16, 4, 64, 32, 0)) == 2      # I_s % 64
+    assert _call(lib, ok, hidden=None) == 1                                # null input
+    assert _call(lib, ok, out=ctypes.c_void_p((1 << 20) + 8)) == 1         # misaligned
+    assert _call(lib, ok, ws=None) == 3                                    # no workspace
+    assert _call(lib, ok, ws_bytes=moe.workspace_size(ok) - 1) == 3        # too small
+    assert _call(lib, ok, ws=ctypes.c_void_p((1 << 20) + 64)) == 3         # ws alignment
+    assert _call(lib, moe.make_dims(0, 128, 16, 4, 64, 64, 0)) == 0        # T = 0: no work
+    for s in range(6):
+        assert moe.status_string(s)

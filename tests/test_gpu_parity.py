@@ -1,0 +1,164 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Bar: expert ids, per-expert counts, offsets and the sorted slot order are
+bit-exact; every checked output element satisfies
+|gpu - oracle| <= 1e-2 |oracle| + 1e-3 RMS(oracle), RMS over the checked rows.
+Small cases check every token; the full-size workloads check every token's
+routing and a sample of tokens' outputs (the oracle evaluates tokens one by one).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_ffn_03_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 1e-2
+RMS_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixture_experts_ffn_03_gb300 as m
+    m.load_library()
+    return m
+
+
+def run_gpu(moe, inp, cfg):
+    dev = torch.device("cuda")
+    x = {n: t.to(dev) for n, t in inp.items()}
+    layer = moe.MoELayer(x["w_gate_up"], x["w_down"], x["ws_gate_up"], x["ws_down"], x["w_g"],
+                         cfg.k, cfg.score_fn)
+    T = cfg.T
+    ids = torch.full((T, cfg.k), -1, dtype=torch.int32, device=dev)
+    w = torch.zeros((T, cfg.k), dtype=torch.float32, device=dev)
+    counts = torch.full((cfg.E,), -1, dtype=torch.int32, device=dev)
+    out = layer.forward(x["hidden"], x["logits"], topk_ids=ids, topk_w=w, counts=counts)
+    st = moe.device_status(layer.workspace(T))
+    assert st == moe.MOE_OK, moe.status_string(st)
+    torch.cuda.synchronize()
+    return layer, out, ids, w, counts
+
+
+def check_routing(moe, layer, cfg, inp, ids, w, counts):
+    o_ids, o_w = oracle.route(inp["logits"], cfg.k, cfg.score_fn)
+    g_ids = ids.cpu().numpy()
+    assert np.array_equal(g_ids, o_ids), f"{(g_ids != o_ids).any(axis=1).sum()} tokens differ"
+    o_counts = oracle.expert_counts(o_ids, cfg.E)
+    assert np.array_equal(counts.cpu().numpy(), o_counts)
+    assert np.max(np.abs(w.cpu().numpy().astype(np.float64) - o_w)) <= 2e-6
+    # Sorted slot order: experts ascending, tokens ascending within an expert.
+    L = moe.workspace_layout(layer.dims(cfg.T))
+    ws = layer.workspace(cfg.T)
+    tk = cfg.T * cfg.k
+
+    def region(off, n, dtype):
+        return ws[off:off + n * torch.tensor([], dtype=dtype).element_size()].view(dtype).cpu().numpy()
+
+    want_perm = np.argsort(o_ids.ravel(), kind="stable")
+    want_inv = np.empty_like(want_perm)
+    want_inv[want_perm] = np.arange(tk)
+    want_off = np.concatenate([[0], np.cumsum(o_counts)])
+    assert np.array_equal(region(L.offsets, cfg.E + 1, torch.int32), want_off)
+    assert np.array_equal(region(L.perm, tk, torch.int32), want_perm)
+    assert np.array_equal(region(L.inv, tk, torch.int32), want_inv)
+    return o_ids
+
+
+def check_output(out, ref, label):
+    g = out.float().cpu().numpy().astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    err = np.abs(g - ref)
+    bound = REL_TOL * np.abs(ref) + RMS_TOL * rms
+    bad = err > bound
+    worst = float(np.max(err / bound)) if err.size else 0.0
+    assert not bad.any(), (f"{label}: {int(bad.sum())} of {bad.size} elements outside tolerance, "
+                           f"worst err/bound {worst:.3f}")
+    return worst
+
+
+def sample_tokens(T, n, seed=0):
+    if T <= n:
+        return np.arange(T)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
+    return np.unique(np.concatenate([[0, T - 1], mid]))
+
+
+def run_case(moe, cfg, inp, n_check=None):
+    layer, out, ids, w, counts = run_gpu(moe, inp, cfg)
+    check_routing(moe, layer, cfg, inp, ids, w, counts)
+    toks = np.arange(cfg.T) if n_check is None else sample_tokens(cfg.T, n_check)
+    ref = oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=toks)["out"]
+    return check_output(out[torch.as_tensor(toks, device=out.device)], ref, cfg.name)
+
+
+SMALL = [
+    wl.CONFIGS["tiny"],
+    wl.MoEConfig("ragged", T=37, H=192, E=24, k=5, I=192, I_s=128, score_fn=wl.SIGMOID),
+    wl.MoEConfig("single_token", T=1, H=64, E=8, k=2, I=64, I_s=64, score_fn=wl.SOFTMAX),
+    wl.MoEConfig("k_equals_E", T=20, H=128, E=6, k=6, I=128, I_s=64, score_fn=wl.SOFTMAX),
+    wl.MoEConfig("k1", T=50, H=256, E=16, k=1, I=64, I_s=192, score_fn=wl.SIGMOID),
+    wl.MoEConfig("bn32", T=256, H=256, E=64, k=4, I=128, I_s=128, score_fn=wl.SOFTMAX),
+    wl.MoEConfig("bn64", T=300, H=320, E=48, k=6, I=256, I_s=64, score_fn=wl.SIGMOID),
+    wl.MoEConfig("max_experts", T=40, H=64, E=1024, k=32, I=64, I_s=64, score_fn=wl.SOFTMAX),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_small_cases(moe, cfg):
+    inp = wl.make_inputs(cfg, seed=0)
+    run_case(moe, cfg, inp)
+
+
+def test_tie_rows_bit_exact(moe):
+    cfg = wl.MoEConfig("ties", T=64, H=128, E=32, k=6, I=64, I_s=64, score_fn=wl.SOFTMAX)
+    inp = wl.make_inputs(cfg, seed=1)
+    g = torch.Generator().manual_seed(5)
+    inp["logits"] = torch.randint(-2, 3, (cfg.T, cfg.E), generator=g).float()
+    inp["logits"][0].zero_()        # all-equal row: experts 0..k-1
+    inp["logits"][1, 3] = -0.0      # -0 ties with +0
+    run_case(moe, cfg, inp)
+
+
+def test_all_tokens_on_one_expert_and_empty_experts(moe):
+    cfg = wl.MoEConfig("hot", T=300, H=128, E=32, k=3, I=128, I_s=64, score_fn=wl.SOFTMAX)
+    inp = wl.make_inputs(cfg, seed=2)
+    inp["logits"][:, 7] += 50.0
+    inp["logits"][:, 20:] -= 50.0   # experts 20..31 receive nothing
+    run_case(moe, cfg, inp)
+
+
+def test_zero_tokens(moe):
+    cfg = wl.MoEConfig("empty", T=0, H=128, E=16, k=4, I=64, I_s=64, score_fn=wl.SOFTMAX)
+    inp = wl.make_inputs(wl.MoEConfig("w", T=1, H=128, E=16, k=4, I=64, I_s=64,
+                                      score_fn=wl.SOFTMAX), seed=0)
+    dev = torch.device("cuda")
+    x = {n: t.to(dev) for n, t in inp.items()}
+    layer = moe.MoELayer(x["w_gate_up"], x["w_down"], x["ws_gate_up"], x["ws_down"], x["w_g"],
+                         cfg.k, cfg.score_fn)
+    out = layer.forward(x["hidden"][:0], x["logits"][:0])
+    torch.cuda.synchronize()
+    assert out.shape == (0, 128)
+
+
+def test_deterministic_repeat(moe):
+    cfg = wl.CONFIGS["tiny"].with_tokens(200)
+    inp = wl.make_inputs(cfg, seed=4)
+    _, a, *_ = run_gpu(moe, inp, cfg)
+    _, b, *_ = run_gpu(moe, inp, cfg)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", 48), ("wide", 24),
+                                          ("skewed", 48)])
+def test_full_size_workloads(moe, name, n_check):
+    cfg = wl.CONFIGS[name]
+    inp = wl.make_inputs(cfg, seed=0, device="cuda")
+    run_case(moe, cfg, inp, n_check)
