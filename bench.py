@@ -154,26 +154,26 @@ def run_reference(args, cfg):
     from mixture_experts_ffn_03_gb300 import workloads as wl
     inp = wl.make_inputs(cfg, seed=0)
     threads = oracle.default_threads()
-    # Size the per-step token sample for about 1-3 s of oracle work per step.
-    probe = oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=np.arange(min(cfg.T, threads)),
-                               n_threads=threads)
-    t0 = time.perf_counter()
-    oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=np.arange(min(cfg.T, threads)),
-                       n_threads=threads)
-    per_batch = time.perf_counter() - t0
-    n_tok = int(max(threads, min(cfg.T, threads * max(1, int(2.0 / max(per_batch, 1e-3))))))
-    toks = np.arange(n_tok) % cfg.T
+    # Size the per-step token sample so that the whole timed run takes about
+    # a minute (at most ~2 s per step), at least one token per thread.
+    batch = np.arange(min(cfg.T, threads))
     for _ in range(args.warmup):
-        oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=toks[:threads], n_threads=threads)
+        oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=batch, n_threads=threads)
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=batch, n_threads=threads)
+    per_batch = time.perf_counter() - t0
+    budget = min(2.0, 60.0 / max(args.steps, 1))
+    n_tok = int(max(len(batch), len(batch) * int(budget / max(per_batch, 1e-3))))
+    toks = np.arange(n_tok) % cfg.T
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
         oracle.moe_forward(inp, cfg.k, cfg.score_fn, tokens=toks, n_threads=threads)
         times.append(time.perf_counter() - t0)
-    del probe
     total = sum(times)
     value = n_tok * len(times) / total
-    sample = f"{n_tok} of {cfg.T} tokens per step, fp64, all routed + shared experts"
+    sample = (f"{n_tok} token evaluations per step (token index mod {cfg.T}), fp64, all routed "
+              f"+ shared experts, {threads} OpenMP threads")
     line = dict(impl="reference", metric="MoE-layer tokens/s", value=value, unit="tokens/s",
                 n_gpus=world, steps=args.steps, warmup=args.warmup,
                 ms_per_step=1e3 * total / len(times), higher_is_better=True, scaling="weak",
@@ -258,6 +258,12 @@ def main():
                for _ in range(K)]
     stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
                 for _ in range(K)]
+    # torch creates CUDA events lazily; record each once so the handles exist.
+    with torch.cuda.stream(stream):
+        for evs in stage_ev:
+            for e in evs:
+                e.record(stream)
+    torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index)
     if dist is not None:
         dist.barrier()
