@@ -55,8 +55,9 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 2,   /* H, I or I_s not a multiple of 64 */
     MOE_ERR_WORKSPACE = 3,     /* workspace null or smaller than moe_workspace_size() */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
-    MOE_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up waiting on an internal pipeline
-                                  barrier and returned early; outputs are invalid */
+    MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up waiting on an internal pipeline
+                                   barrier and returned early; outputs are invalid */
+    MOE_ERR_CAPACITY = 6        /* sizes exceed the fixed scratch of moe_expert_counts_static */
 } moe_status;
 
 /* Problem sizes. T tokens, hidden size H, E routed experts, top-k, expert
@@ -141,6 +142,35 @@ moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layou
  * (n_events = 0) to stop. The library does not own the events. Returns
  * MOE_ERR_INVALID_ARG unless n_events is 0 or MOE_NUM_STAGES + 1. */
 moe_status moe_set_stage_events(void* const* events, int n_events);
+
+/*
+ * Allocation-free expert histogram. The pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory,
+ * for example a plugin behind a fixed interface that receives only its
+ * inputs and outputs and has nowhere to keep a workspace, or a
+ * latency-critical caller whose device memory is fully pre-reserved and
+ * which must not call cudaMalloc (an allocation can synchronise the device).
+ *
+ * Computes, from a table of selected experts topk_ids [T, k] (int32, device),
+ * counts_out [E] (tokens per expert; ids outside [0, E) are not counted) and,
+ * if offsets_out is not NULL, offsets_out [E + 1] (exclusive prefix sum of
+ * the counts). Same values as moe_forward's expert_counts_out and its
+ * workspace offsets for the same routing.
+ *
+ * Scratch lives in a fixed device array inside the library of
+ * MOE_STATIC_HIST_WORDS int32 words (1 MiB) plus a 256-byte header; every
+ * GPU that loads the library holds it until the process exits. Sizes with
+ * ceil(T / 256) * E > MOE_STATIC_HIST_WORDS return MOE_ERR_CAPACITY (for
+ * E = 256: T <= 262144). The call allocates no memory and calls no
+ * allocating library routine. The first call on each device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture. All calls share the array: calls that overlap
+ * on the GPU race and give wrong counts. Enqueued on cuda_stream without a
+ * host synchronisation.
+ */
+#define MOE_STATIC_HIST_WORDS (1 << 18)
+moe_status moe_expert_counts_static(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                                    int32_t* counts_out, int32_t* offsets_out, void* cuda_stream);
 
 #ifdef __cplusplus
 }

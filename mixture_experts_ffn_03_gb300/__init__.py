@@ -18,7 +18,8 @@ SIGMOID = 1
 
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
-                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT"}
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
+                6: "MOE_ERR_CAPACITY"}
 
 EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
             "moe_workspace_layout", "moe_set_stage_events"]

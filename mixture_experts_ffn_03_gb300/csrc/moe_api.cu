@@ -168,6 +168,7 @@ MOE_API const char* moe_status_string(moe_status s) {
         case MOE_ERR_WORKSPACE: return "workspace missing or too small";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+        case MOE_ERR_CAPACITY: return "sizes exceed the fixed static scratch (ceil(T/256)*E > 2^18)";
         default: return "unknown status";
     }
 }
