@@ -61,8 +61,8 @@ Layout layout_of(const moe_dims& d) {
     L.perm = take(tk * 4);
     L.inv = take(tk * 4);
     L.blockhist = take(nb * E * 4);
-    L.rt_gu = take(max_row_tiles(tk, E, 16) * sizeof(int2));
-    L.rt_dn = take(max_row_tiles(tk, E, 16) * sizeof(int2));
+    L.rt_gu = take(max_row_tiles(tk, E, 16) * sizeof(int4));
+    L.rt_dn = take(max_row_tiles(tk, E, 16) * sizeof(int4));
     L.h_hi = take(tk * I * 2);
     L.h_lo = take(tk * I * 2);
     L.hs_hi = take(T * Is * 2);
@@ -207,8 +207,8 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     int* perm = reinterpret_cast<int*>(ws + L.perm);
     int* inv = reinterpret_cast<int*>(ws + L.inv);
     int* blockhist = reinterpret_cast<int*>(ws + L.blockhist);
-    int2* rt_gu = reinterpret_cast<int2*>(ws + L.rt_gu);
-    int2* rt_dn = reinterpret_cast<int2*>(ws + L.rt_dn);
+    int4* rt_gu = reinterpret_cast<int4*>(ws + L.rt_gu);
+    int4* rt_dn = reinterpret_cast<int4*>(ws + L.rt_dn);
     auto* h_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.h_hi);
     auto* h_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.h_lo);
     auto* hs_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_hi);
@@ -259,19 +259,34 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     const size_t max_dn = (tk / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
     const int cap = 1 << 30;
 
-    mark_stage(0, st);
-    if ((launch_route(T, H, E, k, d->score_fn, router_logits,
+    // Status words (error flags, tile counts, completion ticket) start at zero.
+    if (cudaMemsetAsync(meta, 0, META_WORDS * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (route_small_fits(T, E, k)) {
+        // Routing and the whole permute in one launch; stages 1 and 2 are empty.
+        mark_stage(0, st);
+        if ((launch_route_permute(T, H, E, k, d->score_fn, bn_gu, bn_dn, router_logits,
+                                  static_cast<const __nv_bfloat16*>(hidden),
+                                  static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w,
+                                  gate_logit, counts, offsets, perm, inv, rt_gu, rt_dn, meta,
+                                  topk_ids_out, topk_w_out, expert_counts_out, st)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark_stage(1, st);
+        mark_stage(2, st);
+    } else {
+        mark_stage(0, st);
+        if ((launch_route(T, H, E, k, d->score_fn, router_logits,
                           static_cast<const __nv_bfloat16*>(hidden),
                           static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w, gate_logit,
-                          topk_ids_out, topk_w_out, meta, st)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    mark_stage(1, st);
-    if ((launch_count_scan(T, E, k, bn_gu, bn_dn, topk_ids, blockhist, counts, offsets, rt_gu,
+                          topk_ids_out, topk_w_out, st)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark_stage(1, st);
+        if ((launch_count_scan(T, E, k, bn_gu, bn_dn, topk_ids, blockhist, counts, offsets, rt_gu,
                                rt_dn, meta, expert_counts_out, st)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    mark_stage(2, st);
-    if ((launch_scatter(T, E, k, topk_ids, blockhist, offsets, perm, inv, st)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+            return MOE_ERR_CUDA;
+        mark_stage(2, st);
+        if ((launch_scatter(T, E, k, topk_ids, blockhist, offsets, perm, inv, st)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     mark_stage(3, st);
     if ((launch_gate_up(bn_gu, gu, ga, static_cast<int>(max_gu < cap ? max_gu : cap), num_sms,
                             st)) != cudaSuccess)

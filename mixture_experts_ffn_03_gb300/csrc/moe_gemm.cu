@@ -53,8 +53,7 @@ struct Cfg {
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
     static constexpr int CTL_BYTES = 1024;
-    static constexpr int ROWTAB_BYTES = GU ? (BN / 8) * 64 * 4 : 0;  // gather row table
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + CTL_BYTES + ROWTAB_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + CTL_BYTES;
     static constexpr int CHUNK = BN >= 32 ? 32 : 16;  // TMEM columns per epilogue load
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
@@ -88,12 +87,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, int routed_tiles, int F, i
     if (tile < routed_tiles) {
         const int rt = tile / F;
         ti.f = tile - rt * F;
-        const int2 r = a.rowtiles[rt];
+        const int4 r = a.rowtiles[rt];
         ti.shared = 0;
         ti.e = r.x;
         ti.m0 = r.y;
-        ti.n_rows = min(BN, a.counts[r.x] - r.y);
-        ti.p0 = a.offsets[r.x] + r.y;
+        ti.n_rows = r.z;
+        ti.p0 = r.w;
     } else {
         const int t2 = tile - routed_tiles;
         const int rt = t2 / F_s;
@@ -197,13 +196,14 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE_BYTES);
-    int* rowtab = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::CTL_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
     }
     const uint32_t tmem_base = gemm_setup<BN, true>(ctl, warp);
+    ptx::griddep_wait();  // routing, tile lists and the slot order come from earlier kernels
 
     const int R = a.meta[META_RT_GU];
     const int F = (a.I + kGemmBM - 1) / kGemmBM, F_s = (a.I_s + kGemmBM - 1) / kGemmBM;
@@ -220,8 +220,11 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
             bool ok = true;
+            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+                if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
                 const CUtensorMap* tm = ti.shared ? &maps.ws : &maps.w;
                 const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
                 const int row_u = row_g + (ti.shared ? a.I_s : a.I);
@@ -250,8 +253,11 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0, as = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
+            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+                if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
                 const int n_mma = max(16, (ti.n_rows + 15) & ~15);
                 const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, n_mma);
                 if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
@@ -299,31 +305,43 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             }
         }
     } else if (warp < 4) {  // ------------------------------ row gather (64 threads)
+        // Thread gl copies 16-byte chunk c of rows r_first, r_first + 8, ...;
+        // with the 128-byte swizzle that chunk lands at position c ^ r_first.
+        constexpr int RPT = BN / 8;  // rows per thread at most
         const int gl = (warp - 2) * 32 + lane;
-        const int c = gl & 7;          // 16-byte chunk of the 128-byte row
-        const int r_first = gl >> 3;   // rows r_first, r_first + 8, ...
+        const int c = gl & 7;
+        const int r_first = gl >> 3;
+        const uint32_t swz = static_cast<uint32_t>((c ^ r_first) << 4);
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
+        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
-            // Token row of each row this thread copies (thread-private table).
-            for (int r = r_first, j = 0; r < ti.n_rows; r += 8, ++j) {
-                const int t = ti.shared ? ti.m0 + r : a.perm[ti.p0 + r] / a.k;
-                rowtab[j * 64 + gl] = t;
+            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+            if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+            uint32_t trow[RPT];  // token (hidden row) of each row this thread copies
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) {
+                const int r = r_first + 8 * j;
+                uint32_t t = 0;
+                if (r < ti.n_rows) t = ti.shared ? ti.m0 + r : a.perm[ti.p0 + r] / a.k;
+                trow[j] = t;
             }
+            const __nv_bfloat16* col = a.hidden + c * 8;
             for (int ks = 0; ks < ksteps; ++ks) {
                 if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + 2 * C::A_BYTES);
-                for (int r = r_first, j = 0; r < ti.n_rows; r += 8, ++j) {
-                    const __nv_bfloat16* src = a.hidden +
-                                               static_cast<size_t>(rowtab[j * 64 + gl]) * a.H +
-                                               ks * kGemmBK + c * 8;
-                    // 128-byte swizzle: chunk c of row r lands at chunk c ^ (r % 8)
-                    ptx::cp_async_16(sb + r * 128 + ((c ^ (r & 7)) << 4), src);
+                const __nv_bfloat16* src = col + ks * kGemmBK;
+#pragma unroll
+                for (int j = 0; j < RPT; ++j) {
+                    const int r = r_first + 8 * j;
+                    if (r < ti.n_rows)
+                        ptx::cp_async_16(sb + r * 128 + swz,
+                                         src + static_cast<size_t>(trow[j]) * a.H);
                 }
                 ptx::cp_async_arrive_noinc(bar_addr(&ctl->full_b[s]));
                 if (++s == C::STAGES) {
@@ -337,8 +355,11 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         const int q = warp & 3;
         int as = 0;
         uint32_t aph = 0;
+        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F_s, a);
+            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+            if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int n_feat = ti.shared ? a.I_s : a.I;
@@ -395,6 +416,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                                                ~static_cast<uintptr_t>(1023));
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
@@ -404,6 +426,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.hs_lo);
     }
     const uint32_t tmem_base = gemm_setup<BN, false>(ctl, warp);
+    ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
 
     const int R = a.meta[META_RT_DN];
     const int F = (a.H + kGemmBM - 1) / kGemmBM;
@@ -416,12 +439,15 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     if (warp == 0) {
         if (lane == 0) {  // ---------------------------------- TMA producer
             const uint64_t pol_w = ptx::policy_evict_normal();
-            const uint64_t pol_h = ptx::policy_evict_first();
+            const uint64_t pol_h = ptx::policy_evict_last();  // h rows are re-read per feature block
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
             bool ok = true;
+            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F, a);
+                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+                if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
                 const CUtensorMap* thi = ti.shared ? &maps.hs_hi : &maps.h_hi;
@@ -454,8 +480,11 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0, as = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
+            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F, a);
+                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+                if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const int n_mma = max(16, (ti.n_rows + 15) & ~15);
                 const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, n_mma);
@@ -504,8 +533,11 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         int as = 0;
         uint32_t aph = 0;
         const size_t shared_row0 = static_cast<size_t>(a.T) * a.k;
+        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = decode_tile<BN>(tile, routed_tiles, F, F, a);
+            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+            if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int hf = ti.f * kGemmBM + q * 32 + lane;
@@ -556,8 +588,7 @@ cudaError_t launch_bn(const GemmMaps& maps, const GemmArgs& a, int max_tiles, in
     if (e != cudaSuccess) return e;
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, 256, C::SMEM, st>>>(maps, a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(256), C::SMEM, st, true, maps, a);
 }
 
 template <bool GU>

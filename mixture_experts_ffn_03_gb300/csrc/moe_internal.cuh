@@ -5,8 +5,29 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace moe {
+
+// Launch `kern` on `st`; with `pdl`, as a programmatic dependent launch so its
+// CTAs can be scheduled (and run their set-up) while the previous kernel in
+// the stream drains. Kernels launched this way call griddep_wait() before
+// reading anything the previous kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Device status word bits (workspace status block, word 0).
 enum : unsigned {
@@ -24,18 +45,26 @@ enum : int {
 };
 
 constexpr int kRouteWarps = 8;          // tokens per route block (one warp each)
+constexpr int kSmallSlots = 2048;       // T*k up to which the routing launch also permutes
 constexpr int kCountTokens = 256;       // tokens per histogram block
 constexpr int kGemmBM = 128;            // weight rows (output features) per tile
 constexpr int kGemmBK = 64;             // K elements per pipeline stage
 
 // Routing, histogram/scan, scatter and combine (moe_route.cu).
+bool route_small_fits(int T, int E, int k);
+cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                                 const float* logits, const __nv_bfloat16* hidden,
+                                 const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
+                                 float* gate_logit, int* counts, int* offsets, int* perm,
+                                 int* inv, int4* rt_gu, int4* rt_dn, int* meta, int* ids_out,
+                                 float* w_out, int* counts_out, cudaStream_t st);
 cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const float* logits,
                          const __nv_bfloat16* hidden, const __nv_bfloat16* w_g, int* topk_ids,
-                         float* topk_w, float* gate_logit, int* ids_out, float* w_out, int* meta,
+                         float* topk_w, float* gate_logit, int* ids_out, float* w_out,
                          cudaStream_t st);
 cudaError_t launch_count_scan(int T, int E, int k, int bn_gu, int bn_dn, const int* topk_ids,
-                              int* blockhist, int* counts, int* offsets, int2* rt_gu,
-                              int2* rt_dn, int* meta, int* counts_out, cudaStream_t st);
+                              int* blockhist, int* counts, int* offsets, int4* rt_gu,
+                              int4* rt_dn, int* meta, int* counts_out, cudaStream_t st);
 cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
                            const int* offsets, int* perm, int* inv, cudaStream_t st);
 cudaError_t launch_combine(int T, int H, int k, const float* y, const float* topk_w,
@@ -48,7 +77,7 @@ struct GemmArgs {
     const int* perm;
     const int* counts;
     const int* offsets;
-    const int2* rowtiles;   // routed row tiles (expert, first row) of this GEMM
+    const int4* rowtiles;   // routed row tiles {expert, first row, rows, sorted position}
     const int* meta;
     const float* gate_logit;
     __nv_bfloat16* h_hi;

@@ -1,20 +1,27 @@
 // Routing, per-expert token lists and the final combine.
 //
-//   route       one warp per token: score, top-k (ties to the lower expert
-//               index), renormalisation, and the shared-expert gate logit
-//               x . w_g. Router in fp32, softmax or sigmoid score, normalised
-//               top-k affinities: "Add Qwen3.5-35B-A3B (support vision and
-//               text input)", Model Information and Additional Information.
-//   count_scan  per-block expert histograms; the last block to finish turns
-//               them into counts, exclusive offsets and the row-tile lists of
-//               both grouped GEMMs.
-//   scatter     stable scatter of (token, slot) pairs into expert-sorted
-//               order: tokens ascending within each expert.
+//   routing     per token: score, top-k (ties to the lower expert index),
+//               renormalisation, and the shared-expert gate logit x . w_g.
+//               Router in fp32, softmax or sigmoid score, normalised top-k
+//               affinities: "Add Qwen3.5-35B-A3B (support vision and text
+//               input)", Model Information and Additional Information.
+//   permute     per-expert counts, exclusive offsets, the stable expert-sorted
+//               order of (token, slot) pairs (tokens ascending within an
+//               expert), its inverse, and the row-tile lists of both grouped
+//               GEMMs. Each row tile is {expert, first row, rows, first
+//               sorted position}.
 //   combine     out_t = bf16( sum_j w_tj y[inv(t,j)] + y_shared[t] ), summed
 //               in fp32 in slot order, one rounding; gather-based, no atomics.
 //               The expert output of "[RFC] Experimental Qwen3.5 MoE AFD
 //               support: CUDA correctness baseline", Proposed plugin boundary.
+//
+// Routing runs one warp per token. Batches with T*k <= kSmallSlots then
+// permute inside the same launch: the last CTA to finish routing (a completion
+// ticket) builds the whole sorted order (route_permute_kernel). Larger batches
+// use route_kernel, count_scan_kernel (per-block histograms; the last block
+// scans) and scatter_kernel.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -28,55 +35,56 @@ __device__ __forceinline__ uint32_t rank_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Logit value of a key (inverse of rank_key on canonical values).
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
 // One 64-bit code per (logit, expert): larger code ranks first; for equal
-// logits the lower expert index has the larger code. Codes are distinct.
+// logits the lower expert index has the larger code. Codes are distinct and
+// nonzero for e < 2^32 - 1.
 __device__ __forceinline__ uint64_t rank_code(float v, int e) {
     return (static_cast<uint64_t>(rank_key(v)) << 32) |
            static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
 
-__global__ void __launch_bounds__(kRouteWarps * 32)
-route_kernel(int T, int H, int E, int k, int score_fn, const float* __restrict__ logits,
-             const __nv_bfloat16* __restrict__ hidden, const __nv_bfloat16* __restrict__ w_g,
-             int* __restrict__ topk_ids, float* __restrict__ topk_w,
-             float* __restrict__ gate_logit, int* __restrict__ ids_out,
-             float* __restrict__ w_out, int* __restrict__ meta) {
-    extern __shared__ float s_rows[];  // [kRouteWarps][E]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        meta[META_ERR] = 0;
-        meta[META_TICKET] = 0;
-    }
-    const int t = blockIdx.x * kRouteWarps + warp;
-    if (t >= T) return;
-    float* row = s_rows + warp * E;
+// Routing of token t by one warp; lane i holds experts i, i+32, ... (EPL of
+// them, E <= 32*EPL). Each round takes the warp-wide best of the lanes'
+// current bests; only the lane that supplied it looks for its next best.
+// Lane j < k returns the j-th selected expert and its renormalised weight.
+template <int EPL>
+__device__ __forceinline__ void route_token(int t, int E, int k, int score_fn,
+                                            const float* __restrict__ logits, int lane,
+                                            int& my_e, float& my_w) {
     const float* lg = logits + static_cast<size_t>(t) * E;
-    for (int e = lane; e < E; e += 32) row[e] = lg[e];
-    __syncwarp();
-
-    // Top-k: round j takes the best code strictly below the previous pick.
-    uint64_t prev = ~0ull;
-    float my_v = 0.f;
-    int my_e = 0;
+    uint64_t c[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        c[i] = e < E ? rank_code(lg[e], e) : 0ull;
+    }
+    uint64_t lane_best = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) lane_best = c[i] > lane_best ? c[i] : lane_best;
+    uint64_t mine = 0;
     for (int j = 0; j < k; ++j) {
-        uint64_t best = 0;
-        for (int e = lane; e < E; e += 32) {
-            const uint64_t c = rank_code(row[e], e);
-            if (c < prev && c > best) best = c;
-        }
+        uint64_t best = lane_best;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
             best = other > best ? other : best;
         }
-        prev = best;
-        const int e_sel = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
-        if (lane == j) {
-            my_e = e_sel;
-            my_v = row[e_sel];
+        if (lane == j) mine = best;
+        if (lane_best == best) {
+            uint64_t nb = 0;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (c[i] < best && c[i] > nb) nb = c[i];
+            lane_best = nb;
         }
     }
-
+    my_e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
+    const float my_v = key_value(static_cast<uint32_t>(mine >> 32));
     // Renormalised scores of the selected experts. For softmax the full
     // partition function cancels in the renormalisation, leaving a softmax
     // over the selected logits (shifted by the largest one).
@@ -90,19 +98,17 @@ route_kernel(int T, int H, int E, int k, int score_fn, const float* __restrict__
     float sum = s;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane < k) {
-        const float w = s / sum;
-        const size_t o = static_cast<size_t>(t) * k + lane;
-        topk_ids[o] = my_e;
-        topk_w[o] = w;
-        if (ids_out) ids_out[o] = my_e;
-        if (w_out) w_out[o] = w;
-    }
+    my_w = s / sum;
+}
 
-    // Shared-expert gate logit z_t = x_t . w_g, fp32 accumulation.
+// Shared-expert gate logit z_t = x_t . w_g, fp32 accumulation, by one warp.
+__device__ __forceinline__ float gate_logit_of(int t, int H,
+                                               const __nv_bfloat16* __restrict__ hidden,
+                                               const __nv_bfloat16* __restrict__ w_g, int lane) {
     const uint4* xr = reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H);
     const uint4* gr = reinterpret_cast<const uint4*>(w_g);
     float acc = 0.f;
+#pragma unroll 8
     for (int c = lane; c < H / 8; c += 32) {
         const uint4 a = xr[c], b = gr[c];
         const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -117,11 +123,13 @@ route_kernel(int T, int H, int E, int k, int score_fn, const float* __restrict__
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == 0) gate_logit[t] = acc;
+    return acc;
 }
 
-// Exclusive scan of one int per thread over a 256-thread block.
-__device__ int block_excl_scan_256(int v, int* s_warp, int* total) {
+// Exclusive scan of one int per thread over a block of NW warps; *total gets
+// the block sum. Contains __syncthreads: every thread must call it.
+template <int NW>
+__device__ int block_excl_scan(int v, int* s_warp, int* total) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int incl = v;
 #pragma unroll
@@ -134,7 +142,7 @@ __device__ int block_excl_scan_256(int v, int* s_warp, int* total) {
     __syncthreads();
     int base = 0, tot = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
         const int x = s_warp[w];
         if (w < warp) base += x;
         tot += x;
@@ -143,17 +151,181 @@ __device__ int block_excl_scan_256(int v, int* s_warp, int* total) {
     return base + incl - v;
 }
 
+// Row tiles of one expert: {expert, first row, rows, first sorted position}.
+__device__ __forceinline__ void write_row_tiles(int4* rt, int pos, int e, int n_e, int off_e,
+                                                int bn) {
+    for (int m0 = 0; m0 < n_e; m0 += bn)
+        rt[pos++] = make_int4(e, m0, min(bn, n_e - m0), off_e + m0);
+}
+
+// Ordered (stable) scatter of the slots [a0, a1) by one warp; `running[e]` is
+// the next free sorted position of expert e. Equal experts inside a 32-slot
+// chunk are ranked by lane, so slot order (token order) is kept.
+__device__ __forceinline__ void ordered_scatter(const int* ids, long a0, long a1, int* running,
+                                                int* __restrict__ perm, int* __restrict__ inv,
+                                                int lane) {
+    for (long base = a0; base < a1; base += 32) {
+        const long a = base + lane;
+        const int e = a < a1 ? ids[a] : -1;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int pos = 0;
+        if (e >= 0) pos = running[e] + rank;
+        __syncwarp();
+        if (e >= 0 && (peers >> lane) == 1u) running[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            perm[pos] = static_cast<int>(a);
+            inv[a] = pos;
+        }
+    }
+}
+
+// Routing of one token per warp; writes ids, weights and the gate logit.
+template <int EPL>
+__device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int score_fn,
+                                                const float* __restrict__ logits,
+                                                const __nv_bfloat16* __restrict__ hidden,
+                                                const __nv_bfloat16* __restrict__ w_g,
+                                                int* __restrict__ topk_ids,
+                                                float* __restrict__ topk_w,
+                                                float* __restrict__ gate_logit,
+                                                int* __restrict__ ids_out,
+                                                float* __restrict__ w_out, int lane) {
+    const float z = gate_logit_of(t, H, hidden, w_g, lane);
+    if (lane == 0) gate_logit[t] = z;
+    int my_e;
+    float my_w;
+    route_token<EPL>(t, E, k, score_fn, logits, lane, my_e, my_w);
+    if (lane < k) {
+        const size_t o = static_cast<size_t>(t) * k + lane;
+        topk_ids[o] = my_e;
+        topk_w[o] = my_w;
+        if (ids_out) ids_out[o] = my_e;
+        if (w_out) w_out[o] = my_w;
+    }
+}
+
+// ------------------------------------------------------------ small batches
+// Routing (a warp per token) plus, in the last CTA to finish, the complete
+// permute of all T*k <= kSmallSlots slots.
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                     const float* __restrict__ logits, const __nv_bfloat16* __restrict__ hidden,
+                     const __nv_bfloat16* __restrict__ w_g, int* __restrict__ topk_ids,
+                     float* __restrict__ topk_w, float* __restrict__ gate_logit,
+                     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm,
+                     int* __restrict__ inv, int4* __restrict__ rt_gu, int4* __restrict__ rt_dn,
+                     int* __restrict__ meta, int* __restrict__ ids_out, float* __restrict__ w_out,
+                     int* __restrict__ counts_out) {
+    extern __shared__ int s_dyn[];
+    __shared__ int s_warp[kRouteWarps];
+    __shared__ int s_is_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    ptx::griddep_launch_dependents();
+    const int t = blockIdx.x * kRouteWarps + warp;
+    if (t < T)
+        route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w,
+                             gate_logit, ids_out, w_out, lane);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_is_last = (atomicAdd(&meta[META_TICKET], 1) == static_cast<int>(gridDim.x) - 1);
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+
+    // Last CTA: warp w owns the contiguous slot range [a0_w, a1_w).
+    const int tk = T * k;
+    int* s_ids = s_dyn;              // [T*k]
+    int* s_sub = s_dyn + tk;         // [kRouteWarps][E]: per-warp counts, then bases
+    for (int a = tid; a < tk; a += kRouteWarps * 32) s_ids[a] = __ldcg(&topk_ids[a]);
+    for (int i = tid; i < kRouteWarps * E; i += kRouteWarps * 32) s_sub[i] = 0;
+    __syncthreads();
+    const int chunk = (tk + kRouteWarps - 1) / kRouteWarps;
+    const int a0 = min(tk, warp * chunk), a1 = min(tk, a0 + chunk);
+    for (int a = a0 + lane; a < a1; a += 32) atomicAdd(&s_sub[warp * E + s_ids[a]], 1);
+    __syncthreads();
+    // Thread tid owns experts [tid*ept, tid*ept + ept): totals, then a scan.
+    const int ept = (E + kRouteWarps * 32 - 1) / (kRouteWarps * 32);  // <= 4
+    int local[4] = {0, 0, 0, 0};
+    int mine = 0;
+    for (int r = 0; r < ept; ++r) {
+        const int e = tid * ept + r;
+        if (e >= E) break;
+        int c = 0;
+        for (int w = 0; w < kRouteWarps; ++w) c += s_sub[w * E + e];
+        local[r] = c;
+        mine += c;
+    }
+    int total;
+    const int first_off = block_excl_scan<kRouteWarps>(mine, s_warp, &total);
+    int run = first_off;
+    for (int r = 0; r < ept; ++r) {
+        const int e = tid * ept + r;
+        if (e >= E) break;
+        counts[e] = local[r];
+        offsets[e] = run;
+        if (counts_out) counts_out[e] = local[r];
+        int b = run;  // per-warp bases inside expert e, in warp (= slot) order
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int v = s_sub[w * E + e];
+            s_sub[w * E + e] = b;
+            b += v;
+        }
+        run += local[r];
+    }
+    if (tid == 0) offsets[E] = total;
+    for (int g = 0; g < 2; ++g) {
+        const int bn = g == 0 ? bn_gu : bn_dn;
+        int nt = 0;
+        for (int r = 0; r < ept; ++r) nt += (local[r] + bn - 1) / bn;
+        int tot_tiles;
+        int pos = block_excl_scan<kRouteWarps>(nt, s_warp, &tot_tiles);
+        int off = first_off;
+        for (int r = 0; r < ept; ++r) {
+            const int e = tid * ept + r;
+            if (e >= E) break;
+            write_row_tiles(g == 0 ? rt_gu : rt_dn, pos, e, local[r], off, bn);
+            pos += (local[r] + bn - 1) / bn;
+            off += local[r];
+        }
+        if (tid == 0) meta[g == 0 ? META_RT_GU : META_RT_DN] = tot_tiles;
+    }
+    __syncthreads();
+    ordered_scatter(s_ids, a0, a1, s_sub + warp * E, perm, inv, lane);
+    if (tid == 0) meta[META_TICKET] = 0;
+}
+
+// ------------------------------------------------------------ large batches
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_kernel(int T, int H, int E, int k, int score_fn, const float* __restrict__ logits,
+             const __nv_bfloat16* __restrict__ hidden, const __nv_bfloat16* __restrict__ w_g,
+             int* __restrict__ topk_ids, float* __restrict__ topk_w,
+             float* __restrict__ gate_logit, int* __restrict__ ids_out,
+             float* __restrict__ w_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
+    const int t = blockIdx.x * kRouteWarps + warp;
+    if (t >= T) return;
+    route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w, gate_logit,
+                         ids_out, w_out, lane);
+}
+
 __global__ void __launch_bounds__(256)
 count_scan_kernel(int T, int E, int k, int bn_gu, int bn_dn, const int* __restrict__ topk_ids,
                   int* __restrict__ blockhist, int* __restrict__ counts,
-                  int* __restrict__ offsets, int2* __restrict__ rt_gu, int2* __restrict__ rt_dn,
+                  int* __restrict__ offsets, int4* __restrict__ rt_gu, int4* __restrict__ rt_dn,
                   int* __restrict__ meta, int* __restrict__ counts_out) {
     extern __shared__ int s_hist[];  // [E]
     __shared__ int s_warp[8];
     __shared__ int s_is_last;
     const int tid = threadIdx.x;
+    ptx::griddep_launch_dependents();
     for (int e = tid; e < E; e += 256) s_hist[e] = 0;
     __syncthreads();
+    ptx::griddep_wait();
     const long a0 = static_cast<long>(blockIdx.x) * kCountTokens * k;
     const long a1 = min(static_cast<long>(T) * k, a0 + static_cast<long>(kCountTokens) * k);
     for (long a = a0 + tid; a < a1; a += 256) atomicAdd(&s_hist[topk_ids[a]], 1);
@@ -186,7 +358,8 @@ count_scan_kernel(int T, int E, int k, int bn_gu, int bn_dn, const int* __restri
         mine += c;
     }
     int total;
-    int run = block_excl_scan_256(mine, s_warp, &total);
+    int run = block_excl_scan<8>(mine, s_warp, &total);
+    const int first_off = run;
     for (int r = 0; r < ept; ++r) {
         const int e = tid * ept + r;
         if (e >= E) break;
@@ -197,18 +370,19 @@ count_scan_kernel(int T, int E, int k, int bn_gu, int bn_dn, const int* __restri
     }
     if (tid == 0) offsets[E] = total;
 
-    // Row tiles (expert, first row) of both GEMMs; empty experts give none.
     for (int g = 0; g < 2; ++g) {
         const int bn = g == 0 ? bn_gu : bn_dn;
-        int2* rt = g == 0 ? rt_gu : rt_dn;
         int nt = 0;
         for (int r = 0; r < ept; ++r) nt += (local[r] + bn - 1) / bn;
         int tot_tiles;
-        int pos = block_excl_scan_256(nt, s_warp, &tot_tiles);
+        int pos = block_excl_scan<8>(nt, s_warp, &tot_tiles);
+        int off = first_off;
         for (int r = 0; r < ept; ++r) {
             const int e = tid * ept + r;
             if (e >= E) break;
-            for (int m0 = 0; m0 < local[r]; m0 += bn) rt[pos++] = make_int2(e, m0);
+            write_row_tiles(g == 0 ? rt_gu : rt_dn, pos, e, local[r], off, bn);
+            pos += (local[r] + bn - 1) / bn;
+            off += local[r];
         }
         if (tid == 0) meta[g == 0 ? META_RT_GU : META_RT_DN] = tot_tiles;
     }
@@ -221,8 +395,10 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
                int* __restrict__ perm, int* __restrict__ inv) {
     extern __shared__ int s_sub[];  // [8][E]: per-warp counts, then per-warp bases
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    ptx::griddep_launch_dependents();
     for (int i = tid; i < 8 * E; i += 256) s_sub[i] = 0;
     __syncthreads();
+    ptx::griddep_wait();
     const long t0 = static_cast<long>(blockIdx.x) * kCountTokens + warp * 32;
     const long t1 = min(static_cast<long>(T), t0 + 32);
     const long wa0 = t0 * k, wa1 = t1 > t0 ? t1 * k : wa0;
@@ -238,23 +414,7 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
         }
     }
     __syncthreads();
-    // Ordered pass: chunks of 32 consecutive slots; equal experts inside a
-    // chunk are ranked by lane, so slot order (token order) is kept.
-    for (long base = wa0; base < wa1; base += 32) {
-        const long a = base + lane;
-        const int e = a < wa1 ? topk_ids[a] : -1;
-        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        int pos = 0;
-        if (e >= 0) pos = running[e] + rank;
-        __syncwarp();
-        if (e >= 0 && (peers >> lane) == 1u) running[e] += __popc(peers);
-        __syncwarp();
-        if (e >= 0) {
-            perm[pos] = static_cast<int>(a);
-            inv[a] = pos;
-        }
-    }
+    ordered_scatter(topk_ids, wa0, wa1, running, perm, inv, lane);
 }
 
 __global__ void __launch_bounds__(256)
@@ -262,6 +422,8 @@ combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __
                const int* __restrict__ inv, __nv_bfloat16* __restrict__ out) {
     const int t = blockIdx.x;
     const int h = (blockIdx.y * 256 + threadIdx.x) * 4;
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     if (h >= H) return;
     const size_t tk = static_cast<size_t>(t) * k;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -291,41 +453,79 @@ combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __
 
 }  // namespace
 
+bool route_small_fits(int T, int E, int k) {
+    return static_cast<long>(T) * k <= kSmallSlots && E <= 1024;
+}
+
+namespace {
+int experts_per_lane(int E) {
+    int epl = 1;
+    while (32 * epl < E) epl *= 2;
+    return epl;  // 1 .. 32 for E <= 1024
+}
+}  // namespace
+
+#define MOE_EPL_DISPATCH(EPLV, CALL) \
+    switch (EPLV) {                  \
+        case 1: CALL(1);             \
+        case 2: CALL(2);             \
+        case 4: CALL(4);             \
+        case 8: CALL(8);             \
+        case 16: CALL(16);           \
+        default: CALL(32);           \
+    }
+
+cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                                 const float* logits, const __nv_bfloat16* hidden,
+                                 const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
+                                 float* gate_logit, int* counts, int* offsets, int* perm,
+                                 int* inv, int4* rt_gu, int4* rt_dn, int* meta, int* ids_out,
+                                 float* w_out, int* counts_out, cudaStream_t st) {
+    const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
+    const size_t smem = (static_cast<size_t>(T) * k + static_cast<size_t>(kRouteWarps) * E) *
+                        sizeof(int);
+#define MOE_LAUNCH_RP(N)                                                                        \
+    return launch_kernel(route_permute_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), smem,  \
+                         st, false, T, H, E, k, score_fn, bn_gu, bn_dn, logits, hidden, w_g,    \
+                         topk_ids, topk_w, gate_logit, counts, offsets, perm, inv, rt_gu, rt_dn, \
+                         meta, ids_out, w_out, counts_out)
+    MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_RP)
+#undef MOE_LAUNCH_RP
+}
+
 cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const float* logits,
                          const __nv_bfloat16* hidden, const __nv_bfloat16* w_g, int* topk_ids,
-                         float* topk_w, float* gate_logit, int* ids_out, float* w_out, int* meta,
+                         float* topk_w, float* gate_logit, int* ids_out, float* w_out,
                          cudaStream_t st) {
     const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
-    const size_t smem = static_cast<size_t>(kRouteWarps) * E * sizeof(float);
-    route_kernel<<<blocks, kRouteWarps * 32, smem, st>>>(T, H, E, k, score_fn, logits, hidden,
-                                                          w_g, topk_ids, topk_w, gate_logit,
-                                                          ids_out, w_out, meta);
-    return cudaGetLastError();
+#define MOE_LAUNCH_R(N)                                                                      \
+    return launch_kernel(route_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), 0, st, false, \
+                         T, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w,         \
+                         gate_logit, ids_out, w_out)
+    MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_R)
+#undef MOE_LAUNCH_R
 }
 
 cudaError_t launch_count_scan(int T, int E, int k, int bn_gu, int bn_dn, const int* topk_ids,
-                              int* blockhist, int* counts, int* offsets, int2* rt_gu,
-                              int2* rt_dn, int* meta, int* counts_out, cudaStream_t st) {
+                              int* blockhist, int* counts, int* offsets, int4* rt_gu,
+                              int4* rt_dn, int* meta, int* counts_out, cudaStream_t st) {
     const int blocks = (T + kCountTokens - 1) / kCountTokens;
-    count_scan_kernel<<<blocks, 256, E * sizeof(int), st>>>(T, E, k, bn_gu, bn_dn, topk_ids,
-                                                            blockhist, counts, offsets, rt_gu,
-                                                            rt_dn, meta, counts_out);
-    return cudaGetLastError();
+    return launch_kernel(count_scan_kernel, dim3(blocks), dim3(256), E * sizeof(int), st, true, T,
+                         E, k, bn_gu, bn_dn, topk_ids, blockhist, counts, offsets, rt_gu, rt_dn,
+                         meta, counts_out);
 }
 
 cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
                            const int* offsets, int* perm, int* inv, cudaStream_t st) {
     const int blocks = (T + kCountTokens - 1) / kCountTokens;
-    scatter_kernel<<<blocks, 256, 8 * E * sizeof(int), st>>>(T, E, k, topk_ids, blockhist,
-                                                             offsets, perm, inv);
-    return cudaGetLastError();
+    return launch_kernel(scatter_kernel, dim3(blocks), dim3(256), 8 * E * sizeof(int), st, true, T,
+                         E, k, topk_ids, blockhist, offsets, perm, inv);
 }
 
 cudaError_t launch_combine(int T, int H, int k, const float* y, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st) {
     dim3 grid(T, (H / 4 + 255) / 256);
-    combine_kernel<<<grid, 256, 0, st>>>(T, H, k, y, topk_w, inv, out);
-    return cudaGetLastError();
+    return launch_kernel(combine_kernel, grid, dim3(256), 0, st, true, T, H, k, y, topk_w, inv, out);
 }
 
 }  // namespace moe

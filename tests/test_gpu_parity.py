@@ -108,6 +108,12 @@ SMALL = [
     wl.MoEConfig("bn32", T=256, H=256, E=64, k=4, I=128, I_s=128, score_fn=wl.SOFTMAX),
     wl.MoEConfig("bn64", T=300, H=320, E=48, k=6, I=256, I_s=64, score_fn=wl.SIGMOID),
     wl.MoEConfig("max_experts", T=40, H=64, E=1024, k=32, I=64, I_s=64, score_fn=wl.SOFTMAX),
+    # T*k above the single-CTA routing limit: multi-block route / count / scatter path
+    wl.MoEConfig("multiblock", T=600, H=128, E=64, k=4, I=64, I_s=64, score_fn=wl.SOFTMAX),
+    wl.MoEConfig("multiblock_ragged", T=1100, H=192, E=40, k=2, I=128, I_s=192,
+                 score_fn=wl.SIGMOID),
+    wl.MoEConfig("multiblock_max_experts", T=300, H=64, E=1024, k=10, I=64, I_s=64,
+                 score_fn=wl.SIGMOID),
 ]
 
 
