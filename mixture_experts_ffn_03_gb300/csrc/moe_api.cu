@@ -100,6 +100,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major matrix [outer, inner] of `elem` bytes per element, written by the
+// GEMM epilogues in boxes of kEpiCols x kEpiRows (no swizzle).
+bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t elem,
+                    uint64_t inner, uint64_t outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * elem};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kEpiCols), static_cast<cuuint32_t>(kEpiRows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cache[kMaxDevices] = {0};
     int dev = 0;
@@ -227,6 +242,12 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
               make_map(&dn.ws, ws_down, Is, H, kGemmBM) &&
               make_map(&dn.h_hi, h_hi, I, tk, bn_dn) && make_map(&dn.h_lo, h_lo, I, tk, bn_dn) &&
               make_map(&dn.hs_hi, hs_hi, Is, T, bn_dn) && make_map(&dn.hs_lo, hs_lo, Is, T, bn_dn);
+    const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    ok = ok && make_store_map(&gu.st[0], h_hi, BF16, 2, I, tk) &&
+         make_store_map(&gu.st[1], h_lo, BF16, 2, I, tk) &&
+         make_store_map(&gu.st[2], hs_hi, BF16, 2, Is, T) &&
+         make_store_map(&gu.st[3], hs_lo, BF16, 2, Is, T) &&
+         make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T);
     if (!ok) return MOE_ERR_CUDA;
 
     GemmArgs ga{};

@@ -22,9 +22,11 @@
 // (stacked 3D expert weights; per-token sigmoid-gated shared expert); the
 // SwiGLU expert FFN is the plain reading of the stacked gate/up layout.
 //
-// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues the MMAs, warps 2-3 gather hidden rows with cp.async (gate_up only),
-// warps 4-7 drain TMEM in the epilogue (warp w reads TMEM lanes 32*(w%4)..).
+// warps 4-11 drain TMEM in the epilogue (warp w reads TMEM lanes
+// 32*(w%4)..; two warps per lane quadrant split the columns) and write
+// results through shared memory with TMA stores.
 // Every wait on a pipeline barrier gives up after a time limit, sets an error
 // bit in the workspace status word and lets the CTA finish cleanly.
 #include "moe_internal.cuh"
@@ -37,12 +39,18 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;
 
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kThreads = 128 + kEpiWarps * 32;     // TMA, MMA, 2 gather warps, epilogue
+constexpr int kStgBytes = kEpiRows * kEpiCols * 4;  // one staging buffer (2 KB)
+
 template <int BN, bool GU>
 struct Cfg {
     static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;  // 16 KB weight tile
     static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
     static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : (A_BYTES + 2 * B_BYTES);
-    static constexpr int STAGES_FIT = (220 * 1024) / STAGE_BYTES;
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int EPI_BYTES = kEpiWarps * 2 * kStgBytes;  // double-buffered per warp
+    static constexpr int STAGES_FIT = (kSmemLimit - 2048 - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
     static constexpr int ACC_COLS = GU ? 2 * BN : BN;  // TMEM columns per accumulator set
     static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
@@ -52,9 +60,9 @@ struct Cfg {
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
-    static constexpr int CTL_BYTES = 1024;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + CTL_BYTES;
-    static constexpr int CHUNK = BN >= 32 ? 32 : 16;  // TMEM columns per epilogue load
+    static constexpr int CTL_OFF = STAGES * STAGE_BYTES;
+    static constexpr int EPI_OFF = CTL_OFF + CTL_BYTES;
+    static constexpr int SMEM = 1024 + EPI_OFF + EPI_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
@@ -152,7 +160,7 @@ __device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp) {
         }
         for (int s = 0; s < C::ACC_STAGES; ++s) {
             ptx::mbar_init(bar_addr(&ctl->tfull[s]), 1);
-            ptx::mbar_init(bar_addr(&ctl->tempty[s]), 4);
+            ptx::mbar_init(bar_addr(&ctl->tempty[s]), kEpiWarps);
         }
         ptx::mbar_init(bar_addr(&ctl->drain), 1);
         ctl->abort = 0;
@@ -189,13 +197,13 @@ __device__ __forceinline__ void drain_tma(Ctl* ctl, uint32_t armed, uint32_t par
 
 // ================================================================ gate_up
 template <int BN>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     using C = Cfg<BN, true>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE_BYTES);
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::CTL_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
@@ -351,8 +359,14 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             }
         }
         ptx::cp_async_wait_all();
-    } else {  // -------------------------------------------- epilogue (warps 4-7)
-        const int q = warp & 3;
+    } else {  // ------------------------------------------- epilogue (warps 4-11)
+        // Warp we drains TMEM lanes 32*(warp % 4).. (32 intermediate features)
+        // for the 16-column chunks 16*(we / 4) + 32*j of each tile. Full chunks
+        // are staged in the warp's own shared buffers and written with TMA box
+        // stores; a ragged last chunk is written with plain stores.
+        const int we = warp - 4, q = warp & 3, half = we >> 2;
+        uint8_t* stg = smem + C::EPI_OFF + we * 2 * kStgBytes;
+        uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
         Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
@@ -363,33 +377,51 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int n_feat = ti.shared ? a.I_s : a.I;
-            const int i = ti.f * kGemmBM + q * 32 + lane;
-            const bool valid_i = i < n_feat;
+            const int i0 = ti.f * kGemmBM + q * kEpiCols;  // feature of lane 0
+            const bool warp_valid = i0 < n_feat;            // I, I_s are multiples of 64
+            const CUtensorMap* m_hi = ti.shared ? &maps.st[2] : &maps.st[0];
+            const CUtensorMap* m_lo = ti.shared ? &maps.st[3] : &maps.st[1];
             __nv_bfloat16* dhi = ti.shared ? a.hs_hi : a.h_hi;
             __nv_bfloat16* dlo = ti.shared ? a.hs_lo : a.h_lo;
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
-            for (int c0 = 0; c0 < ti.n_rows; c0 += C::CHUNK) {
-                uint32_t g[C::CHUNK], u[C::CHUNK];
-                if constexpr (C::CHUNK == 32) {
-                    ptx::tmem_ld_32x32b_x32(tb + c0, g);
-                    ptx::tmem_ld_32x32b_x32(tb + BN + c0, u);
-                } else {
-                    ptx::tmem_ld_32x32b_x16(tb + c0, g);
-                    ptx::tmem_ld_32x32b_x16(tb + BN + c0, u);
-                }
+            for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
+                uint32_t g[kEpiRows], u[kEpiRows];
+                ptx::tmem_ld_32x32b_x16(tb + c0, g);
+                ptx::tmem_ld_32x32b_x16(tb + BN + c0, u);
                 ptx::tmem_ld_wait();
-                if (valid_i) {
+                if (!warp_valid) continue;
+                const int rows = min(kEpiRows, ti.n_rows - c0);
+                if (rows == kEpiRows) {
+                    const uint32_t b = nbuf++ & 1u;
+                    __nv_bfloat16* shi = reinterpret_cast<__nv_bfloat16*>(stg + b * kStgBytes);
+                    __nv_bfloat16* slo = shi + kEpiRows * kEpiCols;
+                    if (lane == 0) ptx::bulk_wait_read<1>();  // buffer b no longer being read
+                    __syncwarp();
 #pragma unroll
-                    for (int n = 0; n < C::CHUNK; ++n) {
-                        if (c0 + n < ti.n_rows) {
+                    for (int n = 0; n < kEpiRows; ++n) {
+                        const float gv = __uint_as_float(g[n]);
+                        const float h = gv / (1.f + __expf(-gv)) * __uint_as_float(u[n]);
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                        shi[n * kEpiCols + lane] = hi;
+                        slo[n * kEpiCols + lane] = __float2bfloat16_rn(h - __bfloat162float(hi));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(m_hi, ptx::smem_u32(shi), i0, ti.p0 + c0);
+                        ptx::tma_store_2d(m_lo, ptx::smem_u32(slo), i0, ti.p0 + c0);
+                        ptx::bulk_commit();
+                    }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < kEpiRows; ++n) {
+                        if (n < rows) {
                             const float gv = __uint_as_float(g[n]);
-                            const float uv = __uint_as_float(u[n]);
-                            const float h = gv / (1.f + __expf(-gv)) * uv;
+                            const float h = gv / (1.f + __expf(-gv)) * __uint_as_float(u[n]);
                             const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                            const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
-                            const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * n_feat + i;
+                            const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * n_feat + i0 + lane;
                             dhi[o] = hi;
-                            dlo[o] = lo;
+                            dlo[o] = __float2bfloat16_rn(h - __bfloat162float(hi));
                         }
                     }
                 }
@@ -402,19 +434,20 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 aph ^= 1u;
             }
         }
+        if (lane == 0) ptx::bulk_wait_all();
     }
     gemm_teardown<BN, true>(tmem_base, warp);
 }
 
 // =================================================================== down
 template <int BN>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     using C = Cfg<BN, false>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE_BYTES);
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::CTL_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
@@ -528,11 +561,17 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 wait_bounded(bar_addr(&ctl->drain), 0);
             }
         }
-    } else if (warp >= 4) {  // ------------------------------ epilogue
-        const int q = warp & 3;
+    } else if (warp >= 4) {  // ------------------------------ epilogue (warps 4-11)
+        // Same chunking as gate_up: warp we owns 32 output features (TMEM lanes
+        // 32*(warp % 4)..) and every other 16-column chunk; full chunks go out
+        // as fp32 TMA box stores of y, ragged tails as plain stores. Shared
+        // expert rows are scaled by their token's gate sigmoid(x . w_g).
+        const int we = warp - 4, q = warp & 3, half = we >> 2;
+        uint8_t* stg = smem + C::EPI_OFF + we * 2 * kStgBytes;
+        uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
-        const size_t shared_row0 = static_cast<size_t>(a.T) * a.k;
+        const int shared_row0 = a.T * a.k;
         Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
@@ -540,31 +579,41 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
-            const int hf = ti.f * kGemmBM + q * 32 + lane;
-            const bool valid = hf < a.H;
+            const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
+            const bool warp_valid = h0 < a.H;               // H is a multiple of 64
+            const int row0 = ti.shared ? shared_row0 + ti.m0 : ti.p0;
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
-            for (int c0 = 0; c0 < ti.n_rows; c0 += C::CHUNK) {
-                uint32_t v[C::CHUNK];
-                if constexpr (C::CHUNK == 32) {
-                    ptx::tmem_ld_32x32b_x32(tb + c0, v);
-                } else {
-                    ptx::tmem_ld_32x32b_x16(tb + c0, v);
-                }
+            for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
+                uint32_t v[kEpiRows];
+                ptx::tmem_ld_32x32b_x16(tb + c0, v);
                 ptx::tmem_ld_wait();
-                if (valid) {
+                if (!warp_valid) continue;
+                const int rows = min(kEpiRows, ti.n_rows - c0);
+                float val[kEpiRows];
 #pragma unroll
-                    for (int n = 0; n < C::CHUNK; ++n) {
-                        if (c0 + n < ti.n_rows) {
-                            const float val = __uint_as_float(v[n]);
-                            if (!ti.shared) {
-                                a.y[static_cast<size_t>(ti.p0 + c0 + n) * a.H + hf] = val;
-                            } else {
-                                const int t = ti.m0 + c0 + n;
-                                const float gate = 1.f / (1.f + expf(-a.gate_logit[t]));
-                                a.y[(shared_row0 + t) * a.H + hf] = gate * val;
-                            }
-                        }
+                for (int n = 0; n < kEpiRows; ++n) {
+                    val[n] = __uint_as_float(v[n]);
+                    if (ti.shared && n < rows)
+                        val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
+                }
+                if (rows == kEpiRows) {
+                    const uint32_t b = nbuf++ & 1u;
+                    float* sy = reinterpret_cast<float*>(stg + b * kStgBytes);
+                    if (lane == 0) ptx::bulk_wait_read<1>();  // buffer b no longer being read
+                    __syncwarp();
+#pragma unroll
+                    for (int n = 0; n < kEpiRows; ++n) sy[n * kEpiCols + lane] = val[n];
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&maps.st[0], ptx::smem_u32(sy), h0, row0 + c0);
+                        ptx::bulk_commit();
                     }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < kEpiRows; ++n)
+                        if (n < rows)
+                            a.y[static_cast<size_t>(row0 + c0 + n) * a.H + h0 + lane] = val[n];
                 }
             }
             ptx::tc_fence_before();
@@ -575,6 +624,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 aph ^= 1u;
             }
         }
+        if (lane == 0) ptx::bulk_wait_all();
     }
     gemm_teardown<BN, false>(tmem_base, warp);
 }
@@ -588,7 +638,7 @@ cudaError_t launch_bn(const GemmMaps& maps, const GemmArgs& a, int max_tiles, in
     if (e != cudaSuccess) return e;
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
-    return launch_kernel(kern, dim3(grid), dim3(256), C::SMEM, st, true, maps, a);
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, st, true, maps, a);
 }
 
 template <bool GU>

@@ -49,6 +49,8 @@ constexpr int kSmallSlots = 2048;       // T*k up to which the routing launch al
 constexpr int kCountTokens = 256;       // tokens per histogram block
 constexpr int kGemmBM = 128;            // weight rows (output features) per tile
 constexpr int kGemmBK = 64;             // K elements per pipeline stage
+constexpr int kEpiRows = 16;            // token rows per epilogue store box
+constexpr int kEpiCols = 32;            // output columns per epilogue warp (one TMEM lane each)
 
 // Routing, histogram/scan, scatter and combine (moe_route.cu).
 bool route_small_fits(int T, int E, int k);
@@ -89,12 +91,16 @@ struct GemmArgs {
 };
 
 struct GemmMaps {
+    // Operand loads (128-byte swizzle).
     CUtensorMap w;      // gate_up: W_gate_up as [E*2I, H]; down: W_down as [E*H, I]
     CUtensorMap ws;     // gate_up: Ws_gate_up [2I_s, H]; down: Ws_down [H, I_s]
     CUtensorMap h_hi;   // down only: h_hi [T*k, I]
     CUtensorMap h_lo;
     CUtensorMap hs_hi;  // down only: hs_hi [T, I_s]
     CUtensorMap hs_lo;
+    // Epilogue stores (no swizzle), box of 32 columns x kEpiRows rows:
+    // gate_up: st[0..3] = h_hi, h_lo, hs_hi, hs_lo; down: st[0] = y [T*k + T, H].
+    CUtensorMap st[4];
 };
 
 // Supported tile widths (tokens per tile) of both GEMMs.
