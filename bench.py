@@ -306,6 +306,32 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
 
+    # The same step replayed as a CUDA graph (launch overhead removed).
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            layer.forward(inp["hidden"], inp["logits"], out=out)
+        cap.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            layer.forward(inp["hidden"], inp["logits"], out=out)
+        torch.cuda.synchronize(dev)
+        g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                g_ev[i][0].record(stream)
+                g.replay()
+                g_ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        g_ms = sum(a.elapsed_time(b) for a, b in g_ev) / K
+        graph = dict(ms_per_step=g_ms, value=T / (g_ms / 1e3), unit="tokens/s")
+    except Exception as exc:  # capture unsupported here: report, do not fail the bench
+        graph = dict(error=str(exc)[:200])
+
     # End to end through the public API: pinned host inputs in, output back.
     h_host = inp["hidden"].cpu().pin_memory()
     l_host = inp["logits"].cpu().pin_memory()
@@ -370,7 +396,7 @@ def main():
         down_gbs=work["down_bytes"] / (dn_ms / 1e3) / 1e9,
         e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h),
-        gpu_launches=moe.NUM_STAGES * K, clocks=clocks)
+        gpu_launches=moe.NUM_STAGES * K, clocks=clocks, cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
         inp_cpu = {n: t.cpu() for n, t in inp.items()}
         line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu)

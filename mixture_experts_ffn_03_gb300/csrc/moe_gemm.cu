@@ -400,7 +400,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 #pragma unroll
                     for (int n = 0; n < kEpiRows; ++n) {
                         const float gv = __uint_as_float(g[n]);
-                        const float h = gv / (1.f + __expf(-gv)) * __uint_as_float(u[n]);
+                        const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
                         const __nv_bfloat16 hi = __float2bfloat16_rn(h);
                         shi[n * kEpiCols + lane] = hi;
                         slo[n * kEpiCols + lane] = __float2bfloat16_rn(h - __bfloat162float(hi));
@@ -417,7 +417,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     for (int n = 0; n < kEpiRows; ++n) {
                         if (n < rows) {
                             const float gv = __uint_as_float(g[n]);
-                            const float h = gv / (1.f + __expf(-gv)) * __uint_as_float(u[n]);
+                            const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
                             const __nv_bfloat16 hi = __float2bfloat16_rn(h);
                             const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * n_feat + i0 + lane;
                             dhi[o] = hi;
