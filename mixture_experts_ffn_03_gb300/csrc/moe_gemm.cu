@@ -14,10 +14,11 @@
 //   TMEM accumulators that share the B operand X (the gathered hidden rows of
 //   the expert's tokens), and the epilogue writes h = silu(G) * U as a bf16
 //   high/low pair (h_hi = bf16(h), h_lo = bf16(h - h_hi)).
-// down: y = W_down[e][f.., :] [h_hi | h_lo]^T, both halves accumulated into
-//   one TMEM accumulator against the same weight tile; fp32 rows of y are
-//   written per (token, slot); the shared expert's rows are scaled by the
-//   per-token gate sigmoid(x . w_g) in the epilogue.
+// down: y = W_down[e][f.., :] (h_hi + h_lo)^T: the h_hi and h_lo rows of the
+//   tile are adjacent in shared memory and form the N side of one MMA against
+//   the same weight tile; the epilogue adds the two column blocks and writes
+//   fp32 rows of y per (token, slot); the shared expert's rows are scaled by
+//   the per-token gate sigmoid(x . w_g).
 // Sources: "Add Qwen3.5-35B-A3B (support vision and text input)", Description
 // (stacked 3D expert weights; per-token sigmoid-gated shared expert); the
 // SwiGLU expert FFN is the plain reading of the stacked gate/up layout.
@@ -52,7 +53,7 @@ struct Cfg {
     static constexpr int EPI_BYTES = kEpiWarps * 2 * kStgBytes;  // double-buffered per warp
     static constexpr int STAGES_FIT = (kSmemLimit - 2048 - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
-    static constexpr int ACC_COLS = GU ? 2 * BN : BN;  // TMEM columns per accumulator set
+    static constexpr int ACC_COLS = 2 * BN;  // TMEM columns per accumulator set
     static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
     static constexpr int TMEM_USED = ACC_COLS * ACC_STAGES;
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -66,6 +67,7 @@ struct Cfg {
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
+    static_assert(GU || BN <= 128, "down: h_hi and h_lo rows share one MMA of N <= 256");
 };
 
 struct Ctl {
@@ -519,7 +521,10 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (tile + static_cast<int>(gridDim.x) < num_tiles)
                     nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
-                const int n_mma = max(16, (ti.n_rows + 15) & ~15);
+                // h_lo rows sit right after the BN h_hi rows in shared memory, so
+                // one MMA of N = BN + rows covers both halves: accumulator
+                // columns [0, BN) hold W h_hi, columns [BN, BN + rows) W h_lo.
+                const int n_mma = BN + max(16, (ti.n_rows + 15) & ~15);
                 const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, n_mma);
                 if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
                     ok = false;
@@ -535,13 +540,11 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint64_t da = ptx::smem_desc_sw128(sa);
-                    const uint64_t dhi = ptx::smem_desc_sw128(sa + C::A_BYTES);
-                    const uint64_t dlo = ptx::smem_desc_sw128(sa + C::A_BYTES + C::B_BYTES);
+                    const uint64_t dh = ptx::smem_desc_sw128(sa + C::A_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < kGemmBK / 16; ++kk) {
                         const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
-                        ptx::mma_bf16_ss(d, da + 2 * kk, dhi + 2 * kk, idesc, acc);
-                        ptx::mma_bf16_ss(d, da + 2 * kk, dlo + 2 * kk, idesc, 1u);
+                        ptx::mma_bf16_ss(d, da + 2 * kk, dh + 2 * kk, idesc, acc);
                     }
                     ptx::mma_commit(bar_addr(&ctl->empty[s]));
                     if (++s == C::STAGES) {
@@ -584,15 +587,16 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             const int row0 = ti.shared ? shared_row0 + ti.m0 : ti.p0;
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
             for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
-                uint32_t v[kEpiRows];
-                ptx::tmem_ld_32x32b_x16(tb + c0, v);
+                uint32_t v[kEpiRows], vl[kEpiRows];
+                ptx::tmem_ld_32x32b_x16(tb + c0, v);        // W h_hi
+                ptx::tmem_ld_32x32b_x16(tb + BN + c0, vl);  // W h_lo
                 ptx::tmem_ld_wait();
                 if (!warp_valid) continue;
                 const int rows = min(kEpiRows, ti.n_rows - c0);
                 float val[kEpiRows];
 #pragma unroll
                 for (int n = 0; n < kEpiRows; ++n) {
-                    val[n] = __uint_as_float(v[n]);
+                    val[n] = __uint_as_float(v[n]) + __uint_as_float(vl[n]);
                     if (ti.shared && n < rows)
                         val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
                 }
@@ -633,7 +637,11 @@ template <int BN, bool GU>
 cudaError_t launch_bn(const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
                       cudaStream_t st) {
     using C = Cfg<BN, GU>;
-    auto kern = GU ? gate_up_kernel<BN> : down_kernel<BN>;
+    void (*kern)(GemmMaps, GemmArgs);
+    if constexpr (GU)
+        kern = gate_up_kernel<BN>;
+    else
+        kern = down_kernel<BN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
@@ -649,7 +657,9 @@ cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_ti
         case 32: return launch_bn<32, GU>(maps, a, max_tiles, num_sms, st);
         case 64: return launch_bn<64, GU>(maps, a, max_tiles, num_sms, st);
         case 128: return launch_bn<128, GU>(maps, a, max_tiles, num_sms, st);
-        case 256: return launch_bn<256, GU>(maps, a, max_tiles, num_sms, st);
+        case 256:
+            if constexpr (GU) return launch_bn<256, GU>(maps, a, max_tiles, num_sms, st);
+            return cudaErrorInvalidValue;  // down tiles are at most 128 tokens wide
         default: return cudaErrorInvalidValue;
     }
 }
