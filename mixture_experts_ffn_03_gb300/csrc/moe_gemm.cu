@@ -46,14 +46,24 @@ constexpr int kStgBytes = kEpiRows * kEpiCols * 4;  // one staging buffer (2 KB)
 
 template <int BN, bool GU>
 struct Cfg {
+    // gate_up with BN <= 128 puts the tokens on the MMA's M side (M = 128) and
+    // the 128 gate + 128 up weight rows on N = 256: one MMA per K slice.
+    // gate_up with BN = 256 and down keep the weights on M.
+    static constexpr bool TS = GU && BN <= 128;
     static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;  // 16 KB weight tile
     static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
     static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : (A_BYTES + 2 * B_BYTES);
     static constexpr int CTL_BYTES = 1024;
-    static constexpr int EPI_BYTES = kEpiWarps * 2 * kStgBytes;  // double-buffered per warp
-    static constexpr int STAGES_FIT = (kSmemLimit - 2048 - EPI_BYTES) / STAGE_BYTES;
+    static constexpr int EPI_BYTES = TS ? 0 : kEpiWarps * 2 * kStgBytes;  // store staging
+    // TS: the MMA reads the token tile as 128 rows although only BN are loaded
+    // (results of the extra rows are never used), so 16 KB - B_BYTES of
+    // shared memory must follow the last stage's token tile.
+    static constexpr int TS_SLACK = TS ? 16384 - B_BYTES : 0;
+    static constexpr int TAIL_BYTES =
+        CTL_BYTES + (EPI_BYTES > TS_SLACK - CTL_BYTES ? EPI_BYTES : TS_SLACK - CTL_BYTES);
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
-    static constexpr int ACC_COLS = 2 * BN;  // TMEM columns per accumulator set
+    static constexpr int ACC_COLS = TS ? 2 * kGemmBM : 2 * BN;  // TMEM columns per accumulator set
     static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
     static constexpr int TMEM_USED = ACC_COLS * ACC_STAGES;
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -63,7 +73,7 @@ struct Cfg {
                                                         : 512;
     static constexpr int CTL_OFF = STAGES * STAGE_BYTES;
     static constexpr int EPI_OFF = CTL_OFF + CTL_BYTES;
-    static constexpr int SMEM = 1024 + EPI_OFF + EPI_BYTES;
+    static constexpr int SMEM = 1024 + CTL_OFF + TAIL_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
@@ -269,7 +279,8 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (tile + static_cast<int>(gridDim.x) < num_tiles)
                     nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
                 const int n_mma = max(16, (ti.n_rows + 15) & ~15);
-                const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, n_mma);
+                const uint32_t idesc = C::TS ? ptx::idesc_bf16_f32(kGemmBM, 2 * kGemmBM)
+                                             : ptx::idesc_bf16_f32(kGemmBM, n_mma);
                 if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
                     ok = false;
                     break;
@@ -293,8 +304,14 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     for (int kk = 0; kk < kGemmBK / 16; ++kk) {
                         const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
                         // +32 bytes of K per step, in 16-byte descriptor units
-                        ptx::mma_bf16_ss(d_gate, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-                        ptx::mma_bf16_ss(d_up, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+                        if constexpr (C::TS) {
+                            // D[token, 0:128] = gate, D[token, 128:256] = up: the gate
+                            // and up boxes are adjacent, one descriptor spans both.
+                            ptx::mma_bf16_ss(d_gate, db + 2 * kk, da0 + 2 * kk, idesc, acc);
+                        } else {
+                            ptx::mma_bf16_ss(d_gate, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+                            ptx::mma_bf16_ss(d_up, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+                        }
                     }
                     ptx::mma_commit(bar_addr(&ctl->empty[s]));
                     if (++s == C::STAGES) {
@@ -361,6 +378,70 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             }
         }
         ptx::cp_async_wait_all();
+    } else if constexpr (C::TS) {  // ------------------------- epilogue (warps 4-11)
+        // Tokens on TMEM lanes: warp we owns the 32 token rows 32*(warp % 4)..
+        // and the features [64*(we / 4), +64) of the tile; each thread computes
+        // its token's h for 32 features at a time and writes the bf16 hi/lo
+        // pairs as 16-byte vector stores of its own row.
+        const int we = warp - 4, q = warp & 3, half = we >> 2;
+        int as = 0;
+        uint32_t aph = 0;
+        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+            if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+            if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
+            ptx::tc_fence_after();
+            const int r0 = q * 32;  // first token row of this warp's lane quadrant
+            if (r0 < ti.n_rows) {
+                const int n_feat = ti.shared ? a.I_s : a.I;
+                const bool row_ok = r0 + lane < ti.n_rows;
+                const size_t prow = static_cast<size_t>(ti.p0 + r0 + lane) * n_feat;
+                __nv_bfloat16* dhi = ti.shared ? a.hs_hi : a.h_hi;
+                __nv_bfloat16* dlo = ti.shared ? a.hs_lo : a.h_lo;
+                const uint32_t tb =
+                    tmem_base + (static_cast<uint32_t>(r0) << 16) + as * C::ACC_COLS;
+                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                    const int fb = ti.f * kGemmBM + c;
+                    if (fb >= n_feat) break;  // I, I_s are multiples of 64
+                    uint32_t g[32], u[32];
+                    ptx::tmem_ld_32x32b_x32(tb + c, g);
+                    ptx::tmem_ld_32x32b_x32(tb + kGemmBM + c, u);
+                    ptx::tmem_ld_wait();
+                    if (row_ok) {
+                        uint32_t hi2[16], lo2[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float g0 = __uint_as_float(g[2 * j]);
+                            const float g1 = __uint_as_float(g[2 * j + 1]);
+                            const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+                            const float h1 =
+                                __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+                            const __nv_bfloat162 hp = __floats2bfloat162_rn(h0, h1);
+                            const __nv_bfloat162 lp = __floats2bfloat162_rn(
+                                h0 - __low2float(hp), h1 - __high2float(hp));
+                            hi2[j] = *reinterpret_cast<const uint32_t*>(&hp);
+                            lo2[j] = *reinterpret_cast<const uint32_t*>(&lp);
+                        }
+                        uint4* ph = reinterpret_cast<uint4*>(dhi + prow + fb);
+                        uint4* pl = reinterpret_cast<uint4*>(dlo + prow + fb);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            ph[v] = make_uint4(hi2[4 * v], hi2[4 * v + 1], hi2[4 * v + 2], hi2[4 * v + 3]);
+                            pl[v] = make_uint4(lo2[4 * v], lo2[4 * v + 1], lo2[4 * v + 2], lo2[4 * v + 3]);
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
+            if (++as == C::ACC_STAGES) {
+                as = 0;
+                aph ^= 1u;
+            }
+        }
     } else {  // ------------------------------------------- epilogue (warps 4-11)
         // Warp we drains TMEM lanes 32*(warp % 4).. (32 intermediate features)
         // for the 16-column chunks 16*(we / 4) + 32*j of each tile. Full chunks
