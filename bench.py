@@ -396,7 +396,7 @@ def main():
         down_gbs=work["down_bytes"] / (dn_ms / 1e3) / 1e9,
         e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h),
-        gpu_launches=moe.NUM_STAGES * K, clocks=clocks, cuda_graph=graph)
+        gpu_launches=moe.launch_count(layer.dims(T)) * K, clocks=clocks, cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
         inp_cpu = {n: t.cpu() for n, t in inp.items()}
         line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu)

@@ -143,6 +143,11 @@ moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layou
  * MOE_ERR_INVALID_ARG unless n_events is 0 or MOE_NUM_STAGES + 1. */
 moe_status moe_set_stage_events(void* const* events, int n_events);
 
+/* Number of kernels one moe_forward with these sizes launches (4 when
+ * T*k <= 2048: routing and the permute share one launch; else 6), or 0 for
+ * invalid sizes or T = 0. */
+int moe_launch_count(const moe_dims* d);
+
 /*
  * Allocation-free expert histogram. The pages have no counterpart to this
  * entry point; it exists for callers that cannot allocate device memory,

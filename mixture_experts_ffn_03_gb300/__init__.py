@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 6: "MOE_ERR_CAPACITY"}
 
 EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
-            "moe_workspace_layout", "moe_set_stage_events"]
+            "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count"]
 NUM_STAGES = 6
 STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
 
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_workspace_layout.restype = ctypes.c_int
     lib.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
     lib.moe_set_stage_events.restype = ctypes.c_int
+    lib.moe_launch_count.argtypes = [ctypes.POINTER(MoEDims)]
+    lib.moe_launch_count.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -88,6 +90,11 @@ def workspace_layout(dims: MoEDims) -> MoEWorkspaceLayout:
     if st != MOE_OK:
         raise MoEError(st, "moe_workspace_layout")
     return out
+
+
+def launch_count(dims: MoEDims) -> int:
+    """Kernels one moe_forward launches for these sizes."""
+    return int(load_library().moe_launch_count(ctypes.byref(dims)))
 
 
 def status_string(status: int) -> str:

@@ -324,6 +324,11 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     return MOE_OK;
 }
 
+MOE_API int moe_launch_count(const moe_dims* d) {
+    if (!dims_valid(d) || !dims_supported(d) || d->T == 0) return 0;
+    return route_small_fits(d->T, d->E, d->k) ? 4 : 6;
+}
+
 MOE_API moe_status moe_set_stage_events(void* const* events, int n_events) {
     if (n_events == 0 || events == nullptr) {
         tl_stage_events_on = false;

@@ -48,32 +48,32 @@ __device__ __forceinline__ uint64_t rank_code(float v, int e) {
            static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
 
-// Routing of token t by one warp; lane i holds experts i, i+32, ... (EPL of
-// them, E <= 32*EPL). Each round takes the warp-wide best of the lanes'
+// Routing of one token by one warp; lane i holds the logits of experts i,
+// i+32, ... (EPL of them, E <= 32*EPL). Each round takes the warp-wide best of the lanes'
 // current bests; only the lane that supplied it looks for its next best.
 // Lane j < k returns the j-th selected expert and its renormalised weight.
 template <int EPL>
-__device__ __forceinline__ void route_token(int t, int E, int k, int score_fn,
-                                            const float* __restrict__ logits, int lane,
-                                            int& my_e, float& my_w) {
-    const float* lg = logits + static_cast<size_t>(t) * E;
+__device__ __forceinline__ void route_token(const float (&v)[EPL], int E, int k, int score_fn,
+                                            int lane, int& my_e, float& my_w) {
     uint64_t c[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        c[i] = e < E ? rank_code(lg[e], e) : 0ull;
+        c[i] = e < E ? rank_code(v[i], e) : 0ull;
     }
     uint64_t lane_best = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) lane_best = c[i] > lane_best ? c[i] : lane_best;
     uint64_t mine = 0;
     for (int j = 0; j < k; ++j) {
-        uint64_t best = lane_best;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            best = other > best ? other : best;
-        }
+        // Warp-wide maximum of the 64-bit codes with two 32-bit reductions:
+        // the largest logit key, then the largest inverted index among the
+        // lanes that hold that key.
+        const uint32_t khi = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(lane_best >> 32));
+        const uint32_t klo = __reduce_max_sync(
+            0xFFFFFFFFu,
+            static_cast<uint32_t>(lane_best >> 32) == khi ? static_cast<uint32_t>(lane_best) : 0u);
+        const uint64_t best = (static_cast<uint64_t>(khi) << 32) | klo;
         if (lane == j) mine = best;
         if (lane_best == best) {
             uint64_t nb = 0;
@@ -192,11 +192,19 @@ __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int 
                                                 float* __restrict__ gate_logit,
                                                 int* __restrict__ ids_out,
                                                 float* __restrict__ w_out, int lane) {
+    // Issue the logit loads first so their latency overlaps the gate-logit loads.
+    const float* lg = logits + static_cast<size_t>(t) * E;
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldcs(lg + e) : 0.f;
+    }
     const float z = gate_logit_of(t, H, hidden, w_g, lane);
     if (lane == 0) gate_logit[t] = z;
     int my_e;
     float my_w;
-    route_token<EPL>(t, E, k, score_fn, logits, lane, my_e, my_w);
+    route_token<EPL>(v, E, k, score_fn, lane, my_e, my_w);
     if (lane < k) {
         const size_t o = static_cast<size_t>(t) * k + lane;
         topk_ids[o] = my_e;

@@ -86,5 +86,8 @@ def test_host_validation(lib):
     assert _call(lib, ok, ws_bytes=moe.workspace_size(ok) - 1) == 3        # too small
     assert _call(lib, ok, ws=ctypes.c_void_p((1 << 20) + 64)) == 3         # ws alignment
     assert _call(lib, moe.make_dims(0, 128, 16, 4, 64, 64, 0)) == 0        # T = 0: no work
-    for s in range(6):
+    for s in range(7):
         assert moe.status_string(s)
+    assert moe.launch_count(moe.make_dims(64, 2048, 256, 8, 512, 512, 1)) == 4   # T*k <= 2048
+    assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 6
+    assert moe.launch_count(moe.make_dims(0, 2048, 256, 8, 512, 512, 0)) == 0

@@ -168,3 +168,39 @@ def test_full_size_workloads(moe, name, n_check):
     cfg = wl.CONFIGS[name]
     inp = wl.make_inputs(cfg, seed=0, device="cuda")
     run_case(moe, cfg, inp, n_check)
+
+
+def test_single_expert(moe):
+    """E = k = 1: every token goes to expert 0 with weight exactly 1."""
+    cfg = wl.MoEConfig("single_expert", T=33, H=128, E=1, k=1, I=64, I_s=64, score_fn=wl.SOFTMAX)
+    inp = wl.make_inputs(cfg, seed=6)
+    layer, out, ids, w, counts = run_gpu(moe, inp, cfg)
+    assert torch.all(ids == 0) and torch.all(w == 1.0) and counts.tolist() == [cfg.T]
+    run_case(moe, cfg, inp)
+
+
+def test_many_tokens_few_experts(moe):
+    """Large groups (thousands of tokens per expert): many row tiles per expert."""
+    cfg = wl.MoEConfig("big_groups", T=20000, H=64, E=8, k=2, I=64, I_s=64, score_fn=wl.SIGMOID)
+    inp = wl.make_inputs(cfg, seed=7)
+    run_case(moe, cfg, inp, n_check=64)
+
+
+def test_nonfinite_logits_stay_in_range(moe):
+    """Routing of non-finite logits is unspecified, but it must select k distinct
+    in-range experts per token and the layer must complete without an error."""
+    cfg = wl.MoEConfig("nonfinite", T=40, H=128, E=16, k=4, I=64, I_s=64, score_fn=wl.SOFTMAX)
+    inp = wl.make_inputs(cfg, seed=8)
+    lg = inp["logits"]
+    lg[0, :] = float("nan")
+    lg[1, 3] = float("inf")
+    lg[2, :] = float("-inf")
+    lg[3, ::2] = float("nan")
+    layer, out, ids, w, counts = run_gpu(moe, inp, cfg)
+    g = ids.cpu().numpy()
+    assert g.min() >= 0 and g.max() < cfg.E
+    assert all(len(set(row.tolist())) == cfg.k for row in g)
+    assert int(counts.sum()) == cfg.T * cfg.k
+    # rows with finite logits still match the oracle exactly
+    o_ids, _ = oracle.route(inp["logits"][4:], cfg.k, cfg.score_fn)
+    assert np.array_equal(g[4:], o_ids)
