@@ -25,7 +25,7 @@ NVCC = os.environ.get("NVCC", "nvcc")
 
 def _flags():
     return ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
-                   "-fvisibility=hidden", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
+                   "-fvisibility=hidden", "-diag-suppress", "177", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
 
 
 def _stale() -> bool:
@@ -59,7 +59,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write("\n".join(log))
     tmp = LIB + ".tmp"
-    cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + [o for _, o, _ in results]
+    cmd = [NVCC] + ARCH + ["-shared", "-Xlinker", "-z", "-Xlinker", "defs", "-o", tmp] + [
+        o for _, o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
