@@ -115,6 +115,20 @@ bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 y [outer, inner] written by the tokens-on-M down epilogue in boxes of
+// 32 columns x 32 rows staged with the 128-byte swizzle.
+bool make_y_store_map_sw128(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cache[kMaxDevices] = {0};
     int dev = 0;
@@ -247,7 +261,8 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
          make_store_map(&gu.st[1], h_lo, BF16, 2, I, tk) &&
          make_store_map(&gu.st[2], hs_hi, BF16, 2, Is, T) &&
          make_store_map(&gu.st[3], hs_lo, BF16, 2, Is, T) &&
-         make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T);
+         make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
+         make_y_store_map_sw128(&dn.st[1], y, H, tk + T);
     if (!ok) return MOE_ERR_CUDA;
 
     GemmArgs ga{};
@@ -275,7 +290,8 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
 
     const size_t routed_min = tk < static_cast<size_t>(E) ? tk : static_cast<size_t>(E);
     const int F_gu = (I + kGemmBM - 1) / kGemmBM, F_s = (Is + kGemmBM - 1) / kGemmBM;
-    const int F_dn = (H + kGemmBM - 1) / kGemmBM;
+    // 128-token down tiles use the tokens-on-M kernel with 256 output features per tile.
+    const int F_dn = bn_dn == 128 ? (H + 255) / 256 : (H + kGemmBM - 1) / kGemmBM;
     const size_t max_gu = (tk / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
     const size_t max_dn = (tk / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
     const int cap = 1 << 30;

@@ -161,9 +161,9 @@ __device__ __noinline__ void wait_bounded(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t* b) { return ptx::smem_u32(b); }
 
 // Common set-up: barriers, TMEM allocation. Returns the TMEM base address.
-template <int BN, bool GU>
+// C is the kernel's shared-memory / TMEM configuration.
+template <class C>
 __device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp) {
-    using C = Cfg<BN, GU>;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar_addr(&ctl->full_a[s]), 1);
@@ -188,9 +188,8 @@ __device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp) {
     return ctl->tmem_base;
 }
 
-template <int BN, bool GU>
+template <class C>
 __device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, int warp) {
-    using C = Cfg<BN, GU>;
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -222,7 +221,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
     }
-    const uint32_t tmem_base = gemm_setup<BN, true>(ctl, warp);
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
     ptx::griddep_wait();  // routing, tile lists and the slot order come from earlier kernels
 
     const int R = a.meta[META_RT_GU];
@@ -519,7 +518,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         }
         if (lane == 0) ptx::bulk_wait_all();
     }
-    gemm_teardown<BN, true>(tmem_base, warp);
+    gemm_teardown<C>(tmem_base, warp);
 }
 
 // =================================================================== down
@@ -541,7 +540,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.hs_hi);
         ptx::prefetch_tmap(&maps.hs_lo);
     }
-    const uint32_t tmem_base = gemm_setup<BN, false>(ctl, warp);
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
     ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
 
     const int R = a.meta[META_RT_DN];
@@ -711,7 +710,242 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         }
         if (lane == 0) ptx::bulk_wait_all();
     }
-    gemm_teardown<BN, false>(tmem_base, warp);
+    gemm_teardown<C>(tmem_base, warp);
+}
+
+// ====================================================== down, tokens on M
+// Tiles of up to 128 tokens of one expert against 256 output features:
+// D[token, 0:N] = h_hi W^T + h_lo W^T, where the h_hi and h_lo tiles are two A
+// operands (M = 128 token rows) accumulating into one TMEM accumulator and the
+// weight tile (N = 256 rows of W_down[e]) is the B operand. Each h row is read
+// once per 256 output features (twice as few as with the weights on M) and the
+// epilogue drains a single accumulator. Used when groups are large enough to
+// fill most of the 128 token rows.
+struct DownTs {
+    static constexpr int BM = 128;                          // token rows per tile (MMA M)
+    static constexpr int NF = 256;                          // output features per tile (MMA N)
+    static constexpr int A_BYTES = BM * kGemmBK * 2;        // 16 KB: h_hi or h_lo tile
+    static constexpr int W_BYTES = NF * kGemmBK * 2;        // 32 KB: weight tile (two boxes)
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + W_BYTES;
+    static constexpr int STG_BYTES = 32 * 32 * 4;           // one warp's 32 x 32 fp32 store box
+    static constexpr int EPI_BYTES = kEpiWarps * STG_BYTES;
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - EPI_BYTES - CTL_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES;    // 1024-byte aligned (swizzled boxes)
+    static constexpr int CTL_OFF = EPI_OFF + EPI_BYTES;
+    static constexpr int SMEM = 1024 + CTL_OFF + CTL_BYTES;
+    static constexpr int ACC_COLS = NF;
+    static constexpr int ACC_STAGES = 2;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(SMEM <= kSmemLimit, "shared memory budget");
+    static_assert(EPI_OFF % 1024 == 0 && STG_BYTES % 1024 == 0, "swizzled staging alignment");
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    using C = DownTs;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::CTL_OFF);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&maps.w);
+        ptx::prefetch_tmap(&maps.ws);
+        ptx::prefetch_tmap(&maps.h_hi);
+        ptx::prefetch_tmap(&maps.h_lo);
+        ptx::prefetch_tmap(&maps.hs_hi);
+        ptx::prefetch_tmap(&maps.hs_lo);
+        ptx::prefetch_tmap(&maps.st[1]);
+    }
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
+    ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
+
+    const int R = a.meta[META_RT_DN];
+    const int F = (a.H + C::NF - 1) / C::NF;
+    const int routed_tiles = R * F;
+    const int num_tiles = routed_tiles + ((a.T + C::BM - 1) / C::BM) * F;
+    volatile int* abort_flag = &ctl->abort;
+    unsigned* err = a.err;
+    const unsigned code = ERR_DOWN_TIMEOUT;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------------------------- TMA producer
+            const uint64_t pol_w = ptx::policy_evict_normal();
+            const uint64_t pol_h = ptx::policy_evict_last();  // h rows are re-read per feature block
+            int s = 0;
+            uint32_t ph = 0, armed = 0, parity_bits = 0;
+            bool ok = true;
+            Tile nxt = decode_tile<C::BM>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+                if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                    nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
+                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
+                const CUtensorMap* thi = ti.shared ? &maps.hs_hi : &maps.h_hi;
+                const CUtensorMap* tlo = ti.shared ? &maps.hs_lo : &maps.h_lo;
+                // Rows past this expert's H (a ragged last block) read the next
+                // expert's rows or zero fill; their columns are never stored.
+                const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * C::NF;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint32_t fb = bar_addr(&ctl->full_a[s]);
+                    ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    ptx::tma_load_2d(sa, thi, fb, ks * kGemmBK, ti.p0, pol_h);
+                    ptx::tma_load_2d(sa + C::A_BYTES, tlo, fb, ks * kGemmBK, ti.p0, pol_h);
+                    ptx::tma_load_2d(sa + 2 * C::A_BYTES, tw, fb, ks * kGemmBK, row_w, pol_w);
+                    ptx::tma_load_2d(sa + 2 * C::A_BYTES + C::W_BYTES / 2, tw, fb, ks * kGemmBK,
+                                     row_w + C::NF / 2, pol_w);
+                    armed |= 1u << s;
+                    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) drain_tma<C::STAGES>(ctl, armed, parity_bits);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------------------------- MMA issuer
+            int s = 0, as = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            Tile nxt = decode_tile<C::BM>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+                if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                    nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
+                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const int n_f = min(C::NF, a.H - ti.f * C::NF);  // a multiple of 64
+                const uint32_t idesc = ptx::idesc_bf16_f32(C::BM, n_f);
+                if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + as * C::ACC_COLS;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint64_t dhi = ptx::smem_desc_sw128(sa);
+                    const uint64_t dlo = ptx::smem_desc_sw128(sa + C::A_BYTES);
+                    const uint64_t dw = ptx::smem_desc_sw128(sa + 2 * C::A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+                        const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
+                        ptx::mma_bf16_ss(d, dhi + 2 * kk, dw + 2 * kk, idesc, acc);
+                        ptx::mma_bf16_ss(d, dlo + 2 * kk, dw + 2 * kk, idesc, 1u);
+                    }
+                    ptx::mma_commit(bar_addr(&ctl->empty[s]));
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar_addr(&ctl->tfull[as]));
+                if (++as == C::ACC_STAGES) {
+                    as = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) {
+                ptx::mma_commit(bar_addr(&ctl->drain));
+                wait_bounded(bar_addr(&ctl->drain), 0);
+            }
+        }
+    } else if (warp >= 4) {  // ------------------------------ epilogue (warps 4-11)
+        // Tokens on TMEM lanes: warp we owns the token rows 32*(warp % 4).. and
+        // the features [128*(we / 4), +128) of the tile, drained 32 at a time.
+        // Each thread holds 32 consecutive features of its token's y row and
+        // writes them into the warp's 128-byte-swizzled staging box (conflict
+        // free), which goes out as one 32 x 32 TMA store; a warp whose token
+        // rows are only partly valid stores its valid rows directly.
+        const int we = warp - 4, q = warp & 3, half = we >> 2;
+        uint8_t* stg = smem + C::EPI_OFF + we * C::STG_BYTES;
+        const uint32_t stg_u32 = ptx::smem_u32(stg);
+        int as = 0;
+        uint32_t aph = 0;
+        const int shared_row0 = a.T * a.k;
+        Tile nxt = decode_tile<C::BM>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
+            if (tile + static_cast<int>(gridDim.x) < num_tiles)
+                nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
+            if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
+            ptx::tc_fence_after();
+            const int r0 = q * 32;
+            const int rows_valid = ti.n_rows - r0;  // token rows of this warp that are real
+            if (rows_valid > 0) {
+                const int n_f = min(C::NF, a.H - ti.f * C::NF);
+                const int row0 = (ti.shared ? shared_row0 + ti.m0 : ti.p0) + r0;
+                float scale = 1.f;
+                if (ti.shared && lane < rows_valid)
+                    scale = 1.f / (1.f + expf(-a.gate_logit[ti.m0 + r0 + lane]));
+                const uint32_t tb =
+                    tmem_base + (static_cast<uint32_t>(r0) << 16) + as * C::ACC_COLS;
+                for (int col = half * (C::NF / 2); col < half * (C::NF / 2) + C::NF / 2; col += 32) {
+                    if (col >= n_f) break;
+                    const int f0 = ti.f * C::NF + col;
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(tb + col, v);
+                    if (rows_valid >= 32) {
+                        if (lane == 0) ptx::bulk_wait_read<0>();  // staging box free again
+                        ptx::tmem_ld_wait();
+                        __syncwarp();
+                        const uint32_t row_addr = stg_u32 + lane * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            ptx::st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4),
+                                              __uint_as_float(v[4 * j]) * scale,
+                                              __uint_as_float(v[4 * j + 1]) * scale,
+                                              __uint_as_float(v[4 * j + 2]) * scale,
+                                              __uint_as_float(v[4 * j + 3]) * scale);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&maps.st[1], stg_u32, f0, row0);
+                            ptx::bulk_commit();
+                        }
+                    } else {
+                        ptx::tmem_ld_wait();
+                        if (lane < rows_valid) {
+                            float4* dst = reinterpret_cast<float4*>(
+                                a.y + static_cast<size_t>(row0 + lane) * a.H + f0);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = make_float4(__uint_as_float(v[4 * j]) * scale,
+                                                     __uint_as_float(v[4 * j + 1]) * scale,
+                                                     __uint_as_float(v[4 * j + 2]) * scale,
+                                                     __uint_as_float(v[4 * j + 3]) * scale);
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
+            if (++as == C::ACC_STAGES) {
+                as = 0;
+                aph ^= 1u;
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_all();
+    }
+    gemm_teardown<C>(tmem_base, warp);
 }
 
 template <int BN, bool GU>
@@ -730,6 +964,17 @@ cudaError_t launch_bn(const GemmMaps& maps, const GemmArgs& a, int max_tiles, in
     return launch_kernel(kern, dim3(grid), dim3(kThreads), C::SMEM, st, true, maps, a);
 }
 
+cudaError_t launch_down_ts(const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
+                           cudaStream_t st) {
+    using C = DownTs;
+    cudaError_t e = cudaFuncSetAttribute(down_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = max_tiles < num_sms ? max_tiles : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    return launch_kernel(down_ts_kernel, dim3(grid), dim3(kThreads), C::SMEM, st, true, maps, a);
+}
+
 template <bool GU>
 cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
                      cudaStream_t st) {
@@ -737,7 +982,9 @@ cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_ti
         case 16: return launch_bn<16, GU>(maps, a, max_tiles, num_sms, st);
         case 32: return launch_bn<32, GU>(maps, a, max_tiles, num_sms, st);
         case 64: return launch_bn<64, GU>(maps, a, max_tiles, num_sms, st);
-        case 128: return launch_bn<128, GU>(maps, a, max_tiles, num_sms, st);
+        case 128:
+            if constexpr (GU) return launch_bn<128, GU>(maps, a, max_tiles, num_sms, st);
+            return launch_down_ts(maps, a, max_tiles, num_sms, st);
         case 256:
             if constexpr (GU) return launch_bn<256, GU>(maps, a, max_tiles, num_sms, st);
             return cudaErrorInvalidValue;  // down tiles are at most 128 tokens wide

@@ -100,6 +100,7 @@ struct GemmMaps {
     CUtensorMap hs_lo;
     // Epilogue stores (no swizzle), box of 32 columns x kEpiRows rows:
     // gate_up: st[0..3] = h_hi, h_lo, hs_hi, hs_lo; down: st[0] = y [T*k + T, H].
+    // down with tokens on M: st[1] = y in 32 x 32 boxes with the 128-byte swizzle.
     CUtensorMap st[4];
 };
 

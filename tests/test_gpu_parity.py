@@ -114,6 +114,11 @@ SMALL = [
                  score_fn=wl.SIGMOID),
     wl.MoEConfig("multiblock_max_experts", T=300, H=64, E=1024, k=10, I=64, I_s=64,
                  score_fn=wl.SIGMOID),
+    # 128-token down tiles (tokens on the MMA's M side, 256 features per tile):
+    # H not a multiple of 256, ragged row tiles and a ragged shared-expert tail
+    wl.MoEConfig("down_ts_ragged", T=700, H=320, E=8, k=2, I=128, I_s=192, score_fn=wl.SOFTMAX),
+    wl.MoEConfig("down_ts_multiblock", T=1500, H=192, E=6, k=3, I=64, I_s=128,
+                 score_fn=wl.SIGMOID),
 ]
 
 
