@@ -49,9 +49,9 @@ __device__ __forceinline__ uint64_t rank_code(float v, int e) {
 }
 
 // Routing of one token by one warp; lane i holds the logits of experts i,
-// i+32, ... (EPL of them, E <= 32*EPL). Each round takes the warp-wide best of the lanes'
-// current bests; only the lane that supplied it looks for its next best.
-// Lane j < k returns the j-th selected expert and its renormalised weight.
+// i+32, ... (EPL of them, E <= 32*EPL). Each round takes the warp-wide best of
+// the lanes' current bests; only the lane that supplied it looks for its next
+// best. Lane j < k returns the j-th selected expert and its renormalised weight.
 template <int EPL>
 __device__ __forceinline__ void route_token(const float (&v)[EPL], int E, int k, int score_fn,
                                             int lane, int& my_e, float& my_w) {
@@ -66,13 +66,18 @@ __device__ __forceinline__ void route_token(const float (&v)[EPL], int E, int k,
     for (int i = 0; i < EPL; ++i) lane_best = c[i] > lane_best ? c[i] : lane_best;
     uint64_t mine = 0;
     for (int j = 0; j < k; ++j) {
-        // Warp-wide maximum of the 64-bit codes with two 32-bit reductions:
-        // the largest logit key, then the largest inverted index among the
-        // lanes that hold that key.
-        const uint32_t khi = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(lane_best >> 32));
-        const uint32_t klo = __reduce_max_sync(
-            0xFFFFFFFFu,
-            static_cast<uint32_t>(lane_best >> 32) == khi ? static_cast<uint32_t>(lane_best) : 0u);
+        // Warp-wide maximum of the 64-bit codes: the largest logit key first;
+        // when one lane holds it (the usual case) its code is the maximum,
+        // otherwise the largest inverted index among the tied lanes decides.
+        const uint32_t key = static_cast<uint32_t>(lane_best >> 32);
+        const uint32_t khi = __reduce_max_sync(0xFFFFFFFFu, key);
+        const unsigned tied = __ballot_sync(0xFFFFFFFFu, key == khi);
+        uint32_t klo;
+        if ((tied & (tied - 1u)) == 0u)
+            klo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(lane_best), __ffs(tied) - 1);
+        else
+            klo = __reduce_max_sync(0xFFFFFFFFu,
+                                    key == khi ? static_cast<uint32_t>(lane_best) : 0u);
         const uint64_t best = (static_cast<uint64_t>(khi) << 32) | klo;
         if (lane == j) mine = best;
         if (lane_best == best) {
@@ -102,29 +107,62 @@ __device__ __forceinline__ void route_token(const float (&v)[EPL], int E, int k,
 }
 
 // Shared-expert gate logit z_t = x_t . w_g, fp32 accumulation, by one warp.
-__device__ __forceinline__ float gate_logit_of(int t, int H,
-                                               const __nv_bfloat16* __restrict__ hidden,
-                                               const __nv_bfloat16* __restrict__ w_g, int lane) {
-    const uint4* xr = reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H);
-    const uint4* gr = reinterpret_cast<const uint4*>(w_g);
-    float acc = 0.f;
-#pragma unroll 8
-    for (int c = lane; c < H / 8; c += 32) {
-        const uint4 a = xr[c], b = gr[c];
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+// The row is read in batches of kGateBatch 16-byte chunks per lane: load()
+// issues the first batch early (its latency overlaps the top-k selection) and
+// finish() consumes it and any further batches. Lane i accumulates chunks
+// i, i+32, ... in order, then the warp sums the lanes.
+constexpr int kGateBatch = 4;
+
+struct GateLogit {
+    uint4 x[kGateBatch], g[kGateBatch];
+
+    __device__ __forceinline__ void load(int t, int H, const __nv_bfloat16* __restrict__ hidden,
+                                         const __nv_bfloat16* __restrict__ w_g, int lane, int c0) {
+        const uint4* xr = reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H);
+        const uint4* gr = reinterpret_cast<const uint4*>(w_g);
+        const int nch = H / 8;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 fa = __bfloat1622float2(a2[q]);
-            const float2 fb = __bfloat1622float2(b2[q]);
-            acc = fmaf(fa.x, fb.x, acc);
-            acc = fmaf(fa.y, fb.y, acc);
+        for (int i = 0; i < kGateBatch; ++i) {
+            const int c = c0 + lane + 32 * i;
+            if (c < nch) {
+                x[i] = __ldcs(xr + c);
+                g[i] = __ldg(gr + c);
+            } else {
+                x[i] = make_uint4(0u, 0u, 0u, 0u);
+                g[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
+
+    __device__ __forceinline__ float dot(float acc) const {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    return acc;
-}
+        for (int i = 0; i < kGateBatch; ++i) {
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&x[i]);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&g[i]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 fa = __bfloat1622float2(a2[q]);
+                const float2 fb = __bfloat1622float2(b2[q]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+        }
+        return acc;
+    }
+
+    // Chunks past the row end were loaded as zeros and add exact zeros.
+    __device__ __forceinline__ float finish(int t, int H, const __nv_bfloat16* __restrict__ hidden,
+                                            const __nv_bfloat16* __restrict__ w_g, int lane) {
+        float acc = dot(0.f);
+        for (int c0 = 32 * kGateBatch; c0 < H / 8; c0 += 32 * kGateBatch) {
+            load(t, H, hidden, w_g, lane, c0);
+            acc = dot(acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        return acc;
+    }
+};
 
 // Exclusive scan of one int per thread over a block of NW warps; *total gets
 // the block sum. Contains __syncthreads: every thread must call it.
@@ -158,15 +196,16 @@ __device__ __forceinline__ void write_row_tiles(int4* rt, int pos, int e, int n_
         rt[pos++] = make_int4(e, m0, min(bn, n_e - m0), off_e + m0);
 }
 
-// Ordered (stable) scatter of the slots [a0, a1) by one warp; `running[e]` is
-// the next free sorted position of expert e. Equal experts inside a 32-slot
-// chunk are ranked by lane, so slot order (token order) is kept.
+// Ordered (stable) scatter of the slots [a0, a1) by one warp; the expert of
+// slot a is ids[a - a0] and `running[e]` is the next free sorted position of
+// expert e. Equal experts inside a 32-slot chunk are ranked by lane, so slot
+// order (token order) is kept.
 __device__ __forceinline__ void ordered_scatter(const int* ids, long a0, long a1, int* running,
                                                 int* __restrict__ perm, int* __restrict__ inv,
                                                 int lane) {
     for (long base = a0; base < a1; base += 32) {
         const long a = base + lane;
-        const int e = a < a1 ? ids[a] : -1;
+        const int e = a < a1 ? ids[a - a0] : -1;
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
         const int rank = __popc(peers & ((1u << lane) - 1u));
         int pos = 0;
@@ -192,7 +231,7 @@ __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int 
                                                 float* __restrict__ gate_logit,
                                                 int* __restrict__ ids_out,
                                                 float* __restrict__ w_out, int lane) {
-    // Issue the logit loads first so their latency overlaps the gate-logit loads.
+    // All loads are issued first: the hidden row's latency overlaps the top-k.
     const float* lg = logits + static_cast<size_t>(t) * E;
     float v[EPL];
 #pragma unroll
@@ -200,11 +239,13 @@ __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int 
         const int e = lane + 32 * i;
         v[i] = e < E ? __ldcs(lg + e) : 0.f;
     }
-    const float z = gate_logit_of(t, H, hidden, w_g, lane);
-    if (lane == 0) gate_logit[t] = z;
+    GateLogit gl;
+    gl.load(t, H, hidden, w_g, lane, 0);
     int my_e;
     float my_w;
     route_token<EPL>(v, E, k, score_fn, lane, my_e, my_w);
+    const float z = gl.finish(t, H, hidden, w_g, lane);
+    if (lane == 0) gate_logit[t] = z;
     if (lane < k) {
         const size_t o = static_cast<size_t>(t) * k + lane;
         topk_ids[o] = my_e;
@@ -301,7 +342,7 @@ route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn
         if (tid == 0) meta[g == 0 ? META_RT_GU : META_RT_DN] = tot_tiles;
     }
     __syncthreads();
-    ordered_scatter(s_ids, a0, a1, s_sub + warp * E, perm, inv, lane);
+    ordered_scatter(s_ids + a0, a0, a1, s_sub + warp * E, perm, inv, lane);
     if (tid == 0) meta[META_TICKET] = 0;
 }
 
@@ -356,11 +397,18 @@ count_scan_kernel(int T, int E, int k, int bn_gu, int bn_dn, const int* __restri
         const int e = tid * ept + r;
         if (e >= E) break;
         int c = 0;
-        for (int b = 0; b < nb; ++b) {
-            int* p = &blockhist[static_cast<size_t>(b) * E + e];
-            const int v = __ldcg(p);
-            *p = c;  // becomes the block's base inside expert e
-            c += v;
+        // 16 blocks' counts per round trip: all loads first, then the running
+        // sum replaces each count by the block's base inside expert e.
+        for (int b0 = 0; b0 < nb; b0 += 16) {
+            int v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = b0 + j < nb ? __ldcg(&blockhist[static_cast<size_t>(b0 + j) * E + e]) : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (b0 + j < nb) blockhist[static_cast<size_t>(b0 + j) * E + e] = c;
+                c += v[j];
+            }
         }
         local[r] = c;
         mine += c;
@@ -401,7 +449,9 @@ __global__ void __launch_bounds__(256)
 scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
                const int* __restrict__ blockhist, const int* __restrict__ offsets,
                int* __restrict__ perm, int* __restrict__ inv) {
-    extern __shared__ int s_sub[];  // [8][E]: per-warp counts, then per-warp bases
+    extern __shared__ int s_dyn[];
+    int* s_sub = s_dyn;           // [8][E]: per-warp counts, then per-warp bases
+    int* s_ids = s_dyn + 8 * E;   // [8][32 k]: each warp's slot experts
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ptx::griddep_launch_dependents();
     for (int i = tid; i < 8 * E; i += 256) s_sub[i] = 0;
@@ -410,8 +460,15 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
     const long t0 = static_cast<long>(blockIdx.x) * kCountTokens + warp * 32;
     const long t1 = min(static_cast<long>(T), t0 + 32);
     const long wa0 = t0 * k, wa1 = t1 > t0 ? t1 * k : wa0;
+    const int n = static_cast<int>(wa1 - wa0);  // <= 32 k
+    int* ids = s_ids + warp * 32 * k;
+    // The warp's slot experts are read once (all loads in flight together)
+    // and both passes below work from shared memory.
+#pragma unroll 8
+    for (int i = lane; i < n; i += 32) ids[i] = topk_ids[wa0 + i];
+    __syncwarp();
     int* running = s_sub + warp * E;
-    for (long a = wa0 + lane; a < wa1; a += 32) atomicAdd(&running[topk_ids[a]], 1);
+    for (int i = lane; i < n; i += 32) atomicAdd(&running[ids[i]], 1);
     __syncthreads();
     for (int e = tid; e < E; e += 256) {
         int run = offsets[e] + blockhist[static_cast<size_t>(blockIdx.x) * E + e];
@@ -422,7 +479,7 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
         }
     }
     __syncthreads();
-    ordered_scatter(topk_ids, wa0, wa1, running, perm, inv, lane);
+    ordered_scatter(ids, wa0, wa1, running, perm, inv, lane);
 }
 
 __global__ void __launch_bounds__(256)
@@ -526,8 +583,14 @@ cudaError_t launch_count_scan(int T, int E, int k, int bn_gu, int bn_dn, const i
 cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
                            const int* offsets, int* perm, int* inv, cudaStream_t st) {
     const int blocks = (T + kCountTokens - 1) / kCountTokens;
-    return launch_kernel(scatter_kernel, dim3(blocks), dim3(256), 8 * E * sizeof(int), st, true, T,
-                         E, k, topk_ids, blockhist, offsets, perm, inv);
+    const size_t smem = (8 * static_cast<size_t>(E) + 8 * 32 * static_cast<size_t>(k)) * sizeof(int);
+    if (smem > 48 * 1024) {  // E = 1024 with k = 32 needs 64 KB
+        const cudaError_t e = cudaFuncSetAttribute(
+            scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(scatter_kernel, dim3(blocks), dim3(256), smem, st, true, T, E, k,
+                         topk_ids, blockhist, offsets, perm, inv);
 }
 
 cudaError_t launch_combine(int T, int H, int k, const float* y, const float* topk_w,
