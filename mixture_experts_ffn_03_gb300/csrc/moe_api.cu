@@ -143,10 +143,17 @@ int sm_count() {
 }
 
 // Tokens per tile: the smallest supported width >= 1.25x the mean group size.
-int pick_bn(size_t tk, int E, int cap) {
+// gate_up also has a 160-token width (groups of ~128 tokens fit one tile and
+// the pipeline keeps four stages).
+int pick_bn(size_t tk, int E, int cap, bool gate_up) {
     const double mean = static_cast<double>(tk) / E;
+    const int widths[] = {16, 32, 64, 128, 160, 256};
     int bn = 16;
-    while (bn < cap && bn < 1.25 * mean) bn *= 2;
+    for (int w : widths) {
+        if (w > cap || (w == 160 && !gate_up)) continue;
+        bn = w;
+        if (w >= 1.25 * mean) break;
+    }
     return bn;
 }
 
@@ -244,8 +251,8 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     auto* hs_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_lo);
     float* y = reinterpret_cast<float*>(ws + L.y);
 
-    const int bn_gu = pick_bn(tk, E, 256);
-    const int bn_dn = pick_bn(tk, E, 128);
+    const int bn_gu = pick_bn(tk, E, 256, true);
+    const int bn_dn = pick_bn(tk, E, 128, false);
     const int num_sms = sm_count();
     if (num_sms <= 0) return MOE_ERR_CUDA;
 

@@ -54,7 +54,14 @@ struct Cfg {
     static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
     static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : (A_BYTES + 2 * B_BYTES);
     static constexpr int CTL_BYTES = 1024;
-    static constexpr int EPI_BYTES = TS ? 0 : kEpiWarps * 2 * kStgBytes;  // store staging
+    // Store staging: two buffers per epilogue warp, or one when that buys the
+    // pipeline a fourth stage.
+    static constexpr int STAGES_2BUF =
+        (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * 2 * kStgBytes) / STAGE_BYTES;
+    static constexpr int STAGES_1BUF =
+        (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * kStgBytes) / STAGE_BYTES;
+    static constexpr int EPI_BUFS = (STAGES_2BUF < 4 && STAGES_1BUF >= 4) ? 1 : 2;
+    static constexpr int EPI_BYTES = TS ? 0 : kEpiWarps * EPI_BUFS * kStgBytes;
     // TS: the MMA reads the token tile as 128 rows although only BN are loaded
     // (results of the extra rows are never used), so 16 KB - B_BYTES of
     // shared memory must follow the last stage's token tile.
@@ -77,6 +84,7 @@ struct Cfg {
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
+    static_assert(BN % 8 == 0, "row gather: 8 rows per pass");
     static_assert(GU || BN <= 128, "down: h_hi and h_lo rows share one MMA of N <= 256");
 };
 
@@ -447,7 +455,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         // are staged in the warp's own shared buffers and written with TMA box
         // stores; a ragged last chunk is written with plain stores.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
-        uint8_t* stg = smem + C::EPI_OFF + we * 2 * kStgBytes;
+        uint8_t* stg = smem + C::EPI_OFF + we * C::EPI_BUFS * kStgBytes;
         uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
@@ -474,10 +482,10 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (!warp_valid) continue;
                 const int rows = min(kEpiRows, ti.n_rows - c0);
                 if (rows == kEpiRows) {
-                    const uint32_t b = nbuf++ & 1u;
+                    const uint32_t b = nbuf++ % C::EPI_BUFS;
                     __nv_bfloat16* shi = reinterpret_cast<__nv_bfloat16*>(stg + b * kStgBytes);
                     __nv_bfloat16* slo = shi + kEpiRows * kEpiCols;
-                    if (lane == 0) ptx::bulk_wait_read<1>();  // buffer b no longer being read
+                    if (lane == 0) ptx::bulk_wait_read<C::EPI_BUFS - 1>();  // buffer b is free
                     __syncwarp();
 #pragma unroll
                     for (int n = 0; n < kEpiRows; ++n) {
@@ -650,7 +658,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         // as fp32 TMA box stores of y, ragged tails as plain stores. Shared
         // expert rows are scaled by their token's gate sigmoid(x . w_g).
         const int we = warp - 4, q = warp & 3, half = we >> 2;
-        uint8_t* stg = smem + C::EPI_OFF + we * 2 * kStgBytes;
+        uint8_t* stg = smem + C::EPI_OFF + we * C::EPI_BUFS * kStgBytes;
         uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
@@ -681,9 +689,9 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                         val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
                 }
                 if (rows == kEpiRows) {
-                    const uint32_t b = nbuf++ & 1u;
+                    const uint32_t b = nbuf++ % C::EPI_BUFS;
                     float* sy = reinterpret_cast<float*>(stg + b * kStgBytes);
-                    if (lane == 0) ptx::bulk_wait_read<1>();  // buffer b no longer being read
+                    if (lane == 0) ptx::bulk_wait_read<C::EPI_BUFS - 1>();  // buffer b is free
                     __syncwarp();
 #pragma unroll
                     for (int n = 0; n < kEpiRows; ++n) sy[n * kEpiCols + lane] = val[n];
@@ -985,6 +993,9 @@ cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_ti
         case 128:
             if constexpr (GU) return launch_bn<128, GU>(maps, a, max_tiles, num_sms, st);
             return launch_down_ts(maps, a, max_tiles, num_sms, st);
+        case 160:
+            if constexpr (GU) return launch_bn<160, GU>(maps, a, max_tiles, num_sms, st);
+            return cudaErrorInvalidValue;
         case 256:
             if constexpr (GU) return launch_bn<256, GU>(maps, a, max_tiles, num_sms, st);
             return cudaErrorInvalidValue;  // down tiles are at most 128 tokens wide
@@ -995,7 +1006,7 @@ cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_ti
 }  // namespace
 
 bool gemm_bn_supported(int bn) {
-    return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
+    return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 160 || bn == 256;
 }
 
 cudaError_t launch_gate_up(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,

@@ -114,6 +114,8 @@ SMALL = [
                  score_fn=wl.SIGMOID),
     wl.MoEConfig("multiblock_max_experts", T=300, H=64, E=1024, k=10, I=64, I_s=64,
                  score_fn=wl.SIGMOID),
+    # 160-token gate_up tiles (mean group ~125 tokens; some groups need two tiles)
+    wl.MoEConfig("gu160", T=500, H=192, E=8, k=2, I=128, I_s=64, score_fn=wl.SOFTMAX),
     # multi-block permute with E = 1024 and k = 32 (largest scatter shared memory)
     wl.MoEConfig("multiblock_k32", T=100, H=64, E=1024, k=32, I=64, I_s=64, score_fn=wl.SOFTMAX),
     # 128-token down tiles (tokens on the MMA's M side, 256 features per tile):
