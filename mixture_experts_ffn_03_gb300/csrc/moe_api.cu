@@ -100,6 +100,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pair of bf16 matrices [rows, inner], the second `plane_bytes` after the
+// first, as one 3D map {inner, rows, 2}; a box of 64 x box_rows x 2 lands as
+// the first matrix's rows followed by the second's (128-byte swizzle).
+bool make_pair_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t plane_bytes, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, 2};
+    cuuint64_t strides[2] = {inner * 2, plane_bytes};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kGemmBK), box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major matrix [outer, inner] of `elem` bytes per element, written by the
 // GEMM epilogues in boxes of kEpiCols x kEpiRows (no swizzle).
 bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t elem,
@@ -257,12 +273,19 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     if (num_sms <= 0) return MOE_ERR_CUDA;
 
     GemmMaps gu{}, dn{};
-    bool ok = make_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E) * 2 * I, kGemmBM) &&
-              make_map(&gu.ws, ws_gate_up, H, static_cast<uint64_t>(2) * Is, kGemmBM) &&
-              make_map(&dn.w, w_down, I, static_cast<uint64_t>(E) * H, kGemmBM) &&
-              make_map(&dn.ws, ws_down, Is, H, kGemmBM) &&
-              make_map(&dn.h_hi, h_hi, I, tk, bn_dn) && make_map(&dn.h_lo, h_lo, I, tk, bn_dn) &&
-              make_map(&dn.hs_hi, hs_hi, Is, T, bn_dn) && make_map(&dn.hs_lo, hs_lo, Is, T, bn_dn);
+    // gate_up: the gate rows of expert e are rows e*2I + [0, I) of W_gate_up and its up
+    // rows follow I rows later, so a map over the first E*2I - I rows with a plane stride
+    // of I rows reaches both (and no address past the tensor); likewise I_s for the
+    // shared expert. down: 128-token tiles read 256 weight rows per request.
+    const uint32_t dn_w_rows = bn_dn == 128 ? 256u : static_cast<uint32_t>(kGemmBM);
+    bool ok = make_pair_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E) * 2 * I - I,
+                            static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
+              make_pair_map(&gu.ws, ws_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2,
+                            kGemmBM) &&
+              make_map(&dn.w, w_down, I, static_cast<uint64_t>(E) * H, dn_w_rows) &&
+              make_map(&dn.ws, ws_down, Is, H, dn_w_rows) &&
+              make_pair_map(&dn.h, h_hi, I, tk, L.h_lo - L.h_hi, bn_dn) &&
+              make_pair_map(&dn.hs, hs_hi, Is, T, L.hs_lo - L.hs_hi, bn_dn);
     const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     ok = ok && make_store_map(&gu.st[0], h_hi, BF16, 2, I, tk) &&
          make_store_map(&gu.st[1], h_lo, BF16, 2, I, tk) &&

@@ -253,8 +253,8 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (tile + static_cast<int>(gridDim.x) < num_tiles)
                     nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
                 const CUtensorMap* tm = ti.shared ? &maps.ws : &maps.w;
+                // gate rows f.. of the expert; the map's second plane is the up rows
                 const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
-                const int row_u = row_g + (ti.shared ? a.I_s : a.I);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                         ok = false;
@@ -263,8 +263,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
                     ptx::mbar_arrive_expect_tx(fb, 2 * C::A_BYTES);
-                    ptx::tma_load_2d(sa, tm, fb, ks * kGemmBK, row_g, pol);
-                    ptx::tma_load_2d(sa + C::A_BYTES, tm, fb, ks * kGemmBK, row_u, pol);
+                    ptx::tma_load_3d(sa, tm, fb, ks * kGemmBK, row_g, 0, pol);  // gate, then up
                     armed |= 1u << s;
                     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) {
@@ -543,10 +542,8 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
-        ptx::prefetch_tmap(&maps.h_hi);
-        ptx::prefetch_tmap(&maps.h_lo);
-        ptx::prefetch_tmap(&maps.hs_hi);
-        ptx::prefetch_tmap(&maps.hs_lo);
+        ptx::prefetch_tmap(&maps.h);
+        ptx::prefetch_tmap(&maps.hs);
     }
     const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
     ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
@@ -573,8 +570,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
-                const CUtensorMap* thi = ti.shared ? &maps.hs_hi : &maps.h_hi;
-                const CUtensorMap* tlo = ti.shared ? &maps.hs_lo : &maps.h_lo;
+                const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
                 const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * kGemmBM;
                 for (int ks = 0; ks < ksteps; ++ks) {
                     if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
@@ -585,9 +581,8 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
                     ptx::mbar_arrive_expect_tx(fb, C::A_BYTES + 2 * C::B_BYTES);
                     ptx::tma_load_2d(sa, tw, fb, ks * kGemmBK, row_w, pol_w);
-                    ptx::tma_load_2d(sa + C::A_BYTES, thi, fb, ks * kGemmBK, ti.p0, pol_h);
-                    ptx::tma_load_2d(sa + C::A_BYTES + C::B_BYTES, tlo, fb, ks * kGemmBK, ti.p0,
-                                     pol_h);
+                    // the tile's h_hi rows, then its h_lo rows (two planes, one request)
+                    ptx::tma_load_3d(sa + C::A_BYTES, th, fb, ks * kGemmBK, ti.p0, 0, pol_h);
                     armed |= 1u << s;
                     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) {
@@ -763,10 +758,8 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
-        ptx::prefetch_tmap(&maps.h_hi);
-        ptx::prefetch_tmap(&maps.h_lo);
-        ptx::prefetch_tmap(&maps.hs_hi);
-        ptx::prefetch_tmap(&maps.hs_lo);
+        ptx::prefetch_tmap(&maps.h);
+        ptx::prefetch_tmap(&maps.hs);
         ptx::prefetch_tmap(&maps.st[1]);
     }
     const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
@@ -794,8 +787,7 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
-                const CUtensorMap* thi = ti.shared ? &maps.hs_hi : &maps.h_hi;
-                const CUtensorMap* tlo = ti.shared ? &maps.hs_lo : &maps.h_lo;
+                const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
                 // Rows past this expert's H (a ragged last block) read the next
                 // expert's rows or zero fill; their columns are never stored.
                 const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * C::NF;
@@ -807,11 +799,9 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
                     ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                    ptx::tma_load_2d(sa, thi, fb, ks * kGemmBK, ti.p0, pol_h);
-                    ptx::tma_load_2d(sa + C::A_BYTES, tlo, fb, ks * kGemmBK, ti.p0, pol_h);
+                    // h_hi then h_lo tile (one request), then 256 weight rows (one request)
+                    ptx::tma_load_3d(sa, th, fb, ks * kGemmBK, ti.p0, 0, pol_h);
                     ptx::tma_load_2d(sa + 2 * C::A_BYTES, tw, fb, ks * kGemmBK, row_w, pol_w);
-                    ptx::tma_load_2d(sa + 2 * C::A_BYTES + C::W_BYTES / 2, tw, fb, ks * kGemmBK,
-                                     row_w + C::NF / 2, pol_w);
                     armed |= 1u << s;
                     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) {

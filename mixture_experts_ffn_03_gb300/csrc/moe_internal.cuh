@@ -91,13 +91,19 @@ struct GemmArgs {
 };
 
 struct GemmMaps {
-    // Operand loads (128-byte swizzle).
-    CUtensorMap w;      // gate_up: W_gate_up as [E*2I, H]; down: W_down as [E*H, I]
-    CUtensorMap ws;     // gate_up: Ws_gate_up [2I_s, H]; down: Ws_down [H, I_s]
-    CUtensorMap h_hi;   // down only: h_hi [T*k, I]
-    CUtensorMap h_lo;
-    CUtensorMap hs_hi;  // down only: hs_hi [T, I_s]
-    CUtensorMap hs_lo;
+    // Operand loads (128-byte swizzle). A TMA request costs about the same
+    // time whatever its size, so pairs of tiles that are always loaded
+    // together come from one 3D box whose outer dimension (2) selects the
+    // member of the pair; the box lands as two consecutive tiles.
+    // gate_up: w / ws = W_gate_up as [E*2I - I rows, H] x {gate, up} (plane
+    //   stride I rows), Ws_gate_up as [I_s, H] x {gate, up}; boxes 64 x 128 x 2.
+    // down: w / ws = W_down as [E*H, I] and Ws_down as [H, I_s] (2D, boxes of
+    //   64 x 128 rows, or 64 x 256 rows for 128-token tiles); h / hs = the
+    //   h_hi and h_lo planes of [T*k, I] and [T, I_s], boxes 64 x rows x 2.
+    CUtensorMap w;
+    CUtensorMap ws;
+    CUtensorMap h;
+    CUtensorMap hs;
     // Epilogue stores (no swizzle), box of 32 columns x kEpiRows rows:
     // gate_up: st[0..3] = h_hi, h_lo, hs_hi, hs_lo; down: st[0] = y [T*k + T, H].
     // down with tokens on M: st[1] = y in 32 x 32 boxes with the 128-byte swizzle.
