@@ -317,6 +317,8 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     GemmArgs gd = ga;
     ga.rowtiles = rt_gu;
     gd.rowtiles = rt_dn;
+    ga.sched = meta + META_SCHED_GU;
+    gd.sched = meta + META_SCHED_DN;
 
     const size_t routed_min = tk < static_cast<size_t>(E) ? tk : static_cast<size_t>(E);
     const int F_gu = (I + kGemmBM - 1) / kGemmBM, F_s = (Is + kGemmBM - 1) / kGemmBM;

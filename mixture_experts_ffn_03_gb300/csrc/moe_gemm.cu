@@ -41,6 +41,7 @@ constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;
 
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kTileQ = 8;                          // tile descriptors in flight between roles
 constexpr int kThreads = 128 + kEpiWarps * 32;     // TMA, MMA, 2 gather warps, epilogue
 constexpr int kStgBytes = kEpiRows * kEpiCols * 4;  // one staging buffer (2 KB)
 
@@ -88,17 +89,6 @@ struct Cfg {
     static_assert(GU || BN <= 128, "down: h_hi and h_lo rows share one MMA of N <= 256");
 };
 
-struct Ctl {
-    uint64_t full_a[kMaxStages];  // TMA bytes landed
-    uint64_t full_b[kMaxStages];  // gathered rows landed (gate_up)
-    uint64_t empty[kMaxStages];   // MMAs reading the stage completed
-    uint64_t tfull[2];            // accumulator ready for the epilogue
-    uint64_t tempty[2];           // accumulator drained
-    uint64_t drain;               // MMA completion on the abort path
-    uint32_t tmem_base;
-    int abort;
-};
-
 struct Tile {
     int shared;  // 1: shared-expert tile
     int e;       // routed expert
@@ -108,31 +98,96 @@ struct Tile {
     int f;       // 128-row block of output features
 };
 
+struct Ctl {
+    uint64_t full_a[kMaxStages];  // TMA bytes landed
+    uint64_t full_b[kMaxStages];  // gathered rows landed (gate_up)
+    uint64_t empty[kMaxStages];   // MMAs reading the stage completed
+    uint64_t tfull[2];            // accumulator ready for the epilogue
+    uint64_t tempty[2];           // accumulator drained
+    uint64_t drain;               // MMA completion on the abort path
+    uint64_t tq_full[kTileQ];     // tile descriptor published
+    uint64_t tq_empty[kTileQ];    // tile descriptor read by every consumer role
+    Tile tq[kTileQ];              // tile descriptors, in processing order
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Ctl) <= 1024, "control block fits its shared-memory slot");
+
+// Tile order: the shared expert's tiles first (they carry the most tokens
+// per tile), then the routed row tiles, the feature blocks of a row tile
+// consecutive. A tile index past the end gives the sentinel (n_rows < 0).
+__device__ __forceinline__ int4 load_rowtile(int tile, int num_tiles, int shared_tiles, int F,
+                                             const GemmArgs& a) {
+    if (tile < shared_tiles || tile >= num_tiles) return make_int4(0, 0, 0, 0);
+    return a.rowtiles[(tile - shared_tiles) / F];
+}
+
 template <int BN>
-__device__ __forceinline__ Tile decode_tile(int tile, int routed_tiles, int F, int F_s,
-                                            const GemmArgs& a) {
+__device__ __forceinline__ Tile make_tile(int tile, int4 r, int num_tiles, int shared_tiles,
+                                          int F, int F_s, const GemmArgs& a) {
     Tile ti;
-    if (tile < routed_tiles) {
-        const int rt = tile / F;
-        ti.f = tile - rt * F;
-        const int4 r = a.rowtiles[rt];
+    if (tile >= num_tiles) {
         ti.shared = 0;
-        ti.e = r.x;
-        ti.m0 = r.y;
-        ti.n_rows = r.z;
-        ti.p0 = r.w;
-    } else {
-        const int t2 = tile - routed_tiles;
-        const int rt = t2 / F_s;
-        ti.f = t2 - rt * F_s;
+        ti.e = 0;
+        ti.m0 = 0;
+        ti.n_rows = -1;
+        ti.p0 = 0;
+        ti.f = 0;
+    } else if (tile < shared_tiles) {
+        const int rt = tile / F_s;
+        ti.f = tile - rt * F_s;
         ti.shared = 1;
         ti.e = 0;
         ti.m0 = rt * BN;
         ti.n_rows = min(BN, a.T - ti.m0);
         ti.p0 = ti.m0;
+    } else {
+        const int t2 = tile - shared_tiles;
+        const int rt = t2 / F;
+        ti.f = t2 - rt * F;
+        ti.shared = 0;
+        ti.e = r.x;
+        ti.m0 = r.y;
+        ti.n_rows = r.z;
+        ti.p0 = r.w;
     }
     return ti;
 }
+
+// Dynamic tile scheduling, run by the TMA producer thread: a CTA's first tile
+// is blockIdx.x, every further tile is claimed from a global counter. The
+// claim and the row-tile load for the next tile are issued one tile ahead, so
+// their latency hides behind the current tile's loads.
+template <int BN>
+struct TileSched {
+    int nxt;    // tile after the current one
+    int after;  // claim for the tile after nxt (read one tile later)
+    int4 raw;   // row-tile entry of nxt
+    int num_tiles, shared_tiles, F, F_s;
+
+    __device__ __forceinline__ Tile start(int n_tiles, int s_tiles, int f, int f_s,
+                                          const GemmArgs& a) {
+        num_tiles = n_tiles;
+        shared_tiles = s_tiles;
+        F = f;
+        F_s = f_s;
+        const int first = blockIdx.x;
+        nxt = first < num_tiles ? static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1) : num_tiles;
+        return make_tile<BN>(first, load_rowtile(first, num_tiles, shared_tiles, F, a), num_tiles,
+                             shared_tiles, F, F_s, a);
+    }
+    // At the start of a tile: claim the tile after next and load next's row tile.
+    __device__ __forceinline__ void prefetch(const GemmArgs& a) {
+        raw = load_rowtile(nxt, num_tiles, shared_tiles, F, a);
+        after = nxt < num_tiles ? static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1) : num_tiles;
+    }
+    // At the end of a tile: the next tile's descriptor.
+    __device__ __forceinline__ bool next(Tile& ti, const GemmArgs& a) {
+        ti = make_tile<BN>(nxt, raw, num_tiles, shared_tiles, F, F_s, a);
+        nxt = after;
+        return true;
+    }
+};
 
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        unsigned* err, unsigned code) {
@@ -168,10 +223,40 @@ __device__ __noinline__ void wait_bounded(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t* b) { return ptx::smem_u32(b); }
 
+// Publish the next tile descriptor (the producer); false on abort or timeout.
+__device__ __forceinline__ bool tq_publish(Ctl* ctl, int& s, uint32_t& ph, const Tile& ti,
+                                           volatile int* abort_flag, unsigned* err, unsigned code) {
+    if (!wait_bar(bar_addr(&ctl->tq_empty[s]), ph ^ 1u, abort_flag, err, code)) return false;
+    ctl->tq[s] = ti;
+    ptx::mbar_arrive(bar_addr(&ctl->tq_full[s]));  // release: the descriptor is visible
+    if (++s == kTileQ) {
+        s = 0;
+        ph ^= 1u;
+    }
+    return true;
+}
+
+// Read the next tile descriptor (a consumer role; `single` when the role is
+// one thread, else the whole warp calls it and lane 0 releases the slot).
+// False at the end of the sequence, on abort or on timeout.
+__device__ __forceinline__ bool tq_read(Ctl* ctl, int& s, uint32_t& ph, Tile& ti, bool single,
+                                        volatile int* abort_flag, unsigned* err, unsigned code) {
+    if (!wait_bar(bar_addr(&ctl->tq_full[s]), ph, abort_flag, err, code)) return false;
+    ti = ctl->tq[s];
+    if (!single) __syncwarp();
+    if (single || (threadIdx.x & 31) == 0) ptx::mbar_arrive(bar_addr(&ctl->tq_empty[s]));
+    if (++s == kTileQ) {
+        s = 0;
+        ph ^= 1u;
+    }
+    return ti.n_rows >= 0;
+}
+
 // Common set-up: barriers, TMEM allocation. Returns the TMEM base address.
 // C is the kernel's shared-memory / TMEM configuration.
+// tq_consumers: warps (or single threads) that read each tile descriptor.
 template <class C>
-__device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp) {
+__device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp, int tq_consumers) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar_addr(&ctl->full_a[s]), 1);
@@ -183,6 +268,10 @@ __device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp) {
             ptx::mbar_init(bar_addr(&ctl->tempty[s]), kEpiWarps);
         }
         ptx::mbar_init(bar_addr(&ctl->drain), 1);
+        for (int q = 0; q < kTileQ; ++q) {
+            ptx::mbar_init(bar_addr(&ctl->tq_full[q]), 1);
+            ptx::mbar_init(bar_addr(&ctl->tq_empty[q]), tq_consumers);
+        }
         ctl->abort = 0;
         ptx::fence_mbar_init();
     }
@@ -229,13 +318,13 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
     }
-    const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + 2 + kEpiWarps);
     ptx::griddep_wait();  // routing, tile lists and the slot order come from earlier kernels
 
     const int R = a.meta[META_RT_GU];
     const int F = (a.I + kGemmBM - 1) / kGemmBM, F_s = (a.I_s + kGemmBM - 1) / kGemmBM;
-    const int routed_tiles = R * F;
-    const int num_tiles = routed_tiles + ((a.T + BN - 1) / BN) * F_s;
+    const int shared_tiles = ((a.T + BN - 1) / BN) * F_s;
+    const int num_tiles = R * F + shared_tiles;
     const int ksteps = a.H / kGemmBK;
     volatile int* abort_flag = &ctl->abort;
     unsigned* err = a.err;
@@ -247,11 +336,14 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
             bool ok = true;
-            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-                if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+            TileSched<BN> sch;
+            Tile ti = sch.start(num_tiles, shared_tiles, F, F_s, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            ok = tq_publish(ctl, qs, qph, ti, abort_flag, err, code);
+            for (; ok && ti.n_rows >= 0;
+                 ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
+                sch.prefetch(a);
                 const CUtensorMap* tm = ti.shared ? &maps.ws : &maps.w;
                 // gate rows f.. of the expert; the map's second plane is the up rows
                 const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
@@ -279,11 +371,10 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0, as = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-                if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            Tile ti;
+            while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
                 const int n_mma = max(16, (ti.n_rows + 15) & ~15);
                 const uint32_t idesc = C::TS ? ptx::idesc_bf16_f32(kGemmBM, 2 * kGemmBM)
                                              : ptx::idesc_bf16_f32(kGemmBM, n_mma);
@@ -348,11 +439,10 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-            if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+        int qs = 0;
+        uint32_t qph = 0;
+        Tile ti;
+        while (ok && tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             uint32_t trow[RPT];  // token (hidden row) of each row this thread copies
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
@@ -392,11 +482,10 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         const int we = warp - 4, q = warp & 3, half = we >> 2;
         int as = 0;
         uint32_t aph = 0;
-        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-            if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+        int qs = 0;
+        uint32_t qph = 0;
+        Tile ti;
+        while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int r0 = q * 32;  // first token row of this warp's lane quadrant
@@ -458,11 +547,10 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
-        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F_s, a);
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-            if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F_s, a);
+        int qs = 0;
+        uint32_t qph = 0;
+        Tile ti;
+        while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int n_feat = ti.shared ? a.I_s : a.I;
@@ -545,13 +633,13 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.h);
         ptx::prefetch_tmap(&maps.hs);
     }
-    const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + kEpiWarps);
     ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
 
     const int R = a.meta[META_RT_DN];
     const int F = (a.H + kGemmBM - 1) / kGemmBM;
-    const int routed_tiles = R * F;
-    const int num_tiles = routed_tiles + ((a.T + BN - 1) / BN) * F;
+    const int shared_tiles = ((a.T + BN - 1) / BN) * F;
+    const int num_tiles = R * F + shared_tiles;
     volatile int* abort_flag = &ctl->abort;
     unsigned* err = a.err;
     const unsigned code = ERR_DOWN_TIMEOUT;
@@ -563,11 +651,14 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
             bool ok = true;
-            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-                if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
+            TileSched<BN> sch;
+            Tile ti = sch.start(num_tiles, shared_tiles, F, F, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            ok = tq_publish(ctl, qs, qph, ti, abort_flag, err, code);
+            for (; ok && ti.n_rows >= 0;
+                 ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
+                sch.prefetch(a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
                 const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
@@ -598,11 +689,10 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0, as = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-                if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                    nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            Tile ti;
+            while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 // h_lo rows sit right after the BN h_hi rows in shared memory, so
                 // one MMA of N = BN + rows covers both halves: accumulator
@@ -658,11 +748,10 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         int as = 0;
         uint32_t aph = 0;
         const int shared_row0 = a.T * a.k;
-        Tile nxt = decode_tile<BN>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-            if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                nxt = decode_tile<BN>(tile + gridDim.x, routed_tiles, F, F, a);
+        int qs = 0;
+        uint32_t qph = 0;
+        Tile ti;
+        while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
@@ -762,13 +851,13 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.hs);
         ptx::prefetch_tmap(&maps.st[1]);
     }
-    const uint32_t tmem_base = gemm_setup<C>(ctl, warp);
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + kEpiWarps);
     ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
 
     const int R = a.meta[META_RT_DN];
     const int F = (a.H + C::NF - 1) / C::NF;
-    const int routed_tiles = R * F;
-    const int num_tiles = routed_tiles + ((a.T + C::BM - 1) / C::BM) * F;
+    const int shared_tiles = ((a.T + C::BM - 1) / C::BM) * F;
+    const int num_tiles = R * F + shared_tiles;
     volatile int* abort_flag = &ctl->abort;
     unsigned* err = a.err;
     const unsigned code = ERR_DOWN_TIMEOUT;
@@ -780,11 +869,14 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
             bool ok = true;
-            Tile nxt = decode_tile<C::BM>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-                if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                    nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
+            TileSched<C::BM> sch;
+            Tile ti = sch.start(num_tiles, shared_tiles, F, F, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            ok = tq_publish(ctl, qs, qph, ti, abort_flag, err, code);
+            for (; ok && ti.n_rows >= 0;
+                 ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
+                sch.prefetch(a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
                 const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
@@ -817,11 +909,10 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             int s = 0, as = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            Tile nxt = decode_tile<C::BM>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-                if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                    nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            Tile ti;
+            while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
                 const int n_f = min(C::NF, a.H - ti.f * C::NF);  // a multiple of 64
                 const uint32_t idesc = ptx::idesc_bf16_f32(C::BM, n_f);
@@ -878,11 +969,10 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         int as = 0;
         uint32_t aph = 0;
         const int shared_row0 = a.T * a.k;
-        Tile nxt = decode_tile<C::BM>(blockIdx.x < num_tiles ? blockIdx.x : 0, routed_tiles, F, F, a);
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile ti = nxt;  // next tile's descriptor is loaded one tile ahead
-            if (tile + static_cast<int>(gridDim.x) < num_tiles)
-                nxt = decode_tile<C::BM>(tile + gridDim.x, routed_tiles, F, F, a);
+        int qs = 0;
+        uint32_t qph = 0;
+        Tile ti;
+        while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
             const int r0 = q * 32;

@@ -41,6 +41,8 @@ enum : int {
     META_RT_GU = 1,        // routed row tiles of the gate_up GEMM
     META_RT_DN = 2,        // routed row tiles of the down GEMM
     META_TICKET = 3,       // block-completion counter of the count/scan kernel
+    META_SCHED_GU = 4,     // tiles claimed by the gate_up GEMM's CTAs (past their first)
+    META_SCHED_DN = 5,     // tiles claimed by the down GEMM's CTAs
     META_WORDS = 64,
 };
 
@@ -81,6 +83,7 @@ struct GemmArgs {
     const int* offsets;
     const int4* rowtiles;   // routed row tiles {expert, first row, rows, sorted position}
     const int* meta;
+    int* sched;             // this GEMM's tile-claim counter (zero at launch)
     const float* gate_logit;
     __nv_bfloat16* h_hi;
     __nv_bfloat16* h_lo;
