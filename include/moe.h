@@ -120,8 +120,12 @@ const char* moe_status_string(moe_status s);
  *   tokens ascending within an expert), inv [T k] int32 (position of slot
  *   t*k+j), h_hi / h_lo [T k, I] bf16 (SwiGLU activation of each routed slot
  *   in sorted order, as a high + low bf16 pair), hs_hi / hs_lo [T, I_s] bf16
- *   (shared expert activation), y [T k + T, H] fp32 (rows [0, T k): routed
- *   expert outputs in sorted order; rows T k + t: gated shared output). */
+ *   (shared expert activation), y [T k + T, H] (rows [0, T k): routed
+ *   expert outputs in sorted order; rows T k + t: gated shared output).
+ *   y holds fp32 values, except when the mean expert group is large enough
+ *   for 128-token down tiles (1.25 T k / E > 64): then each value is the top
+ *   three bytes of its fp32 encoding rounded to nearest even (rows of 3 H
+ *   bytes, a 16-bit significand). The region is sized for fp32 either way. */
 typedef struct {
     size_t topk_ids, topk_w, gate_logit, counts, offsets, perm, inv;
     size_t h_hi, h_lo, hs_hi, hs_lo, y;

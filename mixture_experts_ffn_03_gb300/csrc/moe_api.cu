@@ -131,17 +131,17 @@ bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 y [outer, inner] written by the tokens-on-M down epilogue in boxes of
-// 32 columns x 32 rows staged with the 128-byte swizzle.
-bool make_y_store_map_sw128(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
+// y of 128-token down tiles: rows of H 24-bit floats (3 bytes each, byte
+// tensor [outer, 3 * inner]) written in boxes of 96 bytes x 32 rows.
+bool make_y24_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint64_t dims[2] = {3 * inner, outer};
+    cuuint64_t strides[1] = {3 * inner};
+    cuuint32_t box[2] = {96, 32};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -292,7 +292,7 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
          make_store_map(&gu.st[2], hs_hi, BF16, 2, Is, T) &&
          make_store_map(&gu.st[3], hs_lo, BF16, 2, Is, T) &&
          make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
-         make_y_store_map_sw128(&dn.st[1], y, H, tk + T);
+         make_y24_store_map(&dn.st[1], y, H, tk + T);
     if (!ok) return MOE_ERR_CUDA;
 
     GemmArgs ga{};
@@ -365,7 +365,9 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
                          st)) != cudaSuccess)
         return MOE_ERR_CUDA;
     mark_stage(5, st);
-    if ((launch_combine(T, H, k, y, topk_w, inv, static_cast<__nv_bfloat16*>(out), st)) !=
+    // 128-token down tiles leave y as 24-bit floats, the other widths as fp32.
+    if ((launch_combine(T, H, k, y, bn_dn == 128, topk_w, inv, static_cast<__nv_bfloat16*>(out),
+                        st)) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     mark_stage(6, st);

@@ -805,6 +805,14 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     gemm_teardown<C>(tmem_base, warp);
 }
 
+// y of the 128-token down tiles is stored with a 16-bit significand: the top
+// three bytes of the fp32 encoding, rounded to nearest even on the dropped
+// byte (NaN stays NaN). The result's low byte is dropped by the caller.
+__device__ __forceinline__ uint32_t y24_round(uint32_t b) {
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u) return b | 0x00400000u;
+    return b + 0x7Fu + ((b >> 8) & 1u);
+}
+
 // ====================================================== down, tokens on M
 // Tiles of up to 128 tokens of one expert against 256 output features:
 // D[token, 0:N] = h_hi W^T + h_lo W^T, where the h_hi and h_lo tiles are two A
@@ -819,7 +827,7 @@ struct DownTs {
     static constexpr int A_BYTES = BM * kGemmBK * 2;        // 16 KB: h_hi or h_lo tile
     static constexpr int W_BYTES = NF * kGemmBK * 2;        // 32 KB: weight tile (two boxes)
     static constexpr int STAGE_BYTES = 2 * A_BYTES + W_BYTES;
-    static constexpr int STG_BYTES = 32 * 32 * 4;           // one warp's 32 x 32 fp32 store box
+    static constexpr int STG_BYTES = 32 * 32 * 4;           // one warp's store box (32 rows x 96 B used)
     static constexpr int EPI_BYTES = kEpiWarps * STG_BYTES;
     static constexpr int CTL_BYTES = 1024;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - EPI_BYTES - CTL_BYTES) / STAGE_BYTES;
@@ -959,10 +967,10 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     } else if (warp >= 4) {  // ------------------------------ epilogue (warps 4-11)
         // Tokens on TMEM lanes: warp we owns the token rows 32*(warp % 4).. and
         // the features [128*(we / 4), +128) of the tile, drained 32 at a time.
-        // Each thread holds 32 consecutive features of its token's y row and
-        // writes them into the warp's 128-byte-swizzled staging box (conflict
-        // free), which goes out as one 32 x 32 TMA store; a warp whose token
-        // rows are only partly valid stores its valid rows directly.
+        // Each thread packs 32 consecutive features of its token's y row (24-bit
+        // floats, 96 bytes) into the warp's staging box, which goes out as one
+        // 96-byte x 32-row TMA store; a warp whose token rows are only partly
+        // valid stores its valid rows directly.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
         uint8_t* stg = smem + C::EPI_OFF + we * C::STG_BYTES;
         const uint32_t stg_u32 = ptx::smem_u32(stg);
@@ -990,36 +998,41 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     const int f0 = ti.f * C::NF + col;
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(tb + col, v);
+                    // The thread's 32 values of its token's y row, rounded to 24-bit
+                    // floats and packed into 96 bytes (24 words).
+                    ptx::tmem_ld_wait();
+                    uint32_t w[24];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t r0 = y24_round(__float_as_uint(__uint_as_float(v[4 * q]) * scale));
+                        const uint32_t r1 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 1]) * scale));
+                        const uint32_t r2 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 2]) * scale));
+                        const uint32_t r3 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 3]) * scale));
+                        w[3 * q] = __byte_perm(r0, r1, 0x5321);
+                        w[3 * q + 1] = __byte_perm(r1, r2, 0x6532);
+                        w[3 * q + 2] = __byte_perm(r2, r3, 0x7653);
+                    }
                     if (rows_valid >= 32) {
                         if (lane == 0) ptx::bulk_wait_read<0>();  // staging box free again
-                        ptx::tmem_ld_wait();
                         __syncwarp();
-                        const uint32_t row_addr = stg_u32 + lane * 128;
+                        const uint32_t row_addr = stg_u32 + lane * 96;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            ptx::st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4),
-                                              __uint_as_float(v[4 * j]) * scale,
-                                              __uint_as_float(v[4 * j + 1]) * scale,
-                                              __uint_as_float(v[4 * j + 2]) * scale,
-                                              __uint_as_float(v[4 * j + 3]) * scale);
+                        for (int j = 0; j < 6; ++j)
+                            ptx::st_shared_v4u(row_addr + 16 * j, w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                                               w[4 * j + 3]);
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&maps.st[1], stg_u32, f0, row0);
+                            ptx::tma_store_2d(&maps.st[1], stg_u32, 3 * f0, row0);
                             ptx::bulk_commit();
                         }
-                    } else {
-                        ptx::tmem_ld_wait();
-                        if (lane < rows_valid) {
-                            float4* dst = reinterpret_cast<float4*>(
-                                a.y + static_cast<size_t>(row0 + lane) * a.H + f0);
+                    } else if (lane < rows_valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            reinterpret_cast<uint8_t*>(a.y) + static_cast<size_t>(row0 + lane) * 3 * a.H +
+                            3 * f0);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                dst[j] = make_float4(__uint_as_float(v[4 * j]) * scale,
-                                                     __uint_as_float(v[4 * j + 1]) * scale,
-                                                     __uint_as_float(v[4 * j + 2]) * scale,
-                                                     __uint_as_float(v[4 * j + 3]) * scale);
-                        }
+                        for (int j = 0; j < 6; ++j)
+                            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                     }
                 }
             }

@@ -71,7 +71,7 @@ cudaError_t launch_count_scan(int T, int E, int k, int bn_gu, int bn_dn, const i
                               int4* rt_dn, int* meta, int* counts_out, cudaStream_t st);
 cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
                            const int* offsets, int* perm, int* inv, cudaStream_t st);
-cudaError_t launch_combine(int T, int H, int k, const float* y, const float* topk_w,
+cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st);
 
 // Grouped GEMMs (moe_gemm.cu).

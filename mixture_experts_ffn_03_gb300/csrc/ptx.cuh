@@ -119,13 +119,13 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
     return p;
 }
 
-// 16-byte shared-memory store at a 32-bit shared address.
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
+// 16-byte shared-memory store of four words at a 32-bit shared address.
+__device__ __forceinline__ void st_shared_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
                  : "memory");
 }
-
 // ------------------------------------------------------- Ampere cp.async
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
