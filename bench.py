@@ -54,6 +54,19 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(local_ms: float, dist, device) -> float:
+    """The slowest rank's timed total: every rank's time is all-reduced with MAX."""
+    import torch
+    t = torch.tensor([local_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the tokens every replica processed over the slowest rank's time."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 def workload_name(cfg):
     sf = "softmax" if cfg.score_fn == 0 else "sigmoid"
     return (f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} I={cfg.I} I_s={cfg.I_s} "
@@ -302,9 +315,7 @@ def main():
     stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev]
                 for j in range(moe.NUM_STAGES)]
     if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dist, dev)
 
     # The same step replayed as a CUDA graph (launch overhead removed).
     graph = None
@@ -357,7 +368,7 @@ def main():
         return 0
 
     peaks = load_peaks()
-    value = world * T * K / (total_ms / 1e3)
+    value = job_tokens_per_s(world, T, K, total_ms)
     ms_step = total_ms / K
     gu_ms = statistics.mean(stage_ms[3])
     dn_ms = statistics.mean(stage_ms[4])
