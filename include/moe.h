@@ -152,6 +152,16 @@ moe_status moe_set_stage_events(void* const* events, int n_events);
  * invalid sizes or T = 0. */
 int moe_launch_count(const moe_dims* d);
 
+/* Self-test of the kernels' bounded waits (failure detection without a GPU
+ * fault): clears the status word at the start of `workspace` (256-byte
+ * aligned device memory, at least 4 bytes) and enqueues one CTA on
+ * `cuda_stream` that waits on a barrier nothing ever completes, with the same
+ * bounded wait the GEMM pipelines use. The wait gives up after its time limit
+ * (2 s) and sets a bit of the status word; moe_device_status(workspace,
+ * stream) then returns MOE_ERR_DEVICE_TIMEOUT and the context stays usable.
+ * Returns MOE_ERR_WORKSPACE for a missing or misaligned workspace. */
+moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream);
+
 /*
  * Allocation-free expert histogram. The pages have no counterpart to this
  * entry point; it exists for callers that cannot allocate device memory,

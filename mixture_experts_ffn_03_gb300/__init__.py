@@ -17,12 +17,19 @@ SOFTMAX = 0
 SIGMOID = 1
 
 MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_CAPACITY = 6
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
                 6: "MOE_ERR_CAPACITY"}
 
 EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
-            "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count"]
+            "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count",
+            "moe_selftest_wait_limit"]
 NUM_STAGES = 6
 STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
 
@@ -72,6 +79,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_set_stage_events.restype = ctypes.c_int
     lib.moe_launch_count.argtypes = [ctypes.POINTER(MoEDims)]
     lib.moe_launch_count.restype = ctypes.c_int
+    lib.moe_selftest_wait_limit.argtypes = [P, P]
+    lib.moe_selftest_wait_limit.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -140,6 +149,12 @@ def forward_raw(dims: MoEDims, hidden, logits, w_gate_up, w_down, ws_gate_up, ws
 
 def device_status(workspace, stream=None) -> int:
     return int(load_library().moe_device_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def selftest_wait_limit(workspace, stream=None) -> int:
+    """Enqueue the bounded-wait self-test on `workspace`'s status word (see
+    moe_selftest_wait_limit in include/moe.h); returns the call's status."""
+    return int(load_library().moe_selftest_wait_limit(_ptr(workspace), _stream_handle(stream)))
 
 
 class MoELayer:

@@ -393,6 +393,16 @@ MOE_API moe_status moe_set_stage_events(void* const* events, int n_events) {
     return MOE_OK;
 }
 
+MOE_API moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    unsigned* err = static_cast<unsigned*>(workspace);
+    if (cudaMemsetAsync(err, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_wait_limit_selftest(err, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 MOE_API moe_status moe_device_status(const void* workspace, void* cuda_stream) {
     if (!workspace) return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);

@@ -1096,6 +1096,20 @@ cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_ti
     }
 }
 
+// Self-test of the bounded barrier wait the GEMM roles use: one thread waits
+// on an mbarrier that nothing arrives on. The wait must give up after its
+// time limit, set `code` in the status word and leave the kernel normally.
+__global__ void __launch_bounds__(32, 1) wait_limit_selftest_kernel(unsigned* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    ptx::mbar_init(bar_addr(&bar), 1);
+    ptx::fence_mbar_init();
+    if (wait_bar(bar_addr(&bar), 0u, &abort_flag, err, ERR_GATE_UP_TIMEOUT))
+        atomicOr(err, 0x80000000u);  // the wait returned "complete": the test fails
+}
+
 }  // namespace
 
 bool gemm_bn_supported(int bn) {
@@ -1105,6 +1119,11 @@ bool gemm_bn_supported(int bn) {
 cudaError_t launch_gate_up(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
                            int num_sms, cudaStream_t st) {
     return dispatch<true>(bn, maps, a, max_tiles, num_sms, st);
+}
+
+cudaError_t launch_wait_limit_selftest(unsigned* err, cudaStream_t st) {
+    wait_limit_selftest_kernel<<<1, 32, 0, st>>>(err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_down(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,

@@ -117,6 +117,8 @@ struct GemmMaps {
 bool gemm_bn_supported(int bn);
 cudaError_t launch_gate_up(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
                            int num_sms, cudaStream_t st);
+// One CTA that waits on an mbarrier nothing arrives on (bounded wait self-test).
+cudaError_t launch_wait_limit_selftest(unsigned* err, cudaStream_t st);
 cudaError_t launch_down(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
                         int num_sms, cudaStream_t st);
 
