@@ -213,3 +213,23 @@ def test_nonfinite_logits_stay_in_range(moe):
     # rows with finite logits still match the oracle exactly
     o_ids, _ = oracle.route(inp["logits"][4:], cfg.k, cfg.score_fn)
     assert np.array_equal(g[4:], o_ids)
+
+
+def test_host_pipeline_matches_forward(moe):
+    """The overlapped serving loop (two staging sets, a copy stream) gives the
+    same bytes as plain forward calls, for alternating inputs."""
+    cfg = wl.CONFIGS["tiny"].with_tokens(96)
+    inps = [wl.make_inputs(cfg, seed=s) for s in (11, 12)]
+    dev = torch.device("cuda")
+    w = {n: t.to(dev) for n, t in inps[0].items()}
+    layer = moe.MoELayer(w["w_gate_up"], w["w_down"], w["ws_gate_up"], w["ws_down"], w["w_g"],
+                         cfg.k, cfg.score_fn)
+    want = [layer.forward(i["hidden"].to(dev), i["logits"].to(dev)).cpu() for i in inps]
+    hosts = [(i["hidden"].pin_memory(), i["logits"].pin_memory()) for i in inps]
+    outs = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+    pipe = moe.HostPipeline(layer, cfg.T)
+    for s in range(6):
+        pipe.submit(hosts[s % 2][0], hosts[s % 2][1], outs[s])
+    pipe.drain()
+    for s in range(6):
+        assert torch.equal(outs[s], want[s % 2]), s
