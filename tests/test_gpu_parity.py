@@ -233,3 +233,24 @@ def test_host_pipeline_matches_forward(moe):
     pipe.drain()
     for s in range(6):
         assert torch.equal(outs[s], want[s % 2]), s
+
+
+def _random_configs(n, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 65))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        out.append(wl.MoEConfig(f"rand{i}", T=int(rng.integers(1, 700)),
+                                H=64 * int(rng.integers(1, 9)), E=E, k=k,
+                                I=64 * int(rng.integers(1, 5)), I_s=64 * int(rng.integers(1, 5)),
+                                score_fn=int(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_configs(24), ids=lambda c: f"{c.name}-T{c.T}-H{c.H}-E{c.E}-k{c.k}")
+def test_random_small_shapes(moe, cfg):
+    """Seeded random shapes: every tile width the host can pick, ragged H / I / I_s
+    multiples of 64, small and large groups, both score functions."""
+    inp = wl.make_inputs(cfg, seed=cfg.T)
+    run_case(moe, cfg, inp)
