@@ -48,6 +48,9 @@ def _bind(lib):
     lib.oracle_expert_counts.argtypes = [i, i, i, P, P]
     lib.oracle_expert_counts.restype = None
     lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i] + [P] * 8 + [i] + [P] * 5 + [i]
+    lib.oracle_mxfp8_to_bf16.argtypes = [i, i, P, P, P]
+    lib.oracle_mxfp8_to_bf16.restype = i
+    lib.oracle_e4m3_table.argtypes = [P]
     lib.oracle_moe_forward.restype = i
     return lib
 
@@ -145,3 +148,63 @@ def moe_forward(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=
                                  n_threads or default_threads())
     assert bad == 0, f"{bad} tokens: fp64 score order contradicts the logit order"
     return dict(out=out, ids=ids, weights=w, gate=gate)
+
+
+def e4m3_table(lib_path: str | None = None) -> np.ndarray:
+    """Values of the 256 FP8 E4M3 codes (NaN for the two NaN codes)."""
+    lib = _load(lib_path)
+    out = np.empty(256, dtype=np.float64)
+    lib.oracle_e4m3_table(_ptr(out))
+    return out
+
+
+def mxfp8_to_bf16(codes, scales, lib_path: str | None = None):
+    """Exact dequantisation of MXFP8 weights to bf16 bit patterns.
+
+    codes: uint8 [..., rows, cols] E4M3 codes; scales: uint8 [..., cols/32, rows]
+    UE8M0 codes (leading dimensions: experts). Returns uint16 bf16 bits of the
+    same shape as codes; raises if any value is not exactly a bf16 value."""
+    lib = _load(lib_path)
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    sc = np.ascontiguousarray(np.asarray(scales, dtype=np.uint8))
+    rows, cols = c.shape[-2], c.shape[-1]
+    lead = int(np.prod(c.shape[:-2])) if c.ndim > 2 else 1
+    c2 = c.reshape(lead, rows, cols)
+    s2 = sc.reshape(lead, cols // 32, rows)
+    out = np.empty((lead, rows, cols), dtype=np.uint16)
+    for e in range(lead):
+        ce, se, oe = np.ascontiguousarray(c2[e]), np.ascontiguousarray(s2[e]), out[e]
+        bad = lib.oracle_mxfp8_to_bf16(rows, cols, _ptr(ce), _ptr(se), _ptr(oe))
+        if bad:
+            raise ValueError(f"{bad} MXFP8 values are not exact bf16 values")
+    return out.reshape(c.shape)
+
+
+def moe_forward_mxfp8(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=None,
+                      lib_path: str | None = None):
+    """The layer with MXFP8 routed-expert weights: the weights are dequantised
+    exactly (every MXFP8 value is a bf16 value) and the fp64 layer runs on them.
+    inputs holds w_gate_up_q / w_gate_up_s / w_down_q / w_down_s instead of
+    w_gate_up / w_down."""
+    import torch
+    wgu = mxfp8_to_bf16(_np(inputs["w_gate_up_q"]), _np(inputs["w_gate_up_s"]), lib_path)
+    wd = mxfp8_to_bf16(_np(inputs["w_down_q"]), _np(inputs["w_down_s"]), lib_path)
+    plain = {n: v for n, v in inputs.items() if not n.startswith(("w_gate_up", "w_down"))}
+    plain["w_gate_up"] = torch.from_numpy(wgu.view(np.int16)).view(torch.bfloat16)
+    plain["w_down"] = torch.from_numpy(wd.view(np.int16)).view(torch.bfloat16)
+    return moe_forward(plain, k, score_fn, tokens=tokens, gate_override=gate_override,
+                       lib_path=lib_path)
+
+
+def _np(t):
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            t = t.detach().cpu()
+            if t.dtype == torch.float8_e4m3fn:
+                t = t.view(torch.uint8)
+            return t.numpy()
+    except ImportError:
+        pass
+    return np.asarray(t)
+

@@ -134,6 +134,69 @@ void oracle_expert_counts(int T, int E, int k, const int32_t* ids, int32_t* coun
         for (int j = 0; j < k; ++j) counts[ids[(size_t)t * k + j]] += 1;
 }
 
+/*
+ * MXFP8 expert weights (OCP Microscaling formats, MXFP8 with E4M3 elements):
+ * each run of 32 consecutive K elements of a weight row shares one UE8M0
+ * scale 2^(s - 127); an element is an FP8 E4M3 code (sign, 4-bit exponent
+ * with bias 7, 3-bit mantissa; exponent 0 holds the subnormals m * 2^-9;
+ * S.1111.111 is NaN; there are no infinities). The pages name block-FP8
+ * expert banks ("qwen3_5_moe is TP=1-only ...", first comment) without a
+ * block layout; this is the plainest block-scaled FP8 with power-of-two
+ * scales.
+ */
+static double e4m3_value(uint8_t b) {
+    const int sign = b >> 7, e = (b >> 3) & 0xF, m = b & 7;
+    double v;
+    if (e == 0xF && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+static double ue8m0_value(uint8_t s) { return s == 255 ? NAN : ldexp(1.0, (int)s - 127); }
+
+/* bf16 bit pattern of a double that bf16 represents exactly (finite, at most
+ * 8 significant bits, normal or subnormal range); returns -1 if it does not. */
+static int32_t exact_bf16_bits(double v) {
+    float f = (float)v;
+    if ((double)f != v) return -1;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if (u & 0xFFFFu) return -1;
+    return (int32_t)(u >> 16);
+}
+
+/*
+ * Dequantise an MXFP8 matrix of `rows` rows and `cols` K elements (cols a
+ * multiple of 32): codes [rows, cols], scales [cols / 32, rows] (the scale of
+ * row r, K block j at j * rows + r). Every value is exactly a bf16 value
+ * (at most 4 significant bits); out gets its bf16 bit pattern. Returns the
+ * number of elements that were not exact (NaN codes or scales, or results
+ * outside the bf16 range).
+ */
+int oracle_mxfp8_to_bf16(int rows, int cols, const uint8_t* codes, const uint8_t* scales,
+                         uint16_t* out) {
+    int bad = 0;
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            const double v = e4m3_value(codes[(size_t)r * cols + c]) *
+                             ue8m0_value(scales[(size_t)(c / 32) * rows + r]);
+            const int32_t bits = exact_bf16_bits(v);
+            if (bits < 0) {
+                ++bad;
+                out[(size_t)r * cols + c] = 0x7FC0u;
+            } else {
+                out[(size_t)r * cols + c] = (uint16_t)bits;
+            }
+        }
+    return bad;
+}
+
+/* Value table of the 256 E4M3 codes (for the oracle's pins). */
+void oracle_e4m3_table(double* out) {
+    for (int b = 0; b < 256; ++b) out[b] = e4m3_value((uint8_t)b);
+}
+
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /*
