@@ -73,18 +73,20 @@ def workload_name(cfg):
             f"{sf}+renorm{', zipf-skewed logits' if cfg.skew else ''}")
 
 
-def algorithmic_work(cfg, counts):
-    """Layer FLOPs and touched bytes from the actual routing (counts per expert)."""
+def algorithmic_work(cfg, counts, wbytes=2.0):
+    """Layer FLOPs and touched bytes from the actual routing (counts per expert);
+    wbytes = bytes per expert weight (2 for bf16, 1 + 1/32 for MXFP8 codes and
+    scales)."""
     T, H, E, k, I, I_s = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_s
     touched = int(sum(1 for c in counts if c > 0))
     flops = 6.0 * H * I * T * k + 6.0 * H * I_s * T + 2.0 * H * T
-    w_routed = touched * 6.0 * I * H
-    w_shared = 6.0 * I_s * H
+    w_routed = touched * 3.0 * wbytes * I * H
+    w_shared = 3.0 * wbytes * I_s * H
     act = 2.0 * T * H + 4.0 * T * E + 2.0 * T * H
     bytes_total = w_routed + w_shared + 2.0 * H + act
-    gate_up_bytes = touched * 4.0 * I * H + 4.0 * I_s * H + 2.0 * T * H
+    gate_up_bytes = touched * 2.0 * wbytes * I * H + 2.0 * wbytes * I_s * H + 2.0 * T * H
     gate_up_flops = 4.0 * H * I * T * k + 4.0 * H * I_s * T
-    down_bytes = touched * 2.0 * I * H + 2.0 * I_s * H
+    down_bytes = touched * wbytes * I * H + wbytes * I_s * H
     down_flops = 2.0 * H * I * T * k + 2.0 * H * I_s * T
     return dict(touched=touched, flops=flops, bytes=bytes_total, gate_up_bytes=gate_up_bytes,
                 gate_up_flops=gate_up_flops, down_bytes=down_bytes, down_flops=down_flops)
@@ -134,6 +136,15 @@ class ClockSampler:
                     samples=len(sm))
 
 
+# Sources of each profiled kernel: a summary's traffic counts only while
+# their hash matches the one recorded with it.
+KERNEL_SOURCES = {
+    "moe_gate_up": ("moe_gemm.cu", "gemm_common.cuh", "ptx.cuh", "moe_internal.cuh"),
+    "moe_gate_up_mxfp8": ("moe_gemm_mx.cu", "mxfp8.cuh", "gemm_common.cuh", "ptx.cuh",
+                          "moe_internal.cuh"),
+}
+
+
 def read_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
     summary was taken on the current kernel source."""
@@ -142,7 +153,7 @@ def read_traffic(kernel: str, workload: str):
     if not os.path.exists(path):
         return None
     h = hashlib.sha256()
-    for f in ("moe_gemm.cu", "ptx.cuh", "moe_internal.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "mixture_experts_ffn_03_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     vals = {}
@@ -227,6 +238,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "mxfp8"],
+                    help="expert weight format: bf16, or MXFP8 codes + scales (moe_forward_mxfp8)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -249,9 +262,16 @@ def main():
     torch.cuda.set_device(dev)
     moe.load_library()
 
-    inp = wl.make_inputs(cfg, seed=0, device=str(dev))
-    layer = moe.MoELayer(inp["w_gate_up"], inp["w_down"], inp["ws_gate_up"], inp["ws_down"],
-                         inp["w_g"], cfg.k, cfg.score_fn)
+    mx = args.weights == "mxfp8"
+    if mx:
+        inp = wl.make_inputs_mxfp8(cfg, seed=0, device=str(dev))
+        pair = lambda n: (inp[n + "_q"], inp[n + "_s"])  # noqa: E731
+        layer = moe.MoELayerMXFP8(pair("w_gate_up"), pair("w_down"), pair("ws_gate_up"),
+                                  pair("ws_down"), inp["w_g"], cfg.k, cfg.score_fn)
+    else:
+        inp = wl.make_inputs(cfg, seed=0, device=str(dev))
+        layer = moe.MoELayer(inp["w_gate_up"], inp["w_down"], inp["ws_gate_up"], inp["ws_down"],
+                             inp["w_g"], cfg.k, cfg.score_fn)
     T = cfg.T
     stream = torch.cuda.Stream(dev)
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -264,7 +284,8 @@ def main():
     st = moe.device_status(layer.workspace(T), stream)
     if st != moe.MOE_OK:
         raise RuntimeError(moe.status_string(st))
-    work = algorithmic_work(cfg, counts.cpu().tolist())
+    work = algorithmic_work(cfg, counts.cpu().tolist(), wbytes=1.0 + 1.0 / 32 if mx else 2.0)
+    gu_kernel = "moe_gate_up_mxfp8" if mx else "moe_gate_up"
 
     K = args.steps
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -397,14 +418,14 @@ def main():
         achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
         roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=achieved / peaks["hbm_gbs"],
-                    traffic=read_traffic("moe_gate_up", cfg.name),
-                    kernel="moe gate_up grouped GEMM", peak_source=peaks["source"])
+                    traffic=read_traffic(gu_kernel, cfg.name),
+                    kernel=f"{gu_kernel} grouped GEMM", peak_source=peaks["source"])
     else:
         achieved = work["gate_up_flops"] / (gu_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
-                    frac=achieved / peak, traffic=read_traffic("moe_gate_up", cfg.name),
-                    kernel="moe gate_up grouped GEMM", peak_source=peaks["source"])
+                    frac=achieved / peak, traffic=read_traffic(gu_kernel, cfg.name),
+                    kernel=f"{gu_kernel} grouped GEMM", peak_source=peaks["source"])
     t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9),
                  work["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
     layer_roof = dict(bound="hbm" if hbm_bound else "tensor", roofline_ms=t_roof * 1e3,
@@ -417,8 +438,10 @@ def main():
     line = dict(
         metric="MoE-layer tokens/s", value=value, unit="tokens/s", n_gpus=world, steps=K,
         warmup=args.warmup, ms_per_step=ms_step, higher_is_better=True, scaling="weak",
-        vs_baseline=None, dtype="bf16", data="synthetic",
-        config=dict(workload=workload_name(cfg), seed=0, parallelism="replicas" if world > 1 else "1gpu",
+        vs_baseline=None, dtype="bf16" if not mx else "bf16 (MXFP8 E4M3 weights, exact to bf16)",
+        data="synthetic",
+        config=dict(workload=workload_name(cfg), seed=0, weights=args.weights,
+                    parallelism="replicas" if world > 1 else "1gpu",
                     l2="flushed: 256 MB write between timed steps", launch="stream",
                     wall_s=round(wall, 3)),
         roofline=roof, layer_roofline=layer_roof, kernel_us=kernels,
@@ -431,6 +454,14 @@ def main():
         gpu_launches=moe.launch_count(layer.dims(T)) * K, clocks=clocks, cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
         inp_cpu = {n: t.cpu() for n, t in inp.items()}
+        if mx:
+            # the oracle's MXFP8 layer is its bf16 layer on the exactly dequantised
+            # weights: dequantise once, then time that layer
+            import oracle
+            for n in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
+                bits = oracle.mxfp8_to_bf16(oracle._np(inp_cpu.pop(n + "_q")),
+                                            oracle._np(inp_cpu.pop(n + "_s")))
+                inp_cpu[n] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
         line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu)
     print(json.dumps(line), flush=True)
     if dist is not None:

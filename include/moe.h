@@ -52,7 +52,7 @@ typedef enum {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
-    MOE_ERR_UNSUPPORTED = 2,   /* H, I or I_s not a multiple of 64 */
+    MOE_ERR_UNSUPPORTED = 2,   /* H, I or I_s not a multiple of 64 (128: MXFP8) */
     MOE_ERR_WORKSPACE = 3,     /* workspace null or smaller than moe_workspace_size() */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
     MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up waiting on an internal pipeline
@@ -103,6 +103,51 @@ moe_status moe_forward(const moe_dims* d, const void* hidden, const float* route
                        const void* ws_down, const void* w_g, void* out, int32_t* topk_ids_out,
                        float* topk_w_out, int32_t* expert_counts_out, void* workspace,
                        size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Run the layer with MXFP8 expert weights: the same computation as
+ * moe_forward, with every weight of the routed and the shared experts given
+ * in the OCP Microscaling MXFP8 format instead of bf16. The pages deploy
+ * block-FP8 expert banks ("qwen3_5_moe is TP=1-only ...", first comment)
+ * without fixing the block format; MXFP8 is the block-scaled FP8 with
+ * power-of-two scales:
+ *   a weight matrix [rows, K] is stored as
+ *     codes  [rows, K]     uint8  FP8 E4M3 (sign, 4-bit exponent with bias 7,
+ *                                 3-bit mantissa; exponent 0 = subnormal)
+ *     scales [K/32, rows]  uint8  UE8M0: scale code s stands for 2^(s - 127)
+ *   and element (r, c) is E4M3(codes[r][c]) * 2^(scales[c/32][r] - 127).
+ *   w_gate_up_q [E, 2I, H] codes, w_gate_up_s [E, H/32, 2I] scales
+ *   w_down_q    [E, H, I]  codes, w_down_s    [E, I/32, H]  scales
+ *   ws_gate_up_q [2I_s, H], ws_gate_up_s [H/32, 2I_s]   (shared expert)
+ *   ws_down_q    [H, I_s],  ws_down_s    [I_s/32, H]
+ * Each such value has at most 4 significant bits and is exactly a bf16
+ * number for scale codes 3..246, so the layer equals moe_forward run on the
+ * dequantised bf16 weights (the E4M3 NaN codes and the scale code 255 are
+ * reserved: the results are then unspecified). The activations (hidden, h),
+ * the router logits and w_g stay as in moe_forward.
+ * Sizes: H, I and I_s must be multiples of 128 (else MOE_ERR_UNSUPPORTED).
+ * The workspace is the one of moe_workspace_size(d); the h_hi / h_lo
+ * regions of moe_workspace_layout then hold h in 64-column panels (panel c:
+ * columns 64c..64c+63 of every h_hi row, then of every h_lo row) and y is
+ * always fp32. Other arguments, the returns and the error behaviour are
+ * those of moe_forward; the scale pointers must be 16-byte aligned.
+ */
+moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden, const float* router_logits,
+                             const void* w_gate_up_q, const void* w_gate_up_s,
+                             const void* w_down_q, const void* w_down_s,
+                             const void* ws_gate_up_q, const void* ws_gate_up_s,
+                             const void* ws_down_q, const void* ws_down_s, const void* w_g,
+                             void* out, int32_t* topk_ids_out, float* topk_w_out,
+                             int32_t* expert_counts_out, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream);
+
+/* bf16 values of one MXFP8 matrix (layout as in moe_forward_mxfp8): codes
+ * [rows, cols] and scales [cols/32, rows] in, out [rows, cols] bf16 written,
+ * with the conversion the MXFP8 GEMMs use (exact for scale codes 3..246).
+ * cols must be a multiple of 32 (else MOE_ERR_INVALID_ARG); codes and out
+ * 16-byte aligned. Enqueued on cuda_stream. */
+moe_status moe_mxfp8_dequant(const void* codes, const void* scales, int rows, int cols, void* out,
+                             void* cuda_stream);
 
 /* Synchronise cuda_stream, then report MOE_ERR_DEVICE_TIMEOUT if the last
  * moe_forward that used this workspace hit a pipeline timeout, MOE_ERR_CUDA

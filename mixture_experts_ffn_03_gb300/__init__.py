@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
             "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count",
-            "moe_selftest_wait_limit"]
+            "moe_selftest_wait_limit", "moe_forward_mxfp8", "moe_mxfp8_dequant"]
 NUM_STAGES = 6
 STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
 
@@ -81,6 +81,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_launch_count.restype = ctypes.c_int
     lib.moe_selftest_wait_limit.argtypes = [P, P]
     lib.moe_selftest_wait_limit.restype = ctypes.c_int
+    lib.moe_forward_mxfp8.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 15 + [P, ctypes.c_size_t, P]
+    lib.moe_forward_mxfp8.restype = ctypes.c_int
+    lib.moe_mxfp8_dequant.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
+    lib.moe_mxfp8_dequant.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -145,6 +149,33 @@ def forward_raw(dims: MoEDims, hidden, logits, w_gate_up, w_down, ws_gate_up, ws
                                _ptr(workspace),
                                ctypes.c_size_t(0 if workspace is None else workspace.numel()),
                                _stream_handle(stream)))
+
+
+def forward_mxfp8_raw(dims: MoEDims, hidden, logits, w_gate_up_q, w_gate_up_s, w_down_q, w_down_s,
+                      ws_gate_up_q, ws_gate_up_s, ws_down_q, ws_down_s, w_g, out, workspace,
+                      topk_ids_out=None, topk_w_out=None, counts_out=None, stream=None) -> int:
+    """Direct call of moe_forward_mxfp8 on tensors (or None); returns the status code."""
+    lib = load_library()
+    return int(lib.moe_forward_mxfp8(
+        ctypes.byref(dims), _ptr(hidden), _ptr(logits), _ptr(w_gate_up_q), _ptr(w_gate_up_s),
+        _ptr(w_down_q), _ptr(w_down_s), _ptr(ws_gate_up_q), _ptr(ws_gate_up_s), _ptr(ws_down_q),
+        _ptr(ws_down_s), _ptr(w_g), _ptr(out), _ptr(topk_ids_out), _ptr(topk_w_out),
+        _ptr(counts_out), _ptr(workspace),
+        ctypes.c_size_t(0 if workspace is None else workspace.numel()), _stream_handle(stream)))
+
+
+def mxfp8_dequant(codes, scales, out=None, stream=None):
+    """bf16 values of an MXFP8 matrix (moe_mxfp8_dequant): codes uint8 [rows,
+    cols], scales uint8 [cols/32, rows] on the GPU; returns out [rows, cols]."""
+    import torch
+    rows, cols = codes.shape
+    if out is None:
+        out = torch.empty(rows, cols, dtype=torch.bfloat16, device=codes.device)
+    st = load_library().moe_mxfp8_dequant(_ptr(codes), _ptr(scales), int(rows), int(cols),
+                                          _ptr(out), _stream_handle(stream))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_mxfp8_dequant")
+    return out
 
 
 def device_status(workspace, stream=None) -> int:
@@ -216,6 +247,37 @@ class MoELayer:
             self.forward(h, l, out=o, stream=s)
             out_host.copy_(o, non_blocking=True)
         return out_host
+
+
+class MoELayerMXFP8(MoELayer):
+    """MoELayer with MXFP8 expert weights (moe_forward_mxfp8): each of
+    w_gate_up, w_down, ws_gate_up, ws_down is a pair (codes uint8 [..., rows,
+    K], scales uint8 [..., K/32, rows]); w_g stays bf16."""
+
+    def __init__(self, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int, score_fn: int):
+        import torch
+        self.w_gate_up, self.w_down = w_gate_up, w_down
+        self.ws_gate_up, self.ws_down, self.w_g = ws_gate_up, ws_down, w_g
+        self.E, two_i, self.H = w_gate_up[0].shape
+        self.I = two_i // 2
+        self.I_s = ws_gate_up[0].shape[0] // 2
+        self.k, self.score_fn = int(k), int(score_fn)
+        self.device = w_gate_up[0].device
+        self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    def forward(self, hidden, logits, out=None, topk_ids=None, topk_w=None, counts=None,
+                stream=None):
+        import torch
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        ws = self.workspace(T)
+        st = forward_mxfp8_raw(self.dims(T), hidden, logits, *self.w_gate_up, *self.w_down,
+                               *self.ws_gate_up, *self.ws_down, self.w_g, out, ws, topk_ids,
+                               topk_w, counts, stream)
+        if st != MOE_OK:
+            raise MoEError(st, "moe_forward_mxfp8")
+        return out
 
 
 class HostPipeline:

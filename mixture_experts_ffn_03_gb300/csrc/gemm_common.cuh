@@ -1,0 +1,315 @@
+// Pipeline machinery shared by the grouped expert GEMMs (moe_gemm.cu, bf16
+// weights; moe_gemm_mx.cu, MXFP8 weights): tile descriptors and their
+// dynamic schedule, the shared-memory control block, bounded mbarrier waits,
+// TMEM set-up and the down GEMM's epilogue role.
+#pragma once
+
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448;
+
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kTileQ = 8;                          // tile descriptors in flight between roles
+constexpr int kMaxAStages = 4;                     // TMEM weight stages (MXFP8 GEMMs)
+constexpr int kStgBytes = kEpiRows * kEpiCols * 4;  // one staging buffer (2 KB)
+
+struct Tile {
+    int shared;  // 1: shared-expert tile
+    int e;       // routed expert
+    int m0;      // first row inside the group
+    int n_rows;  // valid token rows in this tile (1..BN)
+    int p0;      // first row in the sorted slot order (routed) or token index (shared)
+    int f;       // 128-row block of output features
+};
+
+struct Ctl {
+    uint64_t full_a[kMaxStages];  // TMA bytes landed
+    uint64_t full_b[kMaxStages];  // gathered rows landed (gate_up)
+    uint64_t empty[kMaxStages];   // MMAs reading the stage completed
+    uint64_t tfull[2];            // accumulator ready for the epilogue
+    uint64_t tempty[2];           // accumulator drained
+    uint64_t drain;               // MMA completion on the abort path
+    uint64_t a_full[kMaxAStages]; // converted weight stage written to TMEM (MXFP8 GEMMs)
+    uint64_t a_empty[kMaxAStages];// MMAs reading the TMEM weight stage completed
+    uint64_t tq_full[kTileQ];     // tile descriptor published
+    uint64_t tq_empty[kTileQ];    // tile descriptor read by every consumer role
+    Tile tq[kTileQ];              // tile descriptors, in processing order
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Ctl) <= 1024, "control block fits its shared-memory slot");
+
+// Tile order: the shared expert's tiles first (they carry the most tokens
+// per tile), then the routed row tiles, the feature blocks of a row tile
+// consecutive. A tile index past the end gives the sentinel (n_rows < 0).
+__device__ __forceinline__ int4 load_rowtile(int tile, int num_tiles, int shared_tiles, int F,
+                                             const GemmArgs& a) {
+    if (tile < shared_tiles || tile >= num_tiles) return make_int4(0, 0, 0, 0);
+    return a.rowtiles[(tile - shared_tiles) / F];
+}
+
+template <int BN>
+__device__ __forceinline__ Tile make_tile(int tile, int4 r, int num_tiles, int shared_tiles,
+                                          int F, int F_s, const GemmArgs& a) {
+    Tile ti;
+    if (tile >= num_tiles) {
+        ti.shared = 0;
+        ti.e = 0;
+        ti.m0 = 0;
+        ti.n_rows = -1;
+        ti.p0 = 0;
+        ti.f = 0;
+    } else if (tile < shared_tiles) {
+        const int rt = tile / F_s;
+        ti.f = tile - rt * F_s;
+        ti.shared = 1;
+        ti.e = 0;
+        ti.m0 = rt * BN;
+        ti.n_rows = min(BN, a.T - ti.m0);
+        ti.p0 = ti.m0;
+    } else {
+        const int t2 = tile - shared_tiles;
+        const int rt = t2 / F;
+        ti.f = t2 - rt * F;
+        ti.shared = 0;
+        ti.e = r.x;
+        ti.m0 = r.y;
+        ti.n_rows = r.z;
+        ti.p0 = r.w;
+    }
+    return ti;
+}
+
+// Dynamic tile scheduling, run by the TMA producer thread: a CTA's first tile
+// is blockIdx.x, every further tile is claimed from a global counter. The
+// claim and the row-tile load for the next tile are issued one tile ahead, so
+// their latency hides behind the current tile's loads.
+template <int BN>
+struct TileSched {
+    int nxt;    // tile after the current one
+    int after;  // claim for the tile after nxt (read one tile later)
+    int4 raw;   // row-tile entry of nxt
+    int num_tiles, shared_tiles, F, F_s;
+
+    __device__ __forceinline__ Tile start(int n_tiles, int s_tiles, int f, int f_s,
+                                          const GemmArgs& a) {
+        num_tiles = n_tiles;
+        shared_tiles = s_tiles;
+        F = f;
+        F_s = f_s;
+        const int first = blockIdx.x;
+        nxt = first < num_tiles ? static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1) : num_tiles;
+        return make_tile<BN>(first, load_rowtile(first, num_tiles, shared_tiles, F, a), num_tiles,
+                             shared_tiles, F, F_s, a);
+    }
+    // At the start of a tile: claim the tile after next and load next's row tile.
+    __device__ __forceinline__ void prefetch(const GemmArgs& a) {
+        raw = load_rowtile(nxt, num_tiles, shared_tiles, F, a);
+        after = nxt < num_tiles ? static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1) : num_tiles;
+    }
+    // At the end of a tile: the next tile's descriptor.
+    __device__ __forceinline__ bool next(Tile& ti, const GemmArgs& a) {
+        ti = make_tile<BN>(nxt, raw, num_tiles, shared_tiles, F, F_s, a);
+        nxt = after;
+        return true;
+    }
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned* err, unsigned code) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for phase `parity` of `bar`; false if the CTA is aborting or the wait
+// timed out (which starts the abort).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* err, unsigned code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, err, code);
+}
+
+// Abort-path wait that ignores the abort flag, bounded by the time limit.
+__device__ __noinline__ void wait_bounded(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t* b) { return ptx::smem_u32(b); }
+
+// Publish the next tile descriptor (the producer); false on abort or timeout.
+__device__ __forceinline__ bool tq_publish(Ctl* ctl, int& s, uint32_t& ph, const Tile& ti,
+                                           volatile int* abort_flag, unsigned* err, unsigned code) {
+    if (!wait_bar(bar_addr(&ctl->tq_empty[s]), ph ^ 1u, abort_flag, err, code)) return false;
+    ctl->tq[s] = ti;
+    ptx::mbar_arrive(bar_addr(&ctl->tq_full[s]));  // release: the descriptor is visible
+    if (++s == kTileQ) {
+        s = 0;
+        ph ^= 1u;
+    }
+    return true;
+}
+
+// Read the next tile descriptor (a consumer role; `single` when the role is
+// one thread, else the whole warp calls it and lane 0 releases the slot).
+// False at the end of the sequence, on abort or on timeout.
+__device__ __forceinline__ bool tq_read(Ctl* ctl, int& s, uint32_t& ph, Tile& ti, bool single,
+                                        volatile int* abort_flag, unsigned* err, unsigned code) {
+    if (!wait_bar(bar_addr(&ctl->tq_full[s]), ph, abort_flag, err, code)) return false;
+    ti = ctl->tq[s];
+    if (!single) __syncwarp();
+    if (single || (threadIdx.x & 31) == 0) ptx::mbar_arrive(bar_addr(&ctl->tq_empty[s]));
+    if (++s == kTileQ) {
+        s = 0;
+        ph ^= 1u;
+    }
+    return ti.n_rows >= 0;
+}
+
+// Common set-up: barriers, TMEM allocation. Returns the TMEM base address.
+// C is the kernel's shared-memory / TMEM configuration.
+// tq_consumers: warps (or single threads) that read each tile descriptor.
+template <class C>
+__device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp, int tq_consumers) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(bar_addr(&ctl->full_a[s]), 1);
+            ptx::mbar_init(bar_addr(&ctl->full_b[s]), 64);
+            ptx::mbar_init(bar_addr(&ctl->empty[s]), 1);
+        }
+        for (int s = 0; s < C::ACC_STAGES; ++s) {
+            ptx::mbar_init(bar_addr(&ctl->tfull[s]), 1);
+            ptx::mbar_init(bar_addr(&ctl->tempty[s]), kEpiWarps);
+        }
+        for (int s = 0; s < C::A_STAGES; ++s) {
+            ptx::mbar_init(bar_addr(&ctl->a_full[s]), C::CONVERTER_WARPS);
+            ptx::mbar_init(bar_addr(&ctl->a_empty[s]), 1);
+        }
+        ptx::mbar_init(bar_addr(&ctl->drain), 1);
+        for (int q = 0; q < kTileQ; ++q) {
+            ptx::mbar_init(bar_addr(&ctl->tq_full[q]), 1);
+            ptx::mbar_init(bar_addr(&ctl->tq_empty[q]), tq_consumers);
+        }
+        ctl->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    return ctl->tmem_base;
+}
+
+template <class C>
+__device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, int warp) {
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Abort path of the TMA producer: wait (bounded) until the last load armed on
+// every stage has landed, so no copy is in flight when the CTA exits.
+template <int STAGES>
+__device__ __forceinline__ void drain_tma(Ctl* ctl, uint32_t armed, uint32_t parity_bits) {
+    for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) wait_bounded(bar_addr(&ctl->full_a[s]), (parity_bits >> s) & 1u);
+}
+
+// Epilogue role of the down GEMMs with the weights on M (warps 4-11), with
+// the same chunking as the gate_up epilogue: warp we owns 32 output features
+// (TMEM lanes 32*(warp % 4)..) and every other 16-column chunk; full chunks
+// go out as fp32 TMA box stores of y through st_y, ragged tails as plain
+// stores. Shared
+// expert rows are scaled by their token's gate sigmoid(x . w_g).
+template <class C, int BN>
+__device__ __forceinline__ void down_epilogue(uint8_t* smem, Ctl* ctl, uint32_t tmem_base, int warp,
+                                              int lane, const CUtensorMap* st_y,
+                                              const GemmArgs& a, volatile int* abort_flag,
+                                              unsigned* err, unsigned code) {
+    const int we = warp - 4, q = warp & 3, half = we >> 2;
+    uint8_t* stg = smem + C::EPI_OFF + we * C::EPI_BUFS * kStgBytes;
+    uint32_t nbuf = 0;
+    int as = 0;
+    uint32_t aph = 0;
+    const int shared_row0 = a.T * a.k;
+    int qs = 0;
+    uint32_t qph = 0;
+    Tile ti;
+    while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
+        if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
+        ptx::tc_fence_after();
+        const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
+        const bool warp_valid = h0 < a.H;               // H is a multiple of 64
+        const int row0 = ti.shared ? shared_row0 + ti.m0 : ti.p0;
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
+        for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
+            uint32_t v[kEpiRows], vl[kEpiRows];
+            ptx::tmem_ld_32x32b_x16(tb + c0, v);        // W h_hi
+            ptx::tmem_ld_32x32b_x16(tb + BN + c0, vl);  // W h_lo
+            ptx::tmem_ld_wait();
+            if (!warp_valid) continue;
+            const int rows = min(kEpiRows, ti.n_rows - c0);
+            float val[kEpiRows];
+#pragma unroll
+            for (int n = 0; n < kEpiRows; ++n) {
+                val[n] = __uint_as_float(v[n]) + __uint_as_float(vl[n]);
+                if (ti.shared && n < rows)
+                    val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
+            }
+            if (rows == kEpiRows) {
+                const uint32_t b = nbuf++ % C::EPI_BUFS;
+                float* sy = reinterpret_cast<float*>(stg + b * kStgBytes);
+                if (lane == 0) ptx::bulk_wait_read<C::EPI_BUFS - 1>();  // buffer b is free
+                __syncwarp();
+#pragma unroll
+                for (int n = 0; n < kEpiRows; ++n) sy[n * kEpiCols + lane] = val[n];
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(st_y, ptx::smem_u32(sy), h0, row0 + c0);
+                    ptx::bulk_commit();
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < kEpiRows; ++n)
+                    if (n < rows)
+                        a.y[static_cast<size_t>(row0 + c0 + n) * a.H + h0 + lane] = val[n];
+            }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
+        if (++as == C::ACC_STAGES) {
+            as = 0;
+            aph ^= 1u;
+        }
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+}
+
+}  // namespace
+}  // namespace moe

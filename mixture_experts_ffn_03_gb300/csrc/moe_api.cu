@@ -116,6 +116,27 @@ bool make_pair_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tiled map of `rank` dimensions over bytes (dt UINT8) or bf16; dims and box
+// innermost first, strides[i] = byte stride of dimension i + 1.
+bool make_map_nd(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
+                 const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                 CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return fn(m, dt, rank, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swz, swz == CU_TENSOR_MAP_SWIZZLE_NONE ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                                                     : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major matrix [outer, inner] of `elem` bytes per element, written by the
 // GEMM epilogues in boxes of kEpiCols x kEpiRows (no swizzle).
 bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t elem,
@@ -216,7 +237,8 @@ MOE_API const char* moe_status_string(moe_status s) {
     switch (s) {
         case MOE_OK: return "ok";
         case MOE_ERR_INVALID_ARG: return "invalid argument";
-        case MOE_ERR_UNSUPPORTED: return "unsupported size (H, I and I_s must be multiples of 64)";
+        case MOE_ERR_UNSUPPORTED:
+            return "unsupported size (H, I and I_s must be multiples of 64; of 128 for MXFP8 weights)";
         case MOE_ERR_WORKSPACE: return "workspace missing or too small";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
@@ -225,19 +247,98 @@ MOE_API const char* moe_status_string(moe_status s) {
     }
 }
 
-MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const float* router_logits,
-                               const void* w_gate_up, const void* w_down, const void* ws_gate_up,
-                               const void* ws_down, const void* w_g, void* out,
-                               int32_t* topk_ids_out, float* topk_w_out,
-                               int32_t* expert_counts_out, void* workspace,
-                               size_t workspace_bytes, void* cuda_stream) {
+namespace moe {
+namespace {
+
+// The experts' weights: bf16 matrices, or MXFP8 codes with their scales.
+struct ExpertWeights {
+    bool mx;
+    const void* gate_up;      // [E, 2I, H] bf16 or E4M3 codes
+    const void* down;         // [E, H, I]
+    const void* s_gate_up;    // shared expert [2I_s, H]
+    const void* s_down;       // shared expert [H, I_s]
+    const uint8_t* gate_up_sc;    // MXFP8 scales [E, H/32, 2I]
+    const uint8_t* down_sc;       // [E, I/32, H]
+    const uint8_t* s_gate_up_sc;  // [H/32, 2I_s]
+    const uint8_t* s_down_sc;     // [I_s/32, H]
+};
+
+bool dims_supported_mx(const moe_dims* d) {
+    return d->H % 128 == 0 && d->I % 128 == 0 && d->I_s % 128 == 0;
+}
+
+// TMA maps of the MXFP8 GEMMs (layouts in moe_internal.cuh, MxMaps).
+bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, char* ws, int bn_dn,
+                  MxMaps* gu, MxMaps* dn) {
+    const uint64_t T = d.T, H = d.H, E = d.E, I = d.I, Is = d.I_s, tk = T * d.k;
+    const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B, NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
+    bool ok = true;
+    {   // gate_up codes: {H, rows, 2 (gate, up)}, boxes 128 x 128 x 2
+        const uint32_t box[3] = {128, 128, 2};
+        const uint64_t dw[3] = {H, E * 2 * I - I, 2}, sw[2] = {H, I * H};
+        const uint64_t ds[3] = {H, Is, 2}, ss[2] = {H, Is * H};
+        ok = ok && make_map_nd(&gu->w, U8, W.gate_up, 3, dw, sw, box, SW) &&
+             make_map_nd(&gu->ws, U8, W.s_gate_up, 3, ds, ss, box, SW);
+    }
+    {   // gate_up scales: {rows of a plane, 2 planes, K blocks}, boxes 128 x 2 x 4
+        const uint32_t box[3] = {128, 2, 4};
+        const uint64_t dw[3] = {I, 2, E * (H / 32)}, sw[2] = {I, 2 * I};
+        const uint64_t ds[3] = {Is, 2, H / 32}, ss[2] = {Is, 2 * Is};
+        ok = ok && make_map_nd(&gu->sc, U8, W.gate_up_sc, 3, dw, sw, box, NOSW) &&
+             make_map_nd(&gu->scs, U8, W.s_gate_up_sc, 3, ds, ss, box, NOSW);
+    }
+    {   // down codes: {128, K / 128, rows}, boxes 128 x 2 x 128
+        const uint32_t box[3] = {128, 2, 128};
+        const uint64_t dw[3] = {128, I / 128, E * H}, sw[2] = {128, I};
+        const uint64_t ds[3] = {128, Is / 128, H}, ss[2] = {128, Is};
+        ok = ok && make_map_nd(&dn->w, U8, W.down, 3, dw, sw, box, SW) &&
+             make_map_nd(&dn->ws, U8, W.s_down, 3, ds, ss, box, SW);
+    }
+    {   // down scales: {H, K blocks}, boxes 128 x 8
+        const uint32_t box[2] = {128, 8};
+        const uint64_t dw[2] = {H, E * (I / 32)}, sw[1] = {H};
+        const uint64_t ds[2] = {H, Is / 32}, ss[1] = {H};
+        ok = ok && make_map_nd(&dn->sc, U8, W.down_sc, 2, dw, sw, box, NOSW) &&
+             make_map_nd(&dn->scs, U8, W.s_down_sc, 2, ds, ss, box, NOSW);
+    }
+    {   // h panels: {64, P, 2 (hi, lo), K / 64}, boxes 64 x BN x 2 x 4
+        const uint32_t box[4] = {64, static_cast<uint32_t>(bn_dn), 2, 4};
+        const uint64_t dr[4] = {64, tk, 2, I / 64}, sr[3] = {128, tk * 128, 2 * tk * 128};
+        const uint64_t dsh[4] = {64, T, 2, Is / 64}, ssh[3] = {128, T * 128, 2 * T * 128};
+        ok = ok && make_map_nd(&dn->h, BF16, ws + L.h_hi, 4, dr, sr, box, SW) &&
+             make_map_nd(&dn->hs, BF16, ws + L.hs_hi, 4, dsh, ssh, box, SW);
+    }
+    {   // gate_up stores into the panels: {64, P, K / 64}, boxes 32 x kEpiRows x 1
+        const uint32_t box[3] = {static_cast<uint32_t>(kEpiCols), static_cast<uint32_t>(kEpiRows), 1};
+        const uint64_t dr[3] = {64, tk, I / 64}, sr[2] = {128, 2 * tk * 128};
+        const uint64_t dsh[3] = {64, T, Is / 64}, ssh[2] = {128, 2 * T * 128};
+        ok = ok && make_map_nd(&gu->st[0], BF16, ws + L.h_hi, 3, dr, sr, box, NOSW) &&
+             make_map_nd(&gu->st[1], BF16, ws + L.h_hi + tk * 128, 3, dr, sr, box, NOSW) &&
+             make_map_nd(&gu->st[2], BF16, ws + L.hs_hi, 3, dsh, ssh, box, NOSW) &&
+             make_map_nd(&gu->st[3], BF16, ws + L.hs_hi + T * 128, 3, dsh, ssh, box, NOSW);
+    }
+    ok = ok && make_store_map(&dn->st[0], ws + L.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T);
+    return ok;
+}
+
+moe_status forward_impl(const moe_dims* d, const void* hidden, const float* router_logits,
+                        const ExpertWeights& W, const void* w_g, void* out,
+                        int32_t* topk_ids_out, float* topk_w_out, int32_t* expert_counts_out,
+                        void* workspace, size_t workspace_bytes, void* cuda_stream) {
     if (!dims_valid(d)) return MOE_ERR_INVALID_ARG;
-    if (!dims_supported(d)) return MOE_ERR_UNSUPPORTED;
+    if (!dims_supported(d) || (W.mx && !dims_supported_mx(d))) return MOE_ERR_UNSUPPORTED;
     if (d->T == 0) return MOE_OK;
-    const void* required[] = {hidden, router_logits, w_gate_up, w_down, ws_gate_up,
-                              ws_down, w_g, out};
+    const void* required[] = {hidden, router_logits, W.gate_up, W.down, W.s_gate_up,
+                              W.s_down, w_g, out};
     for (const void* p : required)
         if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (W.mx) {
+        const void* scales[] = {W.gate_up_sc, W.down_sc, W.s_gate_up_sc, W.s_down_sc};
+        for (const void* p : scales)
+            if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    }
     const void* optional[] = {topk_ids_out, topk_w_out, expert_counts_out};
     for (const void* p : optional)
         if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
@@ -267,32 +368,40 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     auto* hs_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_lo);
     float* y = reinterpret_cast<float*>(ws + L.y);
 
-    const int bn_gu = pick_bn(tk, E, 256, true);
-    const int bn_dn = pick_bn(tk, E, 128, false);
+    // The MXFP8 GEMMs keep the weights on the MMA's M side at every size and
+    // take tiles of at most 64 tokens.
+    const int bn_gu = pick_bn(tk, E, W.mx ? 64 : 256, true);
+    const int bn_dn = pick_bn(tk, E, W.mx ? 64 : 128, false);
     const int num_sms = sm_count();
     if (num_sms <= 0) return MOE_ERR_CUDA;
 
     GemmMaps gu{}, dn{};
-    // gate_up: the gate rows of expert e are rows e*2I + [0, I) of W_gate_up and its up
-    // rows follow I rows later, so a map over the first E*2I - I rows with a plane stride
-    // of I rows reaches both (and no address past the tensor); likewise I_s for the
-    // shared expert. down: 128-token tiles read 256 weight rows per request.
-    const uint32_t dn_w_rows = bn_dn == 128 ? 256u : static_cast<uint32_t>(kGemmBM);
-    bool ok = make_pair_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E) * 2 * I - I,
-                            static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
-              make_pair_map(&gu.ws, ws_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2,
-                            kGemmBM) &&
-              make_map(&dn.w, w_down, I, static_cast<uint64_t>(E) * H, dn_w_rows) &&
-              make_map(&dn.ws, ws_down, Is, H, dn_w_rows) &&
-              make_pair_map(&dn.h, h_hi, I, tk, L.h_lo - L.h_hi, bn_dn) &&
-              make_pair_map(&dn.hs, hs_hi, Is, T, L.hs_lo - L.hs_hi, bn_dn);
-    const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    ok = ok && make_store_map(&gu.st[0], h_hi, BF16, 2, I, tk) &&
-         make_store_map(&gu.st[1], h_lo, BF16, 2, I, tk) &&
-         make_store_map(&gu.st[2], hs_hi, BF16, 2, Is, T) &&
-         make_store_map(&gu.st[3], hs_lo, BF16, 2, Is, T) &&
-         make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
-         make_y24_store_map(&dn.st[1], y, H, tk + T);
+    MxMaps mgu{}, mdn{};
+    bool ok;
+    if (W.mx) {
+        ok = make_mx_maps(*d, W, L, ws, bn_dn, &mgu, &mdn);
+    } else {
+        // gate_up: the gate rows of expert e are rows e*2I + [0, I) of W_gate_up and its up
+        // rows follow I rows later, so a map over the first E*2I - I rows with a plane stride
+        // of I rows reaches both (and no address past the tensor); likewise I_s for the
+        // shared expert. down: 128-token tiles read 256 weight rows per request.
+        const uint32_t dn_w_rows = bn_dn == 128 ? 256u : static_cast<uint32_t>(kGemmBM);
+        ok = make_pair_map(&gu.w, W.gate_up, H, static_cast<uint64_t>(E) * 2 * I - I,
+                           static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
+             make_pair_map(&gu.ws, W.s_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2,
+                           kGemmBM) &&
+             make_map(&dn.w, W.down, I, static_cast<uint64_t>(E) * H, dn_w_rows) &&
+             make_map(&dn.ws, W.s_down, Is, H, dn_w_rows) &&
+             make_pair_map(&dn.h, h_hi, I, tk, L.h_lo - L.h_hi, bn_dn) &&
+             make_pair_map(&dn.hs, hs_hi, Is, T, L.hs_lo - L.hs_hi, bn_dn);
+        const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        ok = ok && make_store_map(&gu.st[0], h_hi, BF16, 2, I, tk) &&
+             make_store_map(&gu.st[1], h_lo, BF16, 2, I, tk) &&
+             make_store_map(&gu.st[2], hs_hi, BF16, 2, Is, T) &&
+             make_store_map(&gu.st[3], hs_lo, BF16, 2, Is, T) &&
+             make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
+             make_y24_store_map(&dn.st[1], y, H, tk + T);
+    }
     if (!ok) return MOE_ERR_CUDA;
 
     GemmArgs ga{};
@@ -327,6 +436,8 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     const size_t max_gu = (tk / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
     const size_t max_dn = (tk / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
     const int cap = 1 << 30;
+    const int tiles_gu = static_cast<int>(max_gu < cap ? max_gu : cap);
+    const int tiles_dn = static_cast<int>(max_dn < cap ? max_dn : cap);
 
     // Status words (error flags, tile counts, completion ticket) start at zero.
     if (cudaMemsetAsync(meta, 0, META_WORDS * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -357,20 +468,75 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
             return MOE_ERR_CUDA;
     }
     mark_stage(3, st);
-    if ((launch_gate_up(bn_gu, gu, ga, static_cast<int>(max_gu < cap ? max_gu : cap), num_sms,
-                            st)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    const cudaError_t e_gu = W.mx ? launch_gate_up_mx(bn_gu, mgu, ga, tiles_gu, num_sms, st)
+                                  : launch_gate_up(bn_gu, gu, ga, tiles_gu, num_sms, st);
+    if (e_gu != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(4, st);
-    if ((launch_down(bn_dn, dn, gd, static_cast<int>(max_dn < cap ? max_dn : cap), num_sms,
-                         st)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    const cudaError_t e_dn = W.mx ? launch_down_mx(bn_dn, mdn, gd, tiles_dn, num_sms, st)
+                                  : launch_down(bn_dn, dn, gd, tiles_dn, num_sms, st);
+    if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(5, st);
     // 128-token down tiles leave y as 24-bit floats, the other widths as fp32.
-    if ((launch_combine(T, H, k, y, bn_dn == 128, topk_w, inv, static_cast<__nv_bfloat16*>(out),
-                        st)) !=
-        cudaSuccess)
+    if ((launch_combine(T, H, k, y, !W.mx && bn_dn == 128, topk_w, inv,
+                        static_cast<__nv_bfloat16*>(out), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
     mark_stage(6, st);
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const float* router_logits,
+                               const void* w_gate_up, const void* w_down, const void* ws_gate_up,
+                               const void* ws_down, const void* w_g, void* out,
+                               int32_t* topk_ids_out, float* topk_w_out,
+                               int32_t* expert_counts_out, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream) {
+    ExpertWeights W{};
+    W.mx = false;
+    W.gate_up = w_gate_up;
+    W.down = w_down;
+    W.s_gate_up = ws_gate_up;
+    W.s_down = ws_down;
+    return forward_impl(d, hidden, router_logits, W, w_g, out, topk_ids_out, topk_w_out,
+                        expert_counts_out, workspace, workspace_bytes, cuda_stream);
+}
+
+MOE_API moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden,
+                                     const float* router_logits, const void* w_gate_up_q,
+                                     const void* w_gate_up_s, const void* w_down_q,
+                                     const void* w_down_s, const void* ws_gate_up_q,
+                                     const void* ws_gate_up_s, const void* ws_down_q,
+                                     const void* ws_down_s, const void* w_g, void* out,
+                                     int32_t* topk_ids_out, float* topk_w_out,
+                                     int32_t* expert_counts_out, void* workspace,
+                                     size_t workspace_bytes, void* cuda_stream) {
+    ExpertWeights W{};
+    W.mx = true;
+    W.gate_up = w_gate_up_q;
+    W.down = w_down_q;
+    W.s_gate_up = ws_gate_up_q;
+    W.s_down = ws_down_q;
+    W.gate_up_sc = static_cast<const uint8_t*>(w_gate_up_s);
+    W.down_sc = static_cast<const uint8_t*>(w_down_s);
+    W.s_gate_up_sc = static_cast<const uint8_t*>(ws_gate_up_s);
+    W.s_down_sc = static_cast<const uint8_t*>(ws_down_s);
+    return forward_impl(d, hidden, router_logits, W, w_g, out, topk_ids_out, topk_w_out,
+                        expert_counts_out, workspace, workspace_bytes, cuda_stream);
+}
+
+MOE_API moe_status moe_mxfp8_dequant(const void* codes, const void* scales, int rows, int cols,
+                                     void* out, void* cuda_stream) {
+    if (rows < 0 || cols < 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    if (!codes || !scales || !out || !aligned16(codes) || !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    if (launch_mxfp8_dequant(static_cast<const uint8_t*>(codes),
+                             static_cast<const uint8_t*>(scales), rows, cols,
+                             static_cast<__nv_bfloat16*>(out),
+                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

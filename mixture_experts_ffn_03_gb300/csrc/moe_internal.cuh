@@ -113,6 +113,33 @@ struct GemmMaps {
     CUtensorMap st[4];
 };
 
+// TMA maps of the GEMMs with MXFP8 expert weights (moe_gemm_mx.cu). Codes
+// are bytes read with the 128-byte swizzle, scales bytes without swizzle.
+// gate_up: w / ws = codes of W_gate_up as {H, E*2I - I rows, 2} (plane
+//   stride I rows: gate, up) and of Ws_gate_up as {H, I_s, 2}, boxes
+//   128 x 128 x 2; sc / scs = their scales [E, H/32, 2I] as {I, 2, E*H/32}
+//   and [H/32, 2I_s] as {I_s, 2, H/32}, boxes 128 x 2 x 4.
+// down: w / ws = codes of W_down as {128, I/128, E*H rows} and of Ws_down as
+//   {128, I_s/128, H}, boxes 128 x 2 x 128 (256 K values of 128 rows, each
+//   row's two 128-byte halves adjacent); sc / scs = scales [E, I/32, H] as
+//   {H, E*I/32} and [I_s/32, H] as {H, I_s/32}, boxes 128 x 8; h / hs = h in
+//   64-column panels (below) as {64, P rows, 2 (hi, lo), I/64 panels}, boxes
+//   64 x BN x 2 x 4.
+// h of the MXFP8 path is stored in 64-column panels: panel c holds columns
+//   64c..64c+63 of the P rows of h_hi, then of h_lo (P = T*k routed, T
+//   shared), so one box brings the hi and lo rows of four 64-column K
+//   slices. st[0..3] (gate_up) = the hi and lo planes of the routed and the
+//   shared panels as {64, P, I/64}, boxes 32 x kEpiRows x 1; st[0] (down) = y.
+struct MxMaps {
+    CUtensorMap w;
+    CUtensorMap ws;
+    CUtensorMap sc;
+    CUtensorMap scs;
+    CUtensorMap h;
+    CUtensorMap hs;
+    CUtensorMap st[4];
+};
+
 // Supported tile widths (tokens per tile) of both GEMMs.
 bool gemm_bn_supported(int bn);
 cudaError_t launch_gate_up(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
@@ -121,5 +148,16 @@ cudaError_t launch_gate_up(int bn, const GemmMaps& maps, const GemmArgs& a, int 
 cudaError_t launch_wait_limit_selftest(unsigned* err, cudaStream_t st);
 cudaError_t launch_down(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
                         int num_sms, cudaStream_t st);
+
+// MXFP8 GEMMs (moe_gemm_mx.cu): tile widths 16, 32 and 64; H, I and I_s
+// multiples of 128.
+bool gemm_mx_bn_supported(int bn);
+cudaError_t launch_gate_up_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
+                              int num_sms, cudaStream_t st);
+cudaError_t launch_down_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
+                           int num_sms, cudaStream_t st);
+// bf16 values of an MXFP8 matrix [rows, cols] (scales [cols/32, rows]).
+cudaError_t launch_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int rows, int cols,
+                                 __nv_bfloat16* out, cudaStream_t st);
 
 }  // namespace moe

@@ -123,14 +123,16 @@ def quantize_mxfp8(w: torch.Tensor):
     X = floor(log2(max |w|)) - 8 (8 = the largest E4M3 exponent), clamped to
     [-127, 127]; the elements are w / 2^X saturated to +-448 and rounded to
     the nearest E4M3 value (ties to even). Returns (codes uint8 [..., rows, K],
-    scales uint8 [..., K / 32, rows] holding X + 127). Input preparation only:
-    the layer consumes the codes and scales as given."""
+    scales uint8 [..., K / 32, rows] holding X + 127). Every step is exact
+    (frexp, division by a power of two) up to the final rounding, so the codes
+    are the same on every device. Input preparation only: the layer consumes
+    the codes and scales as given."""
     *lead, rows, K = w.shape
     assert K % 32 == 0
     f = w.float().reshape(*lead, rows, K // 32, 32)
     amax = f.abs().amax(dim=-1)
-    X = torch.where(amax > 0, torch.floor(torch.log2(amax.clamp_min(2.0 ** -149))) - 8,
-                    torch.full_like(amax, -127.0)).clamp(-127, 127)
+    _, e = torch.frexp(amax)                      # amax = m 2^e, m in [0.5, 1)
+    X = torch.where(amax > 0, e.float() - 1 - 8, torch.full_like(amax, -127.0)).clamp(-127, 127)
     q = (f / torch.exp2(X).unsqueeze(-1)).clamp(-448.0, 448.0)
     codes = q.to(torch.float8_e4m3fn).view(torch.uint8).reshape(*lead, rows, K)
     scales = (X + 127).to(torch.uint8).transpose(-1, -2).contiguous()  # [..., K/32, rows]
@@ -138,11 +140,17 @@ def quantize_mxfp8(w: torch.Tensor):
 
 
 def make_inputs_mxfp8(cfg: MoEConfig, seed: int = 0, device: str = "cpu") -> dict:
-    """The bf16 inputs of make_inputs with the routed experts' weights replaced
-    by their MXFP8 encoding (w_gate_up_q/_s, w_down_q/_s); shared expert, w_g,
-    hidden and logits unchanged."""
-    inp = make_inputs(cfg, seed=seed, device="cpu")
-    gq, gs = quantize_mxfp8(inp.pop("w_gate_up"))
-    dq, ds = quantize_mxfp8(inp.pop("w_down"))
-    inp.update(w_gate_up_q=gq, w_gate_up_s=gs, w_down_q=dq, w_down_s=ds)
-    return {n: t.to(device) for n, t in inp.items()}
+    """The bf16 inputs of make_inputs (drawn on ``device``) with every expert
+    weight matrix (routed and shared) replaced by its MXFP8 encoding: <name>_q
+    codes and <name>_s scales for w_gate_up, w_down, ws_gate_up and ws_down;
+    hidden, logits and w_g unchanged."""
+    inp = make_inputs(cfg, seed=seed, device=device)
+    for name in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
+        w = inp.pop(name)
+        if w.dim() == 3:   # expert by expert: bounded temporary memory
+            pairs = [quantize_mxfp8(w[e]) for e in range(w.shape[0])]
+            q, s = torch.stack([p[0] for p in pairs]), torch.stack([p[1] for p in pairs])
+        else:
+            q, s = quantize_mxfp8(w)
+        inp[name + "_q"], inp[name + "_s"] = q, s
+    return inp

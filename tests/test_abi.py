@@ -91,3 +91,33 @@ def test_host_validation(lib):
     assert moe.launch_count(moe.make_dims(64, 2048, 256, 8, 512, 512, 1)) == 4   # T*k <= 2048
     assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 6
     assert moe.launch_count(moe.make_dims(0, 2048, 256, 8, 512, 512, 0)) == 0
+
+
+def _call_mx(lib, dims, **kw):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: the checks below fail first
+    names = ["hidden", "logits", "gu_q", "gu_s", "d_q", "d_s", "sgu_q", "sgu_s", "sd_q", "sd_s",
+             "wg", "out"]
+    args = {n: fake for n in names}
+    args.update(ids=None, w=None, counts=None, ws=fake, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return lib.moe_forward_mxfp8(ctypes.byref(dims), *[args[n] for n in names], args["ids"],
+                                 args["w"], args["counts"], args["ws"],
+                                 ctypes.c_size_t(args["ws_bytes"]), args["stream"])
+
+
+def test_host_validation_mxfp8(lib):
+    import mixture_experts_ffn_03_gb300 as moe
+    ok = moe.make_dims(16, 128, 16, 4, 128, 128, 0)
+    assert _call_mx(lib, moe.make_dims(16, 128, 16, 0, 128, 128, 0)) == 1    # k < 1
+    assert _call_mx(lib, moe.make_dims(16, 64, 16, 4, 128, 128, 0)) == 2     # H % 128
+    assert _call_mx(lib, moe.make_dims(16, 128, 16, 4, 192, 128, 0)) == 2    # I % 128
+    assert _call_mx(lib, moe.make_dims(16, 128, 16, 4, 128, 64, 0)) == 2     # I_s % 128
+    assert _call_mx(lib, ok, d_s=None) == 1                                   # null scales
+    assert _call_mx(lib, ok, sgu_s=ctypes.c_void_p((1 << 20) + 4)) == 1      # misaligned scales
+    assert _call_mx(lib, ok, ws=None) == 3                                    # no workspace
+    assert _call_mx(lib, moe.make_dims(0, 128, 16, 4, 128, 128, 0)) == 0     # T = 0: no work
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.moe_mxfp8_dequant(fake, fake, 4, 48, fake, None) == 1         # cols % 32
+    assert lib.moe_mxfp8_dequant(fake, fake, 0, 64, fake, None) == 0         # nothing to do
+    assert lib.moe_mxfp8_dequant(None, fake, 4, 64, fake, None) == 1         # null codes

@@ -68,7 +68,7 @@ def check_exact_weights(lib=None):
     cfg = wl.MoEConfig("mx", T=12, H=64, E=4, k=2, I=64, I_s=64, score_fn=wl.SOFTMAX)
     inp = wl.make_inputs(cfg, seed=5)
     g = torch.Generator().manual_seed(9)
-    for name in ("w_gate_up", "w_down"):
+    for name in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
         shape = inp[name].shape
         codes = torch.randint(0, 256, shape, generator=g, dtype=torch.int32).to(torch.uint8)
         codes[(codes & 0x7F) == 0x7F] = 0x30                         # no NaN codes
@@ -84,7 +84,7 @@ def check_exact_weights(lib=None):
         assert torch.equal(inp[name].float(), w)                    # exact in bf16
     ref = oracle.moe_forward(inp, cfg.k, cfg.score_fn, lib_path=lib)["out"]
     mx = dict(inp)
-    for name in ("w_gate_up", "w_down"):
+    for name in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
         q, s = wl.quantize_mxfp8(mx.pop(name))
         mx[name + "_q"], mx[name + "_s"] = q, s
     got = oracle.moe_forward_mxfp8(mx, cfg.k, cfg.score_fn, lib_path=lib)["out"]
