@@ -182,16 +182,18 @@ def mxfp8_to_bf16(codes, scales, lib_path: str | None = None):
 
 def moe_forward_mxfp8(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=None,
                       lib_path: str | None = None):
-    """The layer with MXFP8 routed-expert weights: the weights are dequantised
-    exactly (every MXFP8 value is a bf16 value) and the fp64 layer runs on them.
-    inputs holds w_gate_up_q / w_gate_up_s / w_down_q / w_down_s instead of
-    w_gate_up / w_down."""
+    """The layer with MXFP8 expert weights: every quantised matrix is
+    dequantised exactly (every MXFP8 value is a bf16 value) and the fp64
+    layer runs on the result. inputs holds <name>_q / <name>_s (codes and
+    scales) instead of <name> for w_gate_up and w_down, and for the shared
+    expert's ws_gate_up and ws_down where those are quantised too."""
     import torch
-    wgu = mxfp8_to_bf16(_np(inputs["w_gate_up_q"]), _np(inputs["w_gate_up_s"]), lib_path)
-    wd = mxfp8_to_bf16(_np(inputs["w_down_q"]), _np(inputs["w_down_s"]), lib_path)
-    plain = {n: v for n, v in inputs.items() if not n.startswith(("w_gate_up", "w_down"))}
-    plain["w_gate_up"] = torch.from_numpy(wgu.view(np.int16)).view(torch.bfloat16)
-    plain["w_down"] = torch.from_numpy(wd.view(np.int16)).view(torch.bfloat16)
+    plain = dict(inputs)
+    for name in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
+        if name + "_q" not in inputs:
+            continue
+        bits = mxfp8_to_bf16(_np(plain.pop(name + "_q")), _np(plain.pop(name + "_s")), lib_path)
+        plain[name] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     return moe_forward(plain, k, score_fn, tokens=tokens, gate_override=gate_override,
                        lib_path=lib_path)
 
