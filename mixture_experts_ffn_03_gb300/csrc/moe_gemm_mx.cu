@@ -81,19 +81,26 @@ struct MxCfg {
 
 // One converter thread's share of a stage: the 128 K values (8 chunks of 16
 // codes, 128-byte swizzled row `crow` of the stage's code tile) of one weight
-// row, scaled by sc[0], sc[sc_stride], ... (one scale per 32 values), written
-// to TMEM columns ta .. ta + 63 of this warp's lane quadrant.
-__device__ __forceinline__ void convert_row(uint32_t codes, int crow, const uint8_t* sc,
-                                            int sc_stride, uint32_t ta) {
+// row, scaled by the scale bytes at shared address sc, sc + sc_stride, ...
+// (one per 32 values), written to TMEM columns ta .. ta + 63 of this warp's
+// lane quadrant. All eight 16-byte loads and the four scale loads are issued
+// before the first conversion.
+__device__ __forceinline__ void convert_row(uint32_t codes, int crow, uint32_t sc, int sc_stride,
+                                            uint32_t ta) {
     const uint32_t row = codes + static_cast<uint32_t>(crow) * kCodeRow;
     const uint32_t swz = static_cast<uint32_t>(crow & 7);
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = ptx::ld_shared_v4u(row + ((c ^ swz) << 4));
+    uint32_t s[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] = ptx::ld_shared_u8(sc + j * sc_stride);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t s = sc[j * sc_stride];
         uint32_t out[16];
         uint32_t lo[8], hi[8];
-        mx_dequant16(ptx::ld_shared_v4u(row + (((2 * j) ^ swz) << 4)), s, lo);
-        mx_dequant16(ptx::ld_shared_v4u(row + (((2 * j + 1) ^ swz) << 4)), s, hi);
+        mx_dequant16(v[2 * j], s[j], lo);
+        mx_dequant16(v[2 * j + 1], s[j], hi);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             out[i] = lo[i];
@@ -135,11 +142,11 @@ __device__ __forceinline__ void converter_role(uint8_t* smem, Ctl* ctl, uint32_t
             const uint32_t ta = lane_base + C::A_BASE + t * C::A_COLS + part * 64;
             if constexpr (GU) {
                 // rows [0, 128) gate, [128, 256) up; scales [block][plane][row]
-                convert_row(codes, part * kGemmBM + r, st + C::SC_OFF + part * 128 + r, 256, ta);
+                convert_row(codes, part * kGemmBM + r, codes + C::SC_OFF + part * 128 + r, 256, ta);
             } else {
                 // code row 2r + part = K values [128 part, 128 part + 128) of row r;
                 // scales [block][row]
-                convert_row(codes, 2 * r + part, st + C::SC_OFF + (part * 4) * 128 + r, 128, ta);
+                convert_row(codes, 2 * r + part, codes + C::SC_OFF + (part * 4) * 128 + r, 128, ta);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();

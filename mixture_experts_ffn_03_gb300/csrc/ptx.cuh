@@ -155,6 +155,12 @@ __device__ __forceinline__ uint4 ld_shared_v4u(uint32_t addr) {
                  : "memory");
     return v;
 }
+// One byte from shared memory at a 32-bit shared address (zero-extended).
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 // Elementwise product of two bf16 pairs, rounded to nearest even.
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     uint32_t d;
