@@ -154,3 +154,18 @@ def make_inputs_mxfp8(cfg: MoEConfig, seed: int = 0, device: str = "cpu") -> dic
             q, s = quantize_mxfp8(w)
         inp[name + "_q"], inp[name + "_s"] = q, s
     return inp
+
+
+def make_inputs_router(cfg: MoEConfig, seed: int = 0, device: str = "cpu") -> dict:
+    """The inputs of make_inputs with the router logits replaced by router
+    weights: w_router [E, H] ~ N(0, 0.02) -> bf16, drawn after w_g from the
+    same generator (so the logits x . w_router^T have a spread close to the
+    N(0, 1) logits of make_inputs). No logits entry."""
+    dev = torch.device(device)
+    inp = make_inputs(cfg, seed=seed, device=device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 7919)
+    inp.pop("logits")
+    inp["w_router"] = _bf16(torch.randn(cfg.E, cfg.H, generator=g, device=dev,
+                                        dtype=torch.float32), 0.02)
+    return inp

@@ -51,6 +51,8 @@ def _bind(lib):
     lib.oracle_mxfp8_to_bf16.argtypes = [i, i, P, P, P]
     lib.oracle_mxfp8_to_bf16.restype = i
     lib.oracle_e4m3_table.argtypes = [P]
+    lib.oracle_router_logits.argtypes = [i, i, i, P, P, P]
+    lib.oracle_router_logits.restype = None
     lib.oracle_moe_forward.restype = i
     return lib
 
@@ -196,6 +198,34 @@ def moe_forward_mxfp8(inputs: dict, k: int, score_fn: int, tokens=None, gate_ove
         plain[name] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     return moe_forward(plain, k, score_fn, tokens=tokens, gate_override=gate_override,
                        lib_path=lib_path)
+
+
+def router_logits(hidden, w_router, lib_path: str | None = None) -> np.ndarray:
+    """fp64 router logits [T, E] = hidden [T, H] (bf16) . w_router [E, H] (bf16)^T."""
+    lib = _load(lib_path)
+    x = _u16(hidden)
+    w = _u16(w_router)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H
+    out = np.empty((T, E), dtype=np.float64)
+    lib.oracle_router_logits(T, H, E, _ptr(x), _ptr(w), _ptr(out))
+    return out
+
+
+def moe_forward_router(inputs: dict, k: int, score_fn: int, tokens=None,
+                       lib_path: str | None = None):
+    """The layer with the router computed on the FFN side: inputs holds
+    w_router [E, H] bf16 instead of logits. The fp32 router's logits are the
+    fp64 sums rounded once to fp32 (round to nearest even), and the layer
+    routes on them; returns moe_forward's dict plus logits64 (the fp64 sums)."""
+    import torch
+    lg64 = router_logits(inputs["hidden"], inputs["w_router"], lib_path)
+    plain = {n: v for n, v in inputs.items() if n != "w_router"}
+    plain["logits"] = torch.from_numpy(lg64.astype(np.float32))
+    res = moe_forward(plain, k, score_fn, tokens=tokens, lib_path=lib_path)
+    res["logits64"] = lg64
+    return res
 
 
 def _np(t):

@@ -197,6 +197,27 @@ void oracle_e4m3_table(double* out) {
     for (int b = 0; b < 256; ++b) out[b] = e4m3_value((uint8_t)b);
 }
 
+/*
+ * Router logits computed on the FFN side: l[t][e] = sum over h of
+ * x[t][h] * W_router[e][h], with W_router [E, H] bf16 (one row per expert,
+ * the layout of a linear layer's weight). The router runs in fp32 ("Add
+ * Qwen3.5-35B-A3B (support vision and text input)", Additional Information:
+ * router dtype float32): every product of two bf16 values is exact, the
+ * oracle sums them in fp64 in the natural order of h; out [T, E] holds the
+ * fp64 sums (the routing ranks them after one rounding to fp32).
+ */
+void oracle_router_logits(int T, int H, int E, const uint16_t* hidden, const uint16_t* w_router,
+                          double* out) {
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += bf16_value(hidden[(size_t)t * H + h]) *
+                       bf16_value(w_router[(size_t)e * H + h]);
+            out[(size_t)t * E + e] = acc;
+        }
+}
+
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /*
