@@ -169,6 +169,11 @@ def read_traffic(kernel: str, workload: str):
         return None
 
 
+def torch_index(toks):
+    import torch
+    return torch.as_tensor(toks, dtype=torch.long)
+
+
 def run_reference(args, cfg):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -211,19 +216,30 @@ def run_reference(args, cfg):
     return 0
 
 
-def time_cpu_baseline(cfg, inp_cpu, budget_s=12.0):
+def time_cpu_baseline(cfg, inp_cpu, budget_s=12.0, router=False):
     import numpy as np
     import oracle
     threads = oracle.default_threads()
     n = min(cfg.T, threads)
+    if router:  # the router's logits for the sampled tokens, then the layer
+        def run(toks):
+            x = inp_cpu["hidden"][torch_index(toks)]
+            lg = oracle.router_logits(x, inp_cpu["w_router"]).astype(np.float32)
+            plain = {k: v for k, v in inp_cpu.items() if k != "w_router"}
+            plain["hidden"] = x
+            plain["logits"] = lg
+            oracle.moe_forward(plain, cfg.k, cfg.score_fn, n_threads=threads)
+    else:
+        def run(toks):
+            oracle.moe_forward(inp_cpu, cfg.k, cfg.score_fn, tokens=toks, n_threads=threads)
     t0 = time.perf_counter()
-    oracle.moe_forward(inp_cpu, cfg.k, cfg.score_fn, tokens=np.arange(n), n_threads=threads)
+    run(np.arange(n))
     dt = time.perf_counter() - t0
     reps = max(1, int(budget_s / max(dt, 1e-3)))
     n_tok = n * reps  # about budget_s of CPU work
     toks = np.arange(n_tok) % cfg.T
     t0 = time.perf_counter()
-    oracle.moe_forward(inp_cpu, cfg.k, cfg.score_fn, tokens=toks, n_threads=threads)
+    run(toks)
     dt = time.perf_counter() - t0
     return dict(value=n_tok / dt, unit="tokens/s", cores=threads, kind="oracle",
                 sample=f"{n_tok} tokens of the {cfg.name} workload (token t mod {cfg.T}), fp64, "
@@ -240,6 +256,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "mxfp8"],
                     help="expert weight format: bf16, or MXFP8 codes + scales (moe_forward_mxfp8)")
+    ap.add_argument("--router", action="store_true",
+                    help="compute the router logits in the layer from W_router (moe_forward_router)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -263,7 +281,15 @@ def main():
     moe.load_library()
 
     mx = args.weights == "mxfp8"
-    if mx:
+    if mx and args.router:
+        raise SystemExit("--router runs with bf16 expert weights")
+    if args.router:
+        inp = wl.make_inputs_router(cfg, seed=0, device=str(dev))
+        layer = moe.MoELayerRouter(inp["w_router"], inp["w_gate_up"], inp["w_down"],
+                                   inp["ws_gate_up"], inp["ws_down"], inp["w_g"], cfg.k,
+                                   cfg.score_fn)
+        inp["logits"] = None
+    elif mx:
         inp = wl.make_inputs_mxfp8(cfg, seed=0, device=str(dev))
         pair = lambda n: (inp[n + "_q"], inp[n + "_s"])  # noqa: E731
         layer = moe.MoELayerMXFP8(pair("w_gate_up"), pair("w_down"), pair("ws_gate_up"),
@@ -285,6 +311,9 @@ def main():
     if st != moe.MOE_OK:
         raise RuntimeError(moe.status_string(st))
     work = algorithmic_work(cfg, counts.cpu().tolist(), wbytes=1.0 + 1.0 / 32 if mx else 2.0)
+    if args.router:  # W_router read and x . W_router^T computed instead of logits read
+        work["flops"] += 2.0 * T * cfg.E * cfg.H
+        work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * T * cfg.E
     gu_kernel = "moe_gate_up_mxfp8" if mx else "moe_gate_up"
 
     K = args.steps
@@ -368,7 +397,7 @@ def main():
     # every step's transfers inside the timed region. Serial: one step at a time
     # on one stream (L2 flushed between steps, outside the step events).
     h_host = inp["hidden"].cpu().pin_memory()
-    l_host = inp["logits"].cpu().pin_memory()
+    l_host = None if args.router else inp["logits"].cpu().pin_memory()
     o_hosts = [torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     o_host = o_hosts[0]
     with torch.cuda.stream(stream):
@@ -433,7 +462,7 @@ def main():
                       experts_touched=work["touched"],
                       frac_vs_nominal_8tbs=(work["bytes"] / 8e12 * 1e3) / ms_step)
     kernels = {n: round(statistics.mean(v) * 1e3, 2) for n, v in zip(moe.STAGE_NAMES, stage_ms)}
-    h2d = T * cfg.H * 2 + T * cfg.E * 4
+    h2d = T * cfg.H * 2 + (0 if args.router else T * cfg.E * 4)
     d2h = T * cfg.H * 2
     line = dict(
         metric="MoE-layer tokens/s", value=value, unit="tokens/s", n_gpus=world, steps=K,
@@ -441,6 +470,7 @@ def main():
         vs_baseline=None, dtype="bf16" if not mx else "bf16 (MXFP8 E4M3 weights, exact to bf16)",
         data="synthetic",
         config=dict(workload=workload_name(cfg), seed=0, weights=args.weights,
+                    router="in the layer (moe_forward_router)" if args.router else "logits input",
                     parallelism="replicas" if world > 1 else "1gpu",
                     l2="flushed: 256 MB write between timed steps", launch="stream",
                     wall_s=round(wall, 3)),
@@ -451,9 +481,10 @@ def main():
                  d2h_bytes_per_step=d2h,
                  mode="serving loop (moe.HostPipeline): transfers overlap neighbouring steps' compute",
                  serial_value=world * T * K / (e2e_serial_ms / 1e3)),
-        gpu_launches=moe.launch_count(layer.dims(T)) * K, clocks=clocks, cuda_graph=graph)
+        gpu_launches=(moe.launch_count_router if args.router else moe.launch_count)(layer.dims(T)) * K,
+        clocks=clocks, cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
-        inp_cpu = {n: t.cpu() for n, t in inp.items()}
+        inp_cpu = {n: t.cpu() for n, t in inp.items() if t is not None}
         if mx:
             # the oracle's MXFP8 layer is its bf16 layer on the exactly dequantised
             # weights: dequantise once, then time that layer
@@ -462,7 +493,7 @@ def main():
                 bits = oracle.mxfp8_to_bf16(oracle._np(inp_cpu.pop(n + "_q")),
                                             oracle._np(inp_cpu.pop(n + "_s")))
                 inp_cpu[n] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
-        line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu)
+        line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu, router=args.router)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

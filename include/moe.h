@@ -149,6 +149,40 @@ moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden, const float*
 moe_status moe_mxfp8_dequant(const void* codes, const void* scales, int rows, int cols, void* out,
                              void* cuda_stream);
 
+/*
+ * Run the layer with the router on the FFN side: the same computation as
+ * moe_forward, with the router logits computed first from the router weights
+ * instead of being passed in (the step just before the layer's boundary in
+ * "[RFC] Experimental Qwen3.5 MoE AFD support: CUDA correctness baseline",
+ * for callers that keep the router with the experts):
+ *   w_router   [E, H]  bf16  router weights, one row per expert
+ *   logits[t][e] = sum_h hidden[t][h] * w_router[e][h], accumulated in fp32
+ *   (the router runs in fp32: "Add Qwen3.5-35B-A3B (support vision and text
+ *   input)", Additional Information; the products of bf16 values are exact),
+ *   in an order fixed by the sizes and the GPU's SM count (repeat calls on
+ *   one GPU give the same bits): a tensor-core GEMM whose K dimension may be
+ *   split across CTAs, the routing kernel adding the split partial sums in a
+ *   fixed order; the routing then ranks these fp32 logits.
+ *   logits_out [T, E] fp32 receives the logits (NULL: not returned).
+ * The workspace must hold moe_workspace_size_router(d) bytes. With
+ * moe_set_stage_events, stage 0 spans the router GEMM and the routing. Other
+ * arguments, returns and errors as moe_forward.
+ */
+moe_status moe_forward_router(const moe_dims* d, const void* hidden, const void* w_router,
+                              const void* w_gate_up, const void* w_down, const void* ws_gate_up,
+                              const void* ws_down, const void* w_g, void* out, float* logits_out,
+                              int32_t* topk_ids_out, float* topk_w_out,
+                              int32_t* expert_counts_out, void* workspace,
+                              size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace bytes of moe_forward_router: moe_workspace_size(d) plus the
+ * router GEMM's split-K partial sums (0 for invalid sizes). */
+size_t moe_workspace_size_router(const moe_dims* d);
+
+/* Kernels one moe_forward_router launches: those of moe_forward plus the
+ * router GEMM (0 for invalid sizes or T = 0). */
+int moe_launch_count_router(const moe_dims* d);
+
 /* Synchronise cuda_stream, then report MOE_ERR_DEVICE_TIMEOUT if the last
  * moe_forward that used this workspace hit a pipeline timeout, MOE_ERR_CUDA
  * on a CUDA error, else MOE_OK. */

@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
             "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count",
-            "moe_selftest_wait_limit", "moe_forward_mxfp8", "moe_mxfp8_dequant"]
+            "moe_selftest_wait_limit", "moe_forward_mxfp8", "moe_mxfp8_dequant",
+            "moe_forward_router", "moe_workspace_size_router", "moe_launch_count_router"]
 NUM_STAGES = 6
 STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
 
@@ -85,6 +86,12 @@ def load_library(path: str = LIB_PATH):
     lib.moe_forward_mxfp8.restype = ctypes.c_int
     lib.moe_mxfp8_dequant.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
     lib.moe_mxfp8_dequant.restype = ctypes.c_int
+    lib.moe_forward_router.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 12 + [P, ctypes.c_size_t, P]
+    lib.moe_forward_router.restype = ctypes.c_int
+    lib.moe_workspace_size_router.argtypes = [ctypes.POINTER(MoEDims)]
+    lib.moe_workspace_size_router.restype = ctypes.c_size_t
+    lib.moe_launch_count_router.argtypes = [ctypes.POINTER(MoEDims)]
+    lib.moe_launch_count_router.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -178,6 +185,27 @@ def mxfp8_dequant(codes, scales, out=None, stream=None):
     return out
 
 
+def forward_router_raw(dims: MoEDims, hidden, w_router, w_gate_up, w_down, ws_gate_up, ws_down,
+                       w_g, out, workspace, logits_out=None, topk_ids_out=None, topk_w_out=None,
+                       counts_out=None, stream=None) -> int:
+    """Direct call of moe_forward_router on tensors (or None); returns the status code."""
+    lib = load_library()
+    return int(lib.moe_forward_router(
+        ctypes.byref(dims), _ptr(hidden), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
+        _ptr(ws_gate_up), _ptr(ws_down), _ptr(w_g), _ptr(out), _ptr(logits_out),
+        _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(counts_out), _ptr(workspace),
+        ctypes.c_size_t(0 if workspace is None else workspace.numel()), _stream_handle(stream)))
+
+
+def workspace_size_router(dims: MoEDims) -> int:
+    return int(load_library().moe_workspace_size_router(ctypes.byref(dims)))
+
+
+def launch_count_router(dims: MoEDims) -> int:
+    """Kernels one moe_forward_router launches for these sizes on the current device."""
+    return int(load_library().moe_launch_count_router(ctypes.byref(dims)))
+
+
 def device_status(workspace, stream=None) -> int:
     return int(load_library().moe_device_status(_ptr(workspace), _stream_handle(stream)))
 
@@ -231,8 +259,9 @@ class MoELayer:
         return out
 
     def forward_from_host(self, hidden_host, logits_host, out_host, stream=None):
-        """End-to-end call from pinned host buffers: copy hidden and logits in,
-        run the layer, copy the output back (all on one stream)."""
+        """End-to-end call from pinned host buffers: copy hidden and logits in
+        (no logits for a layer that computes them itself: pass None), run the
+        layer, copy the output back (all on one stream)."""
         import torch
         T = hidden_host.shape[0]
         if not hasattr(self, "_io") or self._io[0].shape[0] != T:
@@ -243,8 +272,11 @@ class MoELayer:
         s = stream or torch.cuda.current_stream()
         with torch.cuda.stream(s):
             h.copy_(hidden_host, non_blocking=True)
-            l.copy_(logits_host, non_blocking=True)
-            self.forward(h, l, out=o, stream=s)
+            if logits_host is not None:
+                l.copy_(logits_host, non_blocking=True)
+                self.forward(h, l, out=o, stream=s)
+            else:
+                self.forward(h, out=o, stream=s)
             out_host.copy_(o, non_blocking=True)
         return out_host
 
@@ -280,6 +312,38 @@ class MoELayerMXFP8(MoELayer):
         return out
 
 
+class MoELayerRouter(MoELayer):
+    """MoELayer that computes the router logits itself (moe_forward_router):
+    forward(hidden) with w_router [E, H] bf16 held by the layer; the logits
+    [T, E] fp32 are returned through `logits` when given."""
+
+    def __init__(self, w_router, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int,
+                 score_fn: int):
+        super().__init__(w_gate_up, w_down, ws_gate_up, ws_down, w_g, k, score_fn)
+        self.w_router = w_router
+
+    def workspace(self, T: int):
+        import torch
+        need = workspace_size_router(self.dims(T))
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, hidden, logits=None, out=None, topk_ids=None, topk_w=None, counts=None,
+                stream=None):
+        import torch
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        ws = self.workspace(T)
+        st = forward_router_raw(self.dims(T), hidden, self.w_router, self.w_gate_up, self.w_down,
+                                self.ws_gate_up, self.ws_down, self.w_g, out, ws, logits,
+                                topk_ids, topk_w, counts, stream)
+        if st != MOE_OK:
+            raise MoEError(st, "moe_forward_router")
+        return out
+
+
 class HostPipeline:
     """Serving loop from pinned host buffers that overlaps host transfers with
     compute. Each submit() copies one step's hidden rows and router logits on a
@@ -288,7 +352,8 @@ class HostPipeline:
     copy stream once the layer is done; the next step's input copy overlaps
     this step's compute. Every byte still crosses between host and device on
     every step. A caller reuses an out_host buffer only after drain() (or after
-    two further submits)."""
+    two further submits). For a layer that computes its own router logits
+    (MoELayerRouter) pass logits_host=None: only the hidden rows go in."""
 
     def __init__(self, layer, T, compute_stream=None, copy_stream=None):
         import torch
@@ -310,11 +375,15 @@ class HostPipeline:
         self.xs.wait_event(self.done[b])          # step i-2 no longer reads set b
         with torch.cuda.stream(self.xs):
             self.h[b].copy_(hidden_host, non_blocking=True)
-            self.l[b].copy_(logits_host, non_blocking=True)
+            if logits_host is not None:
+                self.l[b].copy_(logits_host, non_blocking=True)
             self.in_ready[b].record(self.xs)
         self.cs.wait_event(self.in_ready[b])
         self.cs.wait_event(self.out_read[b])       # step i-2's output has been copied out
-        self.layer.forward(self.h[b], self.l[b], out=self.o[b], stream=self.cs)
+        if logits_host is not None:
+            self.layer.forward(self.h[b], self.l[b], out=self.o[b], stream=self.cs)
+        else:
+            self.layer.forward(self.h[b], out=self.o[b], stream=self.cs)
         self.done[b].record(self.cs)
         self.xs.wait_event(self.done[b])
         with torch.cuda.stream(self.xs):

@@ -72,6 +72,21 @@ Layout layout_of(const moe_dims& d) {
     return L;
 }
 
+// Extra workspace of the FFN-side router, after the standard layout: the
+// router GEMM's split-K partial sums [max splits, T, E] fp32.
+struct RouterLayout {
+    size_t partial, total;
+};
+
+RouterLayout router_layout_of(const moe_dims& d) {
+    RouterLayout R{};
+    const size_t n = static_cast<size_t>(d.T) * d.E;
+    const int cap = router_max_splits(d.T, d.H, d.E);
+    R.partial = layout_of(d).total;
+    R.total = align_up(R.partial + (n ? static_cast<size_t>(cap) * n * 4 : 1), kAlign);
+    return R;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -323,15 +338,24 @@ bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, ch
     return ok;
 }
 
+// w_router == nullptr: router_logits are an input. Otherwise the layer first
+// computes them from w_router [E, H] into logits_out (if given) or its
+// workspace (router_logits must then be null).
 moe_status forward_impl(const moe_dims* d, const void* hidden, const float* router_logits,
-                        const ExpertWeights& W, const void* w_g, void* out,
-                        int32_t* topk_ids_out, float* topk_w_out, int32_t* expert_counts_out,
-                        void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                        const void* w_router, float* logits_out, const ExpertWeights& W,
+                        const void* w_g, void* out, int32_t* topk_ids_out, float* topk_w_out,
+                        int32_t* expert_counts_out, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream) {
     if (!dims_valid(d)) return MOE_ERR_INVALID_ARG;
     if (!dims_supported(d) || (W.mx && !dims_supported_mx(d))) return MOE_ERR_UNSUPPORTED;
     if (d->T == 0) return MOE_OK;
-    const void* required[] = {hidden, router_logits, W.gate_up, W.down, W.s_gate_up,
-                              W.s_down, w_g, out};
+    if (w_router) {
+        if (router_logits) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(w_router) || (logits_out && !aligned16(logits_out)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const void* required[] = {hidden, w_router ? w_router : router_logits, W.gate_up, W.down,
+                              W.s_gate_up, W.s_down, w_g, out};
     for (const void* p : required)
         if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
     if (W.mx) {
@@ -343,7 +367,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     for (const void* p : optional)
         if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
     const Layout L = layout_of(*d);
-    if (!workspace || workspace_bytes < L.total ||
+    const RouterLayout RL = router_layout_of(*d);
+    if (!workspace || workspace_bytes < (w_router ? RL.total : L.total) ||
         (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return MOE_ERR_WORKSPACE;
 
@@ -441,10 +466,25 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
 
     // Status words (error flags, tile counts, completion ticket) start at zero.
     if (cudaMemsetAsync(meta, 0, META_WORDS * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    mark_stage(0, st);
+    LogitSrc lsrc{router_logits, 1, 0, nullptr};
+    if (w_router) {
+        // The router GEMM belongs to stage 0; the routing kernels add its partial sums.
+        const RouterPlan rp = router_plan(T, H, E, num_sms);
+        CUtensorMap map_w{}, map_x{};
+        if (!make_map(&map_w, w_router, H, E, kGemmBM) ||
+            !make_map(&map_x, hidden, H, T, static_cast<uint32_t>(rp.bn)))
+            return MOE_ERR_CUDA;
+        float* partial = reinterpret_cast<float*>(ws + RL.partial);
+        if (launch_router(rp, map_w, map_x, T, H, E, partial,
+                          reinterpret_cast<unsigned*>(meta + META_ERR), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        lsrc = LogitSrc{partial, rp.splits, static_cast<size_t>(T) * E, logits_out};
+    }
+    const bool route_pdl = w_router != nullptr;
     if (route_small_fits(T, E, k)) {
         // Routing and the whole permute in one launch; stages 1 and 2 are empty.
-        mark_stage(0, st);
-        if ((launch_route_permute(T, H, E, k, d->score_fn, bn_gu, bn_dn, router_logits,
+        if ((launch_route_permute(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, route_pdl,
                                   static_cast<const __nv_bfloat16*>(hidden),
                                   static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w,
                                   gate_logit, counts, offsets, perm, inv, rt_gu, rt_dn, meta,
@@ -453,8 +493,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         mark_stage(1, st);
         mark_stage(2, st);
     } else {
-        mark_stage(0, st);
-        if ((launch_route(T, H, E, k, d->score_fn, router_logits,
+        if ((launch_route(T, H, E, k, d->score_fn, lsrc, route_pdl,
                           static_cast<const __nv_bfloat16*>(hidden),
                           static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w, gate_logit,
                           topk_ids_out, topk_w_out, st)) != cudaSuccess)
@@ -499,8 +538,35 @@ MOE_API moe_status moe_forward(const moe_dims* d, const void* hidden, const floa
     W.down = w_down;
     W.s_gate_up = ws_gate_up;
     W.s_down = ws_down;
-    return forward_impl(d, hidden, router_logits, W, w_g, out, topk_ids_out, topk_w_out,
-                        expert_counts_out, workspace, workspace_bytes, cuda_stream);
+    return forward_impl(d, hidden, router_logits, nullptr, nullptr, W, w_g, out, topk_ids_out,
+                        topk_w_out, expert_counts_out, workspace, workspace_bytes, cuda_stream);
+}
+
+MOE_API moe_status moe_forward_router(const moe_dims* d, const void* hidden, const void* w_router,
+                                      const void* w_gate_up, const void* w_down,
+                                      const void* ws_gate_up, const void* ws_down, const void* w_g,
+                                      void* out, float* logits_out, int32_t* topk_ids_out,
+                                      float* topk_w_out, int32_t* expert_counts_out,
+                                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    if (!w_router) return MOE_ERR_INVALID_ARG;
+    ExpertWeights W{};
+    W.mx = false;
+    W.gate_up = w_gate_up;
+    W.down = w_down;
+    W.s_gate_up = ws_gate_up;
+    W.s_down = ws_down;
+    return forward_impl(d, hidden, nullptr, w_router, logits_out, W, w_g, out, topk_ids_out,
+                        topk_w_out, expert_counts_out, workspace, workspace_bytes, cuda_stream);
+}
+
+MOE_API size_t moe_workspace_size_router(const moe_dims* d) {
+    if (!dims_valid(d)) return 0;
+    return router_layout_of(*d).total;
+}
+
+MOE_API int moe_launch_count_router(const moe_dims* d) {
+    if (!dims_valid(d) || !dims_supported(d) || d->T == 0) return 0;
+    return (route_small_fits(d->T, d->E, d->k) ? 4 : 6) + 1;
 }
 
 MOE_API moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden,
@@ -522,8 +588,8 @@ MOE_API moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden,
     W.down_sc = static_cast<const uint8_t*>(w_down_s);
     W.s_gate_up_sc = static_cast<const uint8_t*>(ws_gate_up_s);
     W.s_down_sc = static_cast<const uint8_t*>(ws_down_s);
-    return forward_impl(d, hidden, router_logits, W, w_g, out, topk_ids_out, topk_w_out,
-                        expert_counts_out, workspace, workspace_bytes, cuda_stream);
+    return forward_impl(d, hidden, router_logits, nullptr, nullptr, W, w_g, out, topk_ids_out,
+                        topk_w_out, expert_counts_out, workspace, workspace_bytes, cuda_stream);
 }
 
 MOE_API moe_status moe_mxfp8_dequant(const void* codes, const void* scales, int rows, int cols,

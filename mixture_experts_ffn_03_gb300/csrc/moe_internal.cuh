@@ -33,6 +33,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 enum : unsigned {
     ERR_GATE_UP_TIMEOUT = 1u << 0,
     ERR_DOWN_TIMEOUT = 1u << 1,
+    ERR_ROUTER_TIMEOUT = 1u << 2,
 };
 
 // Status block layout (int32 words at the start of the workspace).
@@ -54,15 +55,28 @@ constexpr int kGemmBK = 64;             // K elements per pipeline stage
 constexpr int kEpiRows = 16;            // token rows per epilogue store box
 constexpr int kEpiCols = 32;            // output columns per epilogue warp (one TMEM lane each)
 
-// Routing, histogram/scan, scatter and combine (moe_route.cu).
+// Where the routing kernels read the logits: the sum, in order, of `parts`
+// fp32 arrays [T, E] spaced part_stride floats apart (parts = 1: the caller's
+// logits; more: the router GEMM's split-K partial sums). `out` (optional)
+// receives the summed logits.
+struct LogitSrc {
+    const float* p;
+    int parts;
+    size_t part_stride;
+    float* out;
+};
+
+// Routing, histogram/scan, scatter and combine (moe_route.cu). With `pdl` the
+// routing launch is a programmatic dependent of the previous kernel (the
+// router GEMM) and waits for it before reading the logits.
 bool route_small_fits(int T, int E, int k);
 cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
-                                 const float* logits, const __nv_bfloat16* hidden,
+                                 const LogitSrc& logits, bool pdl, const __nv_bfloat16* hidden,
                                  const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
                                  float* gate_logit, int* counts, int* offsets, int* perm,
                                  int* inv, int4* rt_gu, int4* rt_dn, int* meta, int* ids_out,
                                  float* w_out, int* counts_out, cudaStream_t st);
-cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const float* logits,
+cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const LogitSrc& logits, bool pdl,
                          const __nv_bfloat16* hidden, const __nv_bfloat16* w_g, int* topk_ids,
                          float* topk_w, float* gate_logit, int* ids_out, float* w_out,
                          cudaStream_t st);
@@ -156,6 +170,21 @@ cudaError_t launch_gate_up_mx(int bn, const MxMaps& maps, const GemmArgs& a, int
                               int num_sms, cudaStream_t st);
 cudaError_t launch_down_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
                            int num_sms, cudaStream_t st);
+// Router GEMM (moe_router.cu): logits [T, E] fp32 = hidden [T, H] . W_router [E, H]^T,
+// as a split-K GEMM (tiles of 128 experts x bn tokens, `splits` K ranges) that
+// writes the partial sums [splits, T, E]; the routing kernels add them in a
+// fixed order (LogitSrc).
+constexpr int kRouterMaxSplits = 32;
+struct RouterPlan {
+    int bn;      // tokens per tile (16 .. 256)
+    int splits;  // K ranges (1 = the GEMM writes the logits directly)
+};
+int router_max_splits(int T, int H, int E);  // bound on splits (sizes the workspace)
+RouterPlan router_plan(int T, int H, int E, int num_sms);
+// map_w: W_router [E, H] in boxes of 64 x 128 rows; map_x: hidden [T, H], boxes 64 x bn.
+cudaError_t launch_router(const RouterPlan& p, const CUtensorMap& map_w, const CUtensorMap& map_x,
+                          int T, int H, int E, float* partial, unsigned* err, cudaStream_t st);
+
 // bf16 values of an MXFP8 matrix [rows, cols] (scales [cols/32, rows]).
 cudaError_t launch_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int rows, int cols,
                                  __nv_bfloat16* out, cudaStream_t st);

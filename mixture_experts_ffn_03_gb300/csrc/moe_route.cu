@@ -223,7 +223,7 @@ __device__ __forceinline__ void ordered_scatter(const int* ids, long a0, long a1
 // Routing of one token per warp; writes ids, weights and the gate logit.
 template <int EPL>
 __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int score_fn,
-                                                const float* __restrict__ logits,
+                                                const LogitSrc& logits,
                                                 const __nv_bfloat16* __restrict__ hidden,
                                                 const __nv_bfloat16* __restrict__ w_g,
                                                 int* __restrict__ topk_ids,
@@ -232,12 +232,30 @@ __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int 
                                                 int* __restrict__ ids_out,
                                                 float* __restrict__ w_out, int lane) {
     // All loads are issued first: the hidden row's latency overlaps the top-k.
-    const float* lg = logits + static_cast<size_t>(t) * E;
+    const float* lg = logits.p + static_cast<size_t>(t) * E;
     float v[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         v[i] = e < E ? __ldcs(lg + e) : 0.f;
+    }
+    if (logits.parts > 1) {  // split-K partial sums of the router GEMM, added in order
+        for (int s = 1; s < logits.parts; ++s) {
+            const float* ls = lg + static_cast<size_t>(s) * logits.part_stride;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) v[i] += __ldcs(ls + e);
+            }
+        }
+    }
+    if (logits.out) {
+        float* lo = logits.out + static_cast<size_t>(t) * E;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) lo[e] = v[i];
+        }
     }
     GateLogit gl;
     gl.load(t, H, hidden, w_g, lane, 0);
@@ -261,7 +279,7 @@ __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int 
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
-                     const float* __restrict__ logits, const __nv_bfloat16* __restrict__ hidden,
+                     const LogitSrc logits, const __nv_bfloat16* __restrict__ hidden,
                      const __nv_bfloat16* __restrict__ w_g, int* __restrict__ topk_ids,
                      float* __restrict__ topk_w, float* __restrict__ gate_logit,
                      int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm,
@@ -273,6 +291,7 @@ route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn
     __shared__ int s_is_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ptx::griddep_launch_dependents();
+    ptx::griddep_wait();  // no-op unless launched behind the router GEMM
     const int t = blockIdx.x * kRouteWarps + warp;
     if (t < T)
         route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w,
@@ -349,13 +368,14 @@ route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn
 // ------------------------------------------------------------ large batches
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-route_kernel(int T, int H, int E, int k, int score_fn, const float* __restrict__ logits,
+route_kernel(int T, int H, int E, int k, int score_fn, const LogitSrc logits,
              const __nv_bfloat16* __restrict__ hidden, const __nv_bfloat16* __restrict__ w_g,
              int* __restrict__ topk_ids, float* __restrict__ topk_w,
              float* __restrict__ gate_logit, int* __restrict__ ids_out,
              float* __restrict__ w_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_launch_dependents();
+    ptx::griddep_wait();  // no-op unless launched behind the router GEMM
     const int t = blockIdx.x * kRouteWarps + warp;
     if (t >= T) return;
     route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w, gate_logit,
@@ -629,7 +649,7 @@ int experts_per_lane(int E) {
     }
 
 cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
-                                 const float* logits, const __nv_bfloat16* hidden,
+                                 const LogitSrc& logits, bool pdl, const __nv_bfloat16* hidden,
                                  const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
                                  float* gate_logit, int* counts, int* offsets, int* perm,
                                  int* inv, int4* rt_gu, int4* rt_dn, int* meta, int* ids_out,
@@ -639,20 +659,20 @@ cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int b
                         sizeof(int);
 #define MOE_LAUNCH_RP(N)                                                                        \
     return launch_kernel(route_permute_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), smem,  \
-                         st, false, T, H, E, k, score_fn, bn_gu, bn_dn, logits, hidden, w_g,    \
+                         st, pdl, T, H, E, k, score_fn, bn_gu, bn_dn, logits, hidden, w_g,      \
                          topk_ids, topk_w, gate_logit, counts, offsets, perm, inv, rt_gu, rt_dn, \
                          meta, ids_out, w_out, counts_out)
     MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_RP)
 #undef MOE_LAUNCH_RP
 }
 
-cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const float* logits,
+cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const LogitSrc& logits, bool pdl,
                          const __nv_bfloat16* hidden, const __nv_bfloat16* w_g, int* topk_ids,
                          float* topk_w, float* gate_logit, int* ids_out, float* w_out,
                          cudaStream_t st) {
     const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
 #define MOE_LAUNCH_R(N)                                                                      \
-    return launch_kernel(route_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), 0, st, false, \
+    return launch_kernel(route_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), 0, st, pdl,   \
                          T, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w,         \
                          gate_logit, ids_out, w_out)
     MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_R)

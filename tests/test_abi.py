@@ -121,3 +121,21 @@ def test_host_validation_mxfp8(lib):
     assert lib.moe_mxfp8_dequant(fake, fake, 4, 48, fake, None) == 1         # cols % 32
     assert lib.moe_mxfp8_dequant(fake, fake, 0, 64, fake, None) == 0         # nothing to do
     assert lib.moe_mxfp8_dequant(None, fake, 4, 64, fake, None) == 1         # null codes
+
+
+def test_host_validation_router(lib):
+    import mixture_experts_ffn_03_gb300 as moe
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    ok = moe.make_dims(16, 128, 16, 4, 64, 64, 0)
+
+    def call(dims, w_router=fake, ws_bytes=1 << 40, logits_out=None):
+        return lib.moe_forward_router(ctypes.byref(dims), fake, w_router, fake, fake, fake, fake,
+                                      fake, fake, logits_out, None, None, None, fake,
+                                      ctypes.c_size_t(ws_bytes), None)
+    assert call(ok, w_router=None) == 1                                       # no router weights
+    assert call(ok, logits_out=P((1 << 20) + 4)) == 1                         # misaligned logits
+    assert call(ok, ws_bytes=moe.workspace_size(ok)) == 3                     # plain size too small
+    assert call(moe.make_dims(16, 96, 16, 4, 64, 64, 0)) == 2                 # H % 64
+    assert call(moe.make_dims(0, 128, 16, 4, 64, 64, 0)) == 0                 # T = 0
+    assert moe.workspace_size_router(ok) > moe.workspace_size(ok)
