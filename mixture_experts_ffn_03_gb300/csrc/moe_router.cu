@@ -151,7 +151,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_const
                 uint32_t v[16];
                 ptx::tmem_ld_32x32b_x16(tb + c0, v);
                 ptx::tmem_ld_wait();
-                if (e < E) {  // every K range has at least two steps, so D is written
+                if (e < E) {  // every K range has at least one step, so D is written
 #pragma unroll
                     for (int n = 0; n < 16; ++n) {
                         const int t = n0 + c0 + n;
@@ -187,8 +187,10 @@ int router_max_splits(int T, int H, int E) {
     const int ksteps = H / kGemmBK;
     const size_t logits = static_cast<size_t>(T) * E;
     int cap = 1;
-    // powers of two, at least two K steps per split, partial sums <= 2^26 floats (256 MB)
-    while (cap * 2 <= kRouterMaxSplits && ksteps / (cap * 2) >= 2 &&
+    // Powers of two, at least eight K steps per split (fewer, longer splits beat
+    // more CTAs: the routing kernel reads every partial sum; measured at decode
+    // and prefill against two and four steps), partial sums <= 2^26 floats (256 MB).
+    while (cap * 2 <= kRouterMaxSplits && ksteps / (cap * 2) >= 8 &&
            logits * static_cast<size_t>(cap * 2) <= (static_cast<size_t>(1) << 26))
         cap *= 2;
     return cap;
@@ -201,8 +203,8 @@ RouterPlan router_plan(int T, int H, int E, int num_sms) {
     const int tiles = ((E + kGemmBM - 1) / kGemmBM) * ((T + p.bn - 1) / p.bn);
     const int ksteps = H / kGemmBK;
     p.splits = 1;
-    // Split K while the grid stays within two CTAs per SM and every split keeps
-    // at least two K steps, up to router_max_splits (which sizes the workspace).
+    // Split K while the grid stays within two CTAs per SM, up to
+    // router_max_splits (which sizes the workspace).
     const int cap = router_max_splits(T, H, E);
     while (p.splits * 2 <= cap && tiles * p.splits * 2 <= 2 * num_sms) p.splits *= 2;
     return p;
