@@ -325,15 +325,6 @@ bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, ch
         ok = ok && make_map_nd(&dn->h, BF16, ws + L.h_hi, 4, dr, sr, box, SW) &&
              make_map_nd(&dn->hs, BF16, ws + L.hs_hi, 4, dsh, ssh, box, SW);
     }
-    {   // gate_up stores into the panels: {64, P, K / 64}, boxes 32 x kEpiRows x 1
-        const uint32_t box[3] = {static_cast<uint32_t>(kEpiCols), static_cast<uint32_t>(kEpiRows), 1};
-        const uint64_t dr[3] = {64, tk, I / 64}, sr[2] = {128, 2 * tk * 128};
-        const uint64_t dsh[3] = {64, T, Is / 64}, ssh[2] = {128, 2 * T * 128};
-        ok = ok && make_map_nd(&gu->st[0], BF16, ws + L.h_hi, 3, dr, sr, box, NOSW) &&
-             make_map_nd(&gu->st[1], BF16, ws + L.h_hi + tk * 128, 3, dr, sr, box, NOSW) &&
-             make_map_nd(&gu->st[2], BF16, ws + L.hs_hi, 3, dsh, ssh, box, NOSW) &&
-             make_map_nd(&gu->st[3], BF16, ws + L.hs_hi + T * 128, 3, dsh, ssh, box, NOSW);
-    }
     ok = ok && make_store_map(&dn->st[0], ws + L.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T);
     return ok;
 }

@@ -55,7 +55,9 @@ struct MxCfg {
     static constexpr int STAGES_1BUF =
         (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * kStgBytes) / STAGE_BYTES;
     static constexpr int EPI_BUFS = (STAGES_2BUF < 4 && STAGES_1BUF > STAGES_2BUF) ? 1 : 2;
-    static constexpr int EPI_BYTES = kEpiWarps * EPI_BUFS * kStgBytes;
+    // gate_up writes h with plain stores (decode tiles are ragged anyway), which
+    // leaves its shared memory to one more pipeline stage; down stages y.
+    static constexpr int EPI_BYTES = GU ? 0 : kEpiWarps * EPI_BUFS * kStgBytes;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - CTL_BYTES - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
     static constexpr int CTL_OFF = STAGES * STAGE_BYTES;
@@ -343,11 +345,11 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
         ptx::cp_async_wait_all();
     } else if (warp < kFirstCvtWarp) {  // -------------------- epilogue (warps 4-11)
         // As the gate_up epilogue with the weights on M in moe_gemm.cu, with h
-        // written in 64-column panels: warp we drains TMEM lanes 32*(warp % 4)
-        // (32 intermediate features) for the 16-token chunks 16*(we / 4) + 32*j.
+        // written with plain stores into 64-column panels: warp we drains TMEM
+        // lanes 32*(warp % 4) (32 intermediate features, one per lane) for the
+        // 16-token chunks 16*(we / 4) + 32*j; a warp's stores of one token row
+        // are 64 contiguous bytes.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
-        uint8_t* stg = smem + C::EPI_OFF + we * C::EPI_BUFS * kStgBytes;
-        uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
         int qs = 0;
@@ -356,12 +358,11 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
         while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
-            const int i0 = ti.f * kGemmBM + q * kEpiCols;  // feature of lane 0 (< I or I_s)
+            const int i = ti.f * kGemmBM + q * kEpiCols + lane;  // this lane's feature (< I or I_s)
             const size_t P = ti.shared ? static_cast<size_t>(a.T)
                                        : static_cast<size_t>(a.T) * a.k;
-            const CUtensorMap* m_hi = ti.shared ? &maps.st[2] : &maps.st[0];
-            const CUtensorMap* m_lo = ti.shared ? &maps.st[3] : &maps.st[1];
-            __nv_bfloat16* hp = ti.shared ? a.hs_hi : a.h_hi;  // panel base
+            __nv_bfloat16* panel = (ti.shared ? a.hs_hi : a.h_hi) +
+                                   static_cast<size_t>(i >> 6) * 2 * P * 64 + (i & 63);
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
             for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
                 uint32_t g[kEpiRows], u[kEpiRows];
@@ -369,40 +370,15 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
                 ptx::tmem_ld_32x32b_x16(tb + BN + c0, u);
                 ptx::tmem_ld_wait();
                 const int rows = min(kEpiRows, ti.n_rows - c0);
-                if (rows == kEpiRows) {
-                    const uint32_t b = nbuf++ % C::EPI_BUFS;
-                    __nv_bfloat16* shi = reinterpret_cast<__nv_bfloat16*>(stg + b * kStgBytes);
-                    __nv_bfloat16* slo = shi + kEpiRows * kEpiCols;
-                    if (lane == 0) ptx::bulk_wait_read<C::EPI_BUFS - 1>();  // buffer b is free
-                    __syncwarp();
 #pragma unroll
-                    for (int n = 0; n < kEpiRows; ++n) {
+                for (int n = 0; n < kEpiRows; ++n) {
+                    if (n < rows) {
                         const float gv = __uint_as_float(g[n]);
                         const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
                         const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                        shi[n * kEpiCols + lane] = hi;
-                        slo[n * kEpiCols + lane] = __float2bfloat16_rn(h - __bfloat162float(hi));
-                    }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_3d(m_hi, ptx::smem_u32(shi), i0 & 63, ti.p0 + c0, i0 >> 6);
-                        ptx::tma_store_3d(m_lo, ptx::smem_u32(slo), i0 & 63, ti.p0 + c0, i0 >> 6);
-                        ptx::bulk_commit();
-                    }
-                } else {
-                    const int i = i0 + lane;
-                    __nv_bfloat16* panel = hp + static_cast<size_t>(i >> 6) * 2 * P * 64 + (i & 63);
-#pragma unroll
-                    for (int n = 0; n < kEpiRows; ++n) {
-                        if (n < rows) {
-                            const float gv = __uint_as_float(g[n]);
-                            const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
-                            const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                            const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * 64;
-                            panel[o] = hi;
-                            panel[o + P * 64] = __float2bfloat16_rn(h - __bfloat162float(hi));
-                        }
+                        const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * 64;
+                        panel[o] = hi;
+                        panel[o + P * 64] = __float2bfloat16_rn(h - __bfloat162float(hi));
                     }
                 }
             }
@@ -414,7 +390,6 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
                 aph ^= 1u;
             }
         }
-        if (lane == 0) ptx::bulk_wait_all();
     } else {  // --------------------------------------------- converters (warps 12-19)
         converter_role<C, true>(smem, ctl, tmem_base, warp, lane, a, abort_flag, err, code);
     }

@@ -142,8 +142,8 @@ struct GemmMaps {
 // h of the MXFP8 path is stored in 64-column panels: panel c holds columns
 //   64c..64c+63 of the P rows of h_hi, then of h_lo (P = T*k routed, T
 //   shared), so one box brings the hi and lo rows of four 64-column K
-//   slices. st[0..3] (gate_up) = the hi and lo planes of the routed and the
-//   shared panels as {64, P, I/64}, boxes 32 x kEpiRows x 1; st[0] (down) = y.
+//   slices (the gate_up epilogue writes the panels with plain stores).
+//   st[0] (down) = y.
 struct MxMaps {
     CUtensorMap w;
     CUtensorMap ws;
