@@ -169,3 +169,66 @@ def make_inputs_router(cfg: MoEConfig, seed: int = 0, device: str = "cpu") -> di
     inp["w_router"] = _bf16(torch.randn(cfg.E, cfg.H, generator=g, device=dev,
                                         dtype=torch.float32), 0.02)
     return inp
+
+
+_E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _round_e2m1(v: torch.Tensor) -> torch.Tensor:
+    """E2M1 code (0..15) of the value nearest to v, ties to the even mantissa,
+    saturating at +-6."""
+    a = v.abs()
+    # midpoints with the tie going to the even code: 0.25->0, 0.75->1.0, 1.25->1.0,
+    # 1.75->2.0, 2.5->2.0, 3.5->4.0, 5->4.0
+    mag = torch.zeros_like(a, dtype=torch.uint8)
+    mag = torch.where(a > 0.25, 1, mag)
+    mag = torch.where(a >= 0.75, 2, mag)
+    mag = torch.where(a > 1.25, 3, mag)
+    mag = torch.where(a >= 1.75, 4, mag)
+    mag = torch.where(a > 2.5, 5, mag)
+    mag = torch.where(a >= 3.5, 6, mag)
+    mag = torch.where(a > 5.0, 7, mag)
+    return (mag | torch.where(v < 0, 8, 0)).to(torch.uint8)
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """NVFP4 encoding of one bf16 weight matrix [rows, K] (K a multiple of 16),
+    the input format of the NVFP4 entry point: a matrix scale
+    g = max|w| / (6 * 448) (fp32), per row and 16 consecutive K values a block
+    scale b = E4M3(max|w_block| / (6 g)) (round to nearest), and codes
+    E2M1(w / (b g)) (nearest, ties to even, saturating at +-6), two per byte
+    with the lower K index in the low nibble. Returns (codes uint8 [rows, K/2],
+    scales uint8 [K/16, rows], g fp32 scalar tensor). Input preparation only."""
+    rows, K = w.shape
+    assert K % 16 == 0
+    f = w.float()
+    amax = f.abs().max()
+    g = (amax / (6.0 * 448.0)).clamp_min(2.0 ** -126)
+    blk = f.reshape(rows, K // 16, 16)
+    bmax = blk.abs().amax(dim=-1)
+    b = (bmax / (6.0 * g)).clamp(max=448.0).to(torch.float8_e4m3fn)
+    bv = b.float()
+    q = blk / (bv * g).clamp_min(2.0 ** -126).unsqueeze(-1)
+    codes = _round_e2m1(q).reshape(rows, K)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8).contiguous()
+    scales = b.view(torch.uint8).transpose(0, 1).contiguous()
+    return packed, scales, g.to(torch.float32)
+
+
+def make_inputs_nvfp4(cfg: MoEConfig, seed: int = 0, device: str = "cpu") -> dict:
+    """The bf16 inputs of make_inputs (drawn on ``device``) with every expert
+    weight matrix encoded by quantize_nvfp4: <name>_q codes, <name>_s block
+    scales and <name>_g matrix scales (fp32, [E] for the expert stacks, [1]
+    for the shared expert) for w_gate_up, w_down, ws_gate_up and ws_down."""
+    inp = make_inputs(cfg, seed=seed, device=device)
+    for name in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
+        w = inp.pop(name)
+        mats = [w[e] for e in range(w.shape[0])] if w.dim() == 3 else [w]
+        enc = [quantize_nvfp4(m) for m in mats]
+        q = torch.stack([x[0] for x in enc])
+        s = torch.stack([x[1] for x in enc])
+        g = torch.stack([x[2] for x in enc]).reshape(-1)
+        if w.dim() == 2:
+            q, s = q[0], s[0]
+        inp[name + "_q"], inp[name + "_s"], inp[name + "_g"] = q, s, g
+    return inp

@@ -47,11 +47,16 @@ def _bind(lib):
     lib.oracle_route.restype = i
     lib.oracle_expert_counts.argtypes = [i, i, i, P, P]
     lib.oracle_expert_counts.restype = None
-    lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i] + [P] * 8 + [i] + [P] * 5 + [i]
+    d = ctypes.c_double
+    lib.oracle_moe_forward.argtypes = ([i, i, i, i, i, i, i] + [P] * 8 + [i] + [P] * 3 + [d, d] +
+                                       [P] * 4 + [i])
     lib.oracle_mxfp8_to_bf16.argtypes = [i, i, P, P, P]
     lib.oracle_mxfp8_to_bf16.restype = i
     lib.oracle_e4m3_table.argtypes = [P]
     lib.oracle_router_logits.argtypes = [i, i, i, P, P, P]
+    lib.oracle_nvfp4_to_bf16.argtypes = [i, i, P, P, P]
+    lib.oracle_nvfp4_to_bf16.restype = i
+    lib.oracle_e2m1_table.argtypes = [P]
     lib.oracle_router_logits.restype = None
     lib.oracle_moe_forward.restype = i
     return lib
@@ -111,8 +116,11 @@ def moe_forward(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=
     """Evaluate the layer in fp64 for ``tokens`` (default: all tokens).
 
     ``inputs`` holds hidden, logits, w_gate_up, w_down, ws_gate_up, ws_down,
-    w_g (torch tensors or numpy bf16-bit arrays). Returns a dict with
-    out [n,H] fp64, ids [n,k], weights [n,k] fp64 and gate [n] fp64.
+    w_g (torch tensors or numpy bf16-bit arrays), and optionally the matrix
+    scales w_gate_up_g / w_down_g [E] and ws_gate_up_g / ws_down_g (scalars)
+    that multiply each matrix's dot products (NVFP4 weights; 1 if absent).
+    Returns a dict with out [n,H] fp64, ids [n,k], weights [n,k] fp64 and
+    gate [n] fp64.
     """
     lib = _load(lib_path)
     hidden = _u16(inputs["hidden"])
@@ -138,6 +146,13 @@ def moe_forward(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=
     go = None if gate_override is None else np.ascontiguousarray(gate_override, dtype=np.float64)
     if go is not None:
         assert go.shape == (n,)
+    def scales(name, shape):
+        if name not in inputs:
+            return None
+        v = np.ascontiguousarray(np.asarray(_np(inputs[name]), dtype=np.float64).reshape(shape))
+        return v
+    s_gu, s_d = scales("w_gate_up_g", (E,)), scales("w_down_g", (E,))
+    ss_gu, ss_d = scales("ws_gate_up_g", (1,)), scales("ws_down_g", (1,))
     out = np.empty((n, H), dtype=np.float64)
     ids = np.empty((n, k), dtype=np.int32)
     w = np.empty((n, k), dtype=np.float64)
@@ -146,7 +161,10 @@ def moe_forward(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=
         return dict(out=out, ids=ids, weights=w, gate=gate)
     bad = lib.oracle_moe_forward(T, H, E, k, I, I_s, score_fn, _ptr(hidden), _ptr(logits),
                                  _ptr(wgu), _ptr(wd), _ptr(wsgu), _ptr(wsd), _ptr(wg), _ptr(tok),
-                                 n, _ptr(go), _ptr(out), _ptr(ids), _ptr(w), _ptr(gate),
+                                 n, _ptr(go), _ptr(s_gu), _ptr(s_d),
+                                 1.0 if ss_gu is None else float(ss_gu[0]),
+                                 1.0 if ss_d is None else float(ss_d[0]),
+                                 _ptr(out), _ptr(ids), _ptr(w), _ptr(gate),
                                  n_threads or default_threads())
     assert bad == 0, f"{bad} tokens: fp64 score order contradicts the logit order"
     return dict(out=out, ids=ids, weights=w, gate=gate)
@@ -195,6 +213,50 @@ def moe_forward_mxfp8(inputs: dict, k: int, score_fn: int, tokens=None, gate_ove
         if name + "_q" not in inputs:
             continue
         bits = mxfp8_to_bf16(_np(plain.pop(name + "_q")), _np(plain.pop(name + "_s")), lib_path)
+        plain[name] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    return moe_forward(plain, k, score_fn, tokens=tokens, gate_override=gate_override,
+                       lib_path=lib_path)
+
+
+def e2m1_table(lib_path: str | None = None) -> np.ndarray:
+    """Values of the 16 FP4 E2M1 codes."""
+    lib = _load(lib_path)
+    out = np.empty(16, dtype=np.float64)
+    lib.oracle_e2m1_table(_ptr(out))
+    return out
+
+
+def nvfp4_to_bf16(codes, scales, lib_path: str | None = None):
+    """Exact dequantisation of NVFP4 weights (without the fp32 matrix scale)
+    to bf16 bit patterns. codes: uint8 [..., rows, cols/2] (two E2M1 values
+    per byte, low nibble first); scales: uint8 [..., cols/16, rows] E4M3.
+    Returns uint16 [..., rows, cols]; raises on non-finite scales."""
+    lib = _load(lib_path)
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    sc = np.ascontiguousarray(np.asarray(scales, dtype=np.uint8))
+    rows, cols = c.shape[-2], 2 * c.shape[-1]
+    lead = int(np.prod(c.shape[:-2])) if c.ndim > 2 else 1
+    c2 = c.reshape(lead, rows, cols // 2)
+    s2 = sc.reshape(lead, cols // 16, rows)
+    out = np.empty((lead, rows, cols), dtype=np.uint16)
+    for e in range(lead):
+        bad = lib.oracle_nvfp4_to_bf16(rows, cols, _ptr(np.ascontiguousarray(c2[e])),
+                                       _ptr(np.ascontiguousarray(s2[e])), _ptr(out[e]))
+        if bad:
+            raise ValueError(f"{bad} NVFP4 values are not exact bf16 values")
+    return out.reshape(*c.shape[:-1], cols)
+
+
+def moe_forward_nvfp4(inputs: dict, k: int, score_fn: int, tokens=None, gate_override=None,
+                      lib_path: str | None = None):
+    """The layer with NVFP4 expert weights: each matrix's E2M1 x E4M3 values
+    are dequantised exactly to bf16 and its fp32 matrix scale <name>_g
+    multiplies the matrix's dot products. inputs holds <name>_q / <name>_s /
+    <name>_g for w_gate_up, w_down, ws_gate_up and ws_down."""
+    import torch
+    plain = dict(inputs)
+    for name in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
+        bits = nvfp4_to_bf16(_np(plain.pop(name + "_q")), _np(plain.pop(name + "_s")), lib_path)
         plain[name] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     return moe_forward(plain, k, score_fn, tokens=tokens, gate_override=gate_override,
                        lib_path=lib_path)

@@ -198,6 +198,53 @@ void oracle_e4m3_table(double* out) {
 }
 
 /*
+ * NVFP4 expert weights (the pages deploy NVFP4 expert banks: "qwen3_5_moe is
+ * TP=1-only ...", second comment; the format is NVIDIA's NVFP4): FP4 E2M1
+ * elements (sign, 2-bit exponent with bias 1, 1-bit mantissa; exponent 0
+ * holds 0 and 0.5), two per byte with the lower K index in the low nibble;
+ * one FP8 E4M3 scale per 16 consecutive K values of a row; one fp32 scale
+ * per weight matrix, applied by the layer to that matrix's products.
+ */
+static double e2m1_value(uint8_t nib) {
+    const int sign = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Value table of the 16 E2M1 codes (for the oracle's pins). */
+void oracle_e2m1_table(double* out) {
+    for (int b = 0; b < 16; ++b) out[b] = e2m1_value((uint8_t)b);
+}
+
+/*
+ * Dequantise an NVFP4 matrix of `rows` rows and `cols` K values (cols a
+ * multiple of 16) without its fp32 matrix scale: codes [rows, cols / 2]
+ * (value c of row r in byte c / 2, low nibble for even c), scales
+ * [cols / 16, rows] E4M3 (row r, block j at j * rows + r). Every E2M1 x E4M3
+ * product has at most 6 significant bits and lies within [2^-10, 2688], so it
+ * is exactly a bf16 value; out gets its bit pattern. Returns the number of
+ * elements that were not exact (NaN scales).
+ */
+int oracle_nvfp4_to_bf16(int rows, int cols, const uint8_t* codes, const uint8_t* scales,
+                         uint16_t* out) {
+    int bad = 0;
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            const uint8_t byte = codes[(size_t)r * (cols / 2) + c / 2];
+            const uint8_t nib = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            const double v = e2m1_value(nib) * e4m3_value(scales[(size_t)(c / 16) * rows + r]);
+            const int32_t bits = exact_bf16_bits(v);
+            if (bits < 0) {
+                ++bad;
+                out[(size_t)r * cols + c] = 0x7FC0u;
+            } else {
+                out[(size_t)r * cols + c] = (uint16_t)bits;
+            }
+        }
+    return bad;
+}
+
+/*
  * Router logits computed on the FFN side: l[t][e] = sum over h of
  * x[t][h] * W_router[e][h], with W_router [E, H] bf16 (one row per expert,
  * the layout of a linear layer's weight). The router runs in fp32 ("Add
@@ -221,14 +268,16 @@ void oracle_router_logits(int T, int H, int E, const uint16_t* hidden, const uin
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /*
- * One SwiGLU FFN applied to one token:
- *   g_i = W_gu[i, :] . x,  u_i = W_gu[I + i, :] . x   (i < I)
+ * One SwiGLU FFN applied to one token, with the weight matrices s_gu * W_gu
+ * and s_d * W_d (s = 1 for bf16 weights; the fp32 matrix scale of NVFP4
+ * weights otherwise, multiplied into each dot product of the matrix):
+ *   g_i = s_gu (W_gu[i, :] . x),  u_i = s_gu (W_gu[I + i, :] . x)   (i < I)
  *   a_i = silu(g_i) * u_i
- *   y_h = W_d[h, :] . a                                 (h < H)
+ *   y_h = s_d (W_d[h, :] . a)                                      (h < H)
  * w_gu [2I, H] and w_d [H, I] are bf16 bit patterns; x is fp64 [H].
  */
-static void swiglu_ffn(int H, int I, const uint16_t* w_gu, const uint16_t* w_d,
-                       const double* x, double* a_scratch, double* y) {
+static void swiglu_ffn(int H, int I, const uint16_t* w_gu, const uint16_t* w_d, double s_gu,
+                       double s_d, const double* x, double* a_scratch, double* y) {
     for (int i = 0; i < I; ++i) {
         const uint16_t* wg = w_gu + (size_t)i * H;
         const uint16_t* wu = w_gu + (size_t)(I + i) * H;
@@ -237,13 +286,13 @@ static void swiglu_ffn(int H, int I, const uint16_t* w_gu, const uint16_t* w_d,
             g += bf16_value(wg[h]) * x[h];
             u += bf16_value(wu[h]) * x[h];
         }
-        a_scratch[i] = silu(g) * u;
+        a_scratch[i] = silu(s_gu * g) * (s_gu * u);
     }
     for (int h = 0; h < H; ++h) {
         const uint16_t* wd = w_d + (size_t)h * I;
         double acc = 0.0;
         for (int i = 0; i < I; ++i) acc += bf16_value(wd[i]) * a_scratch[i];
-        y[h] = acc;
+        y[h] = s_d * acc;
     }
 }
 
@@ -260,6 +309,9 @@ static void swiglu_ffn(int H, int I, const uint16_t* w_gu, const uint16_t* w_d,
  *   tokens     [n_tok]     token indices to evaluate (NULL: all T, n_tok = T)
  *   gate_override [n_tok]  NULL, or a shared-gate value to use instead of
  *                          sigmoid(x . w_g) (a hook for the gate pins)
+ *   scale_gu, scale_d [E]  NULL (1), or the matrix scale of each expert's
+ *                          W_gate_up / W_down (NVFP4 weights)
+ *   scale_s_gu, scale_s_d  the shared expert's matrix scales (1 for bf16)
  *   out        [n_tok, H]  fp64
  *   ids_out    [n_tok, k]  selected experts (may be NULL)
  *   w_out      [n_tok, k]  renormalised weights (may be NULL)
@@ -271,8 +323,9 @@ int oracle_moe_forward(int T, int H, int E, int k, int I, int I_s, int score_fn,
                        const uint16_t* hidden, const float* logits, const uint16_t* w_gate_up,
                        const uint16_t* w_down, const uint16_t* ws_gate_up,
                        const uint16_t* ws_down, const uint16_t* w_g, const int64_t* tokens,
-                       int n_tok, const double* gate_override, double* out, int32_t* ids_out,
-                       double* w_out, double* gate_out, int n_threads) {
+                       int n_tok, const double* gate_override, const double* scale_gu,
+                       const double* scale_d, double scale_s_gu, double scale_s_d, double* out,
+                       int32_t* ids_out, double* w_out, double* gate_out, int n_threads) {
     if (tokens == NULL) n_tok = T;
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads) reduction(+ : bad)
@@ -292,8 +345,8 @@ int oracle_moe_forward(int T, int H, int E, int k, int I, int I_s, int score_fn,
         /* routed experts, in selection order */
         for (int j = 0; j < k; ++j) {
             int e = ids[j];
-            swiglu_ffn(H, I, w_gate_up + (size_t)e * 2 * I * H, w_down + (size_t)e * H * I, x, a,
-                       y);
+            swiglu_ffn(H, I, w_gate_up + (size_t)e * 2 * I * H, w_down + (size_t)e * H * I,
+                       scale_gu ? scale_gu[e] : 1.0, scale_d ? scale_d[e] : 1.0, x, a, y);
             for (int h = 0; h < H; ++h) o[h] += w[j] * y[h];
         }
         /* shared expert with its per-token sigmoid gate */
@@ -305,7 +358,7 @@ int oracle_moe_forward(int T, int H, int E, int k, int I, int I_s, int score_fn,
             for (int h = 0; h < H; ++h) s += bf16_value(w_g[h]) * x[h];
             gate = 1.0 / (1.0 + exp(-s));
         }
-        swiglu_ffn(H, I_s, ws_gate_up, ws_down, x, a, y);
+        swiglu_ffn(H, I_s, ws_gate_up, ws_down, scale_s_gu, scale_s_d, x, a, y);
         for (int h = 0; h < H; ++h) o[h] += gate * y[h];
 
         if (ids_out)

@@ -108,7 +108,8 @@ MUTANTS = {
     "scale_bias": [("return s == 255 ? NAN : ldexp(1.0, (int)s - 127);", "return s == 255 ? NAN : ldexp(1.0, (int)s - 128);")],
     "scale_layout_transposed": [("ue8m0_value(scales[(size_t)(c / 32) * rows + r]);",
                                  "ue8m0_value(scales[(size_t)r * (cols / 32) + c / 32]);")],
-    "sign_dropped": [("return sign ? -v : v;", "return v;")],
+    "sign_dropped": [("    else v = ldexp(1.0 + m / 8.0, e - 7);\n    return sign ? -v : v;",
+                      "    else v = ldexp(1.0 + m / 8.0, e - 7);\n    return v;")],
 }
 
 
