@@ -142,6 +142,8 @@ KERNEL_SOURCES = {
     "moe_gate_up": ("moe_gemm.cu", "gemm_common.cuh", "ptx.cuh", "moe_internal.cuh"),
     "moe_gate_up_mxfp8": ("moe_gemm_mx.cu", "mxfp8.cuh", "gemm_common.cuh", "ptx.cuh",
                           "moe_internal.cuh"),
+    "moe_gate_up_nvfp4": ("moe_gemm_mx.cu", "mxfp8.cuh", "gemm_common.cuh", "ptx.cuh",
+                          "moe_internal.cuh"),
 }
 
 
@@ -254,8 +256,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--weights", default="bf16", choices=["bf16", "mxfp8"],
-                    help="expert weight format: bf16, or MXFP8 codes + scales (moe_forward_mxfp8)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
+                    help="expert weight format: bf16, MXFP8 (moe_forward_mxfp8) or NVFP4 "
+                         "(moe_forward_nvfp4)")
     ap.add_argument("--router", action="store_true",
                     help="compute the router logits in the layer from W_router (moe_forward_router)")
     args = ap.parse_args()
@@ -281,7 +284,8 @@ def main():
     moe.load_library()
 
     mx = args.weights == "mxfp8"
-    if mx and args.router:
+    nv = args.weights == "nvfp4"
+    if (mx or nv) and args.router:
         raise SystemExit("--router runs with bf16 expert weights")
     if args.router:
         inp = wl.make_inputs_router(cfg, seed=0, device=str(dev))
@@ -289,6 +293,11 @@ def main():
                                    inp["ws_gate_up"], inp["ws_down"], inp["w_g"], cfg.k,
                                    cfg.score_fn)
         inp["logits"] = None
+    elif nv:
+        inp = wl.make_inputs_nvfp4(cfg, seed=0, device=str(dev))
+        tri = lambda n: (inp[n + "_q"], inp[n + "_s"], inp[n + "_g"])  # noqa: E731
+        layer = moe.MoELayerNVFP4(tri("w_gate_up"), tri("w_down"), tri("ws_gate_up"),
+                                  tri("ws_down"), inp["w_g"], cfg.k, cfg.score_fn)
     elif mx:
         inp = wl.make_inputs_mxfp8(cfg, seed=0, device=str(dev))
         pair = lambda n: (inp[n + "_q"], inp[n + "_s"])  # noqa: E731
@@ -310,11 +319,12 @@ def main():
     st = moe.device_status(layer.workspace(T), stream)
     if st != moe.MOE_OK:
         raise RuntimeError(moe.status_string(st))
-    work = algorithmic_work(cfg, counts.cpu().tolist(), wbytes=1.0 + 1.0 / 32 if mx else 2.0)
+    work = algorithmic_work(cfg, counts.cpu().tolist(),
+                            wbytes=1.0 + 1.0 / 32 if mx else (0.5 + 1.0 / 16 if nv else 2.0))
     if args.router:  # W_router read and x . W_router^T computed instead of logits read
         work["flops"] += 2.0 * T * cfg.E * cfg.H
         work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * T * cfg.E
-    gu_kernel = "moe_gate_up_mxfp8" if mx else "moe_gate_up"
+    gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
 
     K = args.steps
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -467,7 +477,10 @@ def main():
     line = dict(
         metric="MoE-layer tokens/s", value=value, unit="tokens/s", n_gpus=world, steps=K,
         warmup=args.warmup, ms_per_step=ms_step, higher_is_better=True, scaling="weak",
-        vs_baseline=None, dtype="bf16" if not mx else "bf16 (MXFP8 E4M3 weights, exact to bf16)",
+        vs_baseline=None,
+        dtype=("bf16 (MXFP8 E4M3 weights, exact to bf16)" if mx else
+               "bf16 (NVFP4 E2M1 weights with E4M3 block scales, exact to bf16; fp32 matrix scales)"
+               if nv else "bf16"),
         data="synthetic",
         config=dict(workload=workload_name(cfg), seed=0, weights=args.weights,
                     router="in the layer (moe_forward_router)" if args.router else "logits input",
@@ -485,13 +498,13 @@ def main():
         clocks=clocks, cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
         inp_cpu = {n: t.cpu() for n, t in inp.items() if t is not None}
-        if mx:
-            # the oracle's MXFP8 layer is its bf16 layer on the exactly dequantised
-            # weights: dequantise once, then time that layer
+        if mx or nv:
+            # the oracle's quantised layer is its bf16 layer on the exactly dequantised
+            # weights (NVFP4: plus the matrix scales): dequantise once, then time that layer
             import oracle
+            deq = oracle.nvfp4_to_bf16 if nv else oracle.mxfp8_to_bf16
             for n in ("w_gate_up", "w_down", "ws_gate_up", "ws_down"):
-                bits = oracle.mxfp8_to_bf16(oracle._np(inp_cpu.pop(n + "_q")),
-                                            oracle._np(inp_cpu.pop(n + "_s")))
+                bits = deq(oracle._np(inp_cpu.pop(n + "_q")), oracle._np(inp_cpu.pop(n + "_s")))
                 inp_cpu[n] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
         line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu, router=args.router)
     print(json.dumps(line), flush=True)

@@ -52,7 +52,7 @@ typedef enum {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
-    MOE_ERR_UNSUPPORTED = 2,   /* H, I or I_s not a multiple of 64 (128: MXFP8) */
+    MOE_ERR_UNSUPPORTED = 2,   /* H, I or I_s not a multiple of 64 (128: MXFP8, NVFP4) */
     MOE_ERR_WORKSPACE = 3,     /* workspace null or smaller than moe_workspace_size() */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
     MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up waiting on an internal pipeline
@@ -139,6 +139,48 @@ moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden, const float*
                              const void* ws_down_q, const void* ws_down_s, const void* w_g,
                              void* out, int32_t* topk_ids_out, float* topk_w_out,
                              int32_t* expert_counts_out, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream);
+
+/*
+ * Run the layer with NVFP4 expert weights: the same computation as
+ * moe_forward, with every weight matrix of the routed and the shared experts
+ * given in NVIDIA's NVFP4 format (the pages deploy NVFP4 expert banks:
+ * "qwen3_5_moe is TP=1-only ...", second comment, without fixing a layout):
+ *   a weight matrix [rows, K] is stored as
+ *     codes  [rows, K/2]   uint8  two FP4 E2M1 values per byte (sign, 2-bit
+ *                                 exponent with bias 1, 1-bit mantissa), the
+ *                                 lower K index in the low nibble
+ *     scales [K/16, rows]  uint8  FP8 E4M3 block scale of each 16 values
+ *     g                    fp32   one scale for the whole matrix
+ *   and element (r, c) is g * E2M1(value c of row r) * E4M3(scales[c/16][r]).
+ *   w_gate_up_q [E, 2I, H/2], w_gate_up_s [E, H/16, 2I], w_gate_up_g [E]
+ *   w_down_q    [E, H, I/2],  w_down_s    [E, I/16, H],  w_down_g    [E]
+ *   ws_gate_up_q [2I_s, H/2], ws_gate_up_s [H/16, 2I_s], ws_gate_up_g [1]
+ *   ws_down_q    [H, I_s/2],  ws_down_s    [I_s/16, H],  ws_down_g    [1]
+ * E2M1 x E4M3 is exactly a bf16 number, so the GEMMs run bf16 MMAs on exact
+ * values and multiply each matrix's fp32 accumulators by its g (the gate and
+ * up projections before SiLU, the down projection before the shared gate and
+ * the combine). The E4M3 NaN scale codes are reserved (results unspecified).
+ * Sizes: H, I and I_s multiples of 128 (else MOE_ERR_UNSUPPORTED); the g
+ * pointers 4-byte aligned, the codes and scales 16-byte aligned. Workspace,
+ * other arguments, returns and errors as moe_forward_mxfp8.
+ */
+moe_status moe_forward_nvfp4(const moe_dims* d, const void* hidden, const float* router_logits,
+                             const void* w_gate_up_q, const void* w_gate_up_s,
+                             const float* w_gate_up_g, const void* w_down_q, const void* w_down_s,
+                             const float* w_down_g, const void* ws_gate_up_q,
+                             const void* ws_gate_up_s, const float* ws_gate_up_g,
+                             const void* ws_down_q, const void* ws_down_s, const float* ws_down_g,
+                             const void* w_g, void* out, int32_t* topk_ids_out, float* topk_w_out,
+                             int32_t* expert_counts_out, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream);
+
+/* bf16 values E2M1 x E4M3 (without the matrix scale g) of one NVFP4 matrix
+ * (layout as in moe_forward_nvfp4): codes [rows, cols/2], scales [cols/16,
+ * rows] in, out [rows, cols] bf16 written, with the conversion the NVFP4
+ * GEMMs use (exact). cols must be a multiple of 32 (else MOE_ERR_INVALID_ARG);
+ * codes and out 16-byte aligned. Enqueued on cuda_stream. */
+moe_status moe_nvfp4_dequant(const void* codes, const void* scales, int rows, int cols, void* out,
                              void* cuda_stream);
 
 /* bf16 values of one MXFP8 matrix (layout as in moe_forward_mxfp8): codes

@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_status_string",
             "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count",
             "moe_selftest_wait_limit", "moe_forward_mxfp8", "moe_mxfp8_dequant",
-            "moe_forward_router", "moe_workspace_size_router", "moe_launch_count_router"]
+            "moe_forward_router", "moe_workspace_size_router", "moe_launch_count_router",
+            "moe_forward_nvfp4", "moe_nvfp4_dequant"]
 NUM_STAGES = 6
 STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
 
@@ -87,6 +88,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp8_dequant.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
     lib.moe_mxfp8_dequant.restype = ctypes.c_int
     lib.moe_forward_router.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 12 + [P, ctypes.c_size_t, P]
+    lib.moe_forward_nvfp4.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 19 + [P, ctypes.c_size_t, P]
+    lib.moe_forward_nvfp4.restype = ctypes.c_int
+    lib.moe_nvfp4_dequant.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
+    lib.moe_nvfp4_dequant.restype = ctypes.c_int
     lib.moe_forward_router.restype = ctypes.c_int
     lib.moe_workspace_size_router.argtypes = [ctypes.POINTER(MoEDims)]
     lib.moe_workspace_size_router.restype = ctypes.c_size_t
@@ -169,6 +174,34 @@ def forward_mxfp8_raw(dims: MoEDims, hidden, logits, w_gate_up_q, w_gate_up_s, w
         _ptr(ws_down_s), _ptr(w_g), _ptr(out), _ptr(topk_ids_out), _ptr(topk_w_out),
         _ptr(counts_out), _ptr(workspace),
         ctypes.c_size_t(0 if workspace is None else workspace.numel()), _stream_handle(stream)))
+
+
+def forward_nvfp4_raw(dims: MoEDims, hidden, logits, w_gate_up, w_down, ws_gate_up, ws_down, w_g,
+                      out, workspace, topk_ids_out=None, topk_w_out=None, counts_out=None,
+                      stream=None) -> int:
+    """Direct call of moe_forward_nvfp4; each weight is a (codes, scales, g) triple."""
+    lib = load_library()
+    return int(lib.moe_forward_nvfp4(
+        ctypes.byref(dims), _ptr(hidden), _ptr(logits), *[_ptr(t) for t in w_gate_up],
+        *[_ptr(t) for t in w_down], *[_ptr(t) for t in ws_gate_up], *[_ptr(t) for t in ws_down],
+        _ptr(w_g), _ptr(out), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(counts_out),
+        _ptr(workspace), ctypes.c_size_t(0 if workspace is None else workspace.numel()),
+        _stream_handle(stream)))
+
+
+def nvfp4_dequant(codes, scales, out=None, stream=None):
+    """bf16 values E2M1 x E4M3 of an NVFP4 matrix (moe_nvfp4_dequant): codes uint8
+    [rows, cols/2], scales uint8 [cols/16, rows] on the GPU; returns out [rows, cols]."""
+    import torch
+    rows, half = codes.shape
+    cols = 2 * half
+    if out is None:
+        out = torch.empty(rows, cols, dtype=torch.bfloat16, device=codes.device)
+    st = load_library().moe_nvfp4_dequant(_ptr(codes), _ptr(scales), int(rows), int(cols),
+                                          _ptr(out), _stream_handle(stream))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_nvfp4_dequant")
+    return out
 
 
 def mxfp8_dequant(codes, scales, out=None, stream=None):
@@ -309,6 +342,38 @@ class MoELayerMXFP8(MoELayer):
                                topk_w, counts, stream)
         if st != MOE_OK:
             raise MoEError(st, "moe_forward_mxfp8")
+        return out
+
+
+class MoELayerNVFP4(MoELayer):
+    """MoELayer with NVFP4 expert weights (moe_forward_nvfp4): each of w_gate_up,
+    w_down, ws_gate_up, ws_down is a triple (codes uint8 [..., rows, K/2],
+    scales uint8 [..., K/16, rows], g fp32 [E] or [1]); w_g stays bf16."""
+
+    def __init__(self, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int, score_fn: int):
+        import torch
+        self.w_gate_up, self.w_down = w_gate_up, w_down
+        self.ws_gate_up, self.ws_down, self.w_g = ws_gate_up, ws_down, w_g
+        self.E, two_i, half_h = w_gate_up[0].shape
+        self.H = 2 * half_h
+        self.I = two_i // 2
+        self.I_s = ws_gate_up[0].shape[0] // 2
+        self.k, self.score_fn = int(k), int(score_fn)
+        self.device = w_gate_up[0].device
+        self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    def forward(self, hidden, logits, out=None, topk_ids=None, topk_w=None, counts=None,
+                stream=None):
+        import torch
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        ws = self.workspace(T)
+        st = forward_nvfp4_raw(self.dims(T), hidden, logits, self.w_gate_up, self.w_down,
+                               self.ws_gate_up, self.ws_down, self.w_g, out, ws, topk_ids,
+                               topk_w, counts, stream)
+        if st != MOE_OK:
+            raise MoEError(st, "moe_forward_nvfp4")
         return out
 
 

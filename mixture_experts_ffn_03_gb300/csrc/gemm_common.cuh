@@ -239,6 +239,13 @@ __device__ __forceinline__ void drain_tma(Ctl* ctl, uint32_t armed, uint32_t par
         if (armed & (1u << s)) wait_bounded(bar_addr(&ctl->full_a[s]), (parity_bits >> s) & 1u);
 }
 
+// Scale of the tile's weight matrix: the fp32 matrix scale of NVFP4 weights
+// (per routed expert, or the shared expert's), 1 for bf16 and MXFP8 weights.
+__device__ __forceinline__ float matrix_scale(const GemmArgs& a, const Tile& ti) {
+    if (!a.msc) return 1.f;
+    return ti.shared ? a.msc_s[0] : a.msc[ti.e];
+}
+
 // Epilogue role of the down GEMMs with the weights on M (warps 4-11), with
 // the same chunking as the gate_up epilogue: warp we owns 32 output features
 // (TMEM lanes 32*(warp % 4)..) and every other 16-column chunk; full chunks
@@ -265,6 +272,7 @@ __device__ __forceinline__ void down_epilogue(uint8_t* smem, Ctl* ctl, uint32_t 
         const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
         const bool warp_valid = h0 < a.H;               // H is a multiple of 64
         const int row0 = ti.shared ? shared_row0 + ti.m0 : ti.p0;
+        const float msc = matrix_scale(a, ti);
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
         for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
             uint32_t v[kEpiRows], vl[kEpiRows];
@@ -276,7 +284,7 @@ __device__ __forceinline__ void down_epilogue(uint8_t* smem, Ctl* ctl, uint32_t 
             float val[kEpiRows];
 #pragma unroll
             for (int n = 0; n < kEpiRows; ++n) {
-                val[n] = __uint_as_float(v[n]) + __uint_as_float(vl[n]);
+                val[n] = msc * (__uint_as_float(v[n]) + __uint_as_float(vl[n]));
                 if (ti.shared && n < rows)
                     val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
             }

@@ -253,7 +253,8 @@ MOE_API const char* moe_status_string(moe_status s) {
         case MOE_OK: return "ok";
         case MOE_ERR_INVALID_ARG: return "invalid argument";
         case MOE_ERR_UNSUPPORTED:
-            return "unsupported size (H, I and I_s must be multiples of 64; of 128 for MXFP8 weights)";
+            return "unsupported size (H, I and I_s must be multiples of 64; of 128 for MXFP8 or "
+                   "NVFP4 weights)";
         case MOE_ERR_WORKSPACE: return "workspace missing or too small";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
@@ -265,24 +266,30 @@ MOE_API const char* moe_status_string(moe_status s) {
 namespace moe {
 namespace {
 
-// The experts' weights: bf16 matrices, or MXFP8 codes with their scales.
+// The experts' weights: bf16 matrices, or block-quantised codes with their
+// scales (mx: MXFP8, or NVFP4 when nv is also set).
 struct ExpertWeights {
     bool mx;
-    const void* gate_up;      // [E, 2I, H] bf16 or E4M3 codes
-    const void* down;         // [E, H, I]
+    bool nv;
+    const void* gate_up;      // [E, 2I, H] bf16, E4M3 codes, or [E, 2I, H/2] E2M1 pairs
+    const void* down;         // [E, H, I] (NVFP4: [E, H, I/2])
     const void* s_gate_up;    // shared expert [2I_s, H]
     const void* s_down;       // shared expert [H, I_s]
-    const uint8_t* gate_up_sc;    // MXFP8 scales [E, H/32, 2I]
-    const uint8_t* down_sc;       // [E, I/32, H]
-    const uint8_t* s_gate_up_sc;  // [H/32, 2I_s]
-    const uint8_t* s_down_sc;     // [I_s/32, H]
+    const uint8_t* gate_up_sc;    // block scales [E, H/B, 2I] (B = 32 MXFP8, 16 NVFP4)
+    const uint8_t* down_sc;       // [E, I/B, H]
+    const uint8_t* s_gate_up_sc;  // [H/B, 2I_s]
+    const uint8_t* s_down_sc;     // [I_s/B, H]
+    const float* g_gate_up;       // NVFP4 matrix scales [E]
+    const float* g_down;          // [E]
+    const float* g_s_gate_up;     // [1]
+    const float* g_s_down;        // [1]
 };
 
 bool dims_supported_mx(const moe_dims* d) {
     return d->H % 128 == 0 && d->I % 128 == 0 && d->I_s % 128 == 0;
 }
 
-// TMA maps of the MXFP8 GEMMs (layouts in moe_internal.cuh, MxMaps).
+// TMA maps of the block-quantised GEMMs (layouts in moe_internal.cuh, MxMaps).
 bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, char* ws, int bn_dn,
                   MxMaps* gu, MxMaps* dn) {
     const uint64_t T = d.T, H = d.H, E = d.E, I = d.I, Is = d.I_s, tk = T * d.k;
@@ -290,31 +297,41 @@ bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, ch
     const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B, NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
     bool ok = true;
-    {   // gate_up codes: {H, rows, 2 (gate, up)}, boxes 128 x 128 x 2
-        const uint32_t box[3] = {128, 128, 2};
-        const uint64_t dw[3] = {H, E * 2 * I - I, 2}, sw[2] = {H, I * H};
-        const uint64_t ds[3] = {H, Is, 2}, ss[2] = {H, Is * H};
-        ok = ok && make_map_nd(&gu->w, U8, W.gate_up, 3, dw, sw, box, SW) &&
-             make_map_nd(&gu->ws, U8, W.s_gate_up, 3, ds, ss, box, SW);
+    const uint64_t B = W.nv ? 16 : 32;  // K values per block scale
+    {   // gate_up codes: {row bytes, rows, 2 (gate, up)}: MXFP8 boxes 128 x 128 x 2
+        // (128 K), NVFP4 boxes 64 x 128 x 2 (128 K at half a byte, 64-byte swizzle)
+        const uint64_t rb = W.nv ? H / 2 : H;
+        const uint32_t box[3] = {W.nv ? 64u : 128u, 128, 2};
+        const CUtensorMapSwizzle sz = W.nv ? CU_TENSOR_MAP_SWIZZLE_64B : SW;
+        const uint64_t dw[3] = {rb, E * 2 * I - I, 2}, sw[2] = {rb, I * rb};
+        const uint64_t ds[3] = {rb, Is, 2}, ss[2] = {rb, Is * rb};
+        ok = ok && make_map_nd(&gu->w, U8, W.gate_up, 3, dw, sw, box, sz) &&
+             make_map_nd(&gu->ws, U8, W.s_gate_up, 3, ds, ss, box, sz);
     }
-    {   // gate_up scales: {rows of a plane, 2 planes, K blocks}, boxes 128 x 2 x 4
-        const uint32_t box[3] = {128, 2, 4};
-        const uint64_t dw[3] = {I, 2, E * (H / 32)}, sw[2] = {I, 2 * I};
-        const uint64_t ds[3] = {Is, 2, H / 32}, ss[2] = {Is, 2 * Is};
+    {   // gate_up scales: {rows of a plane, 2 planes, K blocks}, boxes 128 x 2 x (128 / B)
+        const uint32_t box[3] = {128, 2, static_cast<uint32_t>(128 / B)};
+        const uint64_t dw[3] = {I, 2, E * (H / B)}, sw[2] = {I, 2 * I};
+        const uint64_t ds[3] = {Is, 2, H / B}, ss[2] = {Is, 2 * Is};
         ok = ok && make_map_nd(&gu->sc, U8, W.gate_up_sc, 3, dw, sw, box, NOSW) &&
              make_map_nd(&gu->scs, U8, W.s_gate_up_sc, 3, ds, ss, box, NOSW);
     }
-    {   // down codes: {128, K / 128, rows}, boxes 128 x 2 x 128
+    if (W.nv) {  // down codes: {I/2 bytes, rows}, boxes 128 x 128 (256 K values)
+        const uint32_t box[2] = {128, 128};
+        const uint64_t dw[2] = {I / 2, E * H}, sw[1] = {I / 2};
+        const uint64_t ds[2] = {Is / 2, H}, ss[1] = {Is / 2};
+        ok = ok && make_map_nd(&dn->w, U8, W.down, 2, dw, sw, box, SW) &&
+             make_map_nd(&dn->ws, U8, W.s_down, 2, ds, ss, box, SW);
+    } else {  // down codes: {128, K / 128, rows}, boxes 128 x 2 x 128
         const uint32_t box[3] = {128, 2, 128};
         const uint64_t dw[3] = {128, I / 128, E * H}, sw[2] = {128, I};
         const uint64_t ds[3] = {128, Is / 128, H}, ss[2] = {128, Is};
         ok = ok && make_map_nd(&dn->w, U8, W.down, 3, dw, sw, box, SW) &&
              make_map_nd(&dn->ws, U8, W.s_down, 3, ds, ss, box, SW);
     }
-    {   // down scales: {H, K blocks}, boxes 128 x 8
-        const uint32_t box[2] = {128, 8};
-        const uint64_t dw[2] = {H, E * (I / 32)}, sw[1] = {H};
-        const uint64_t ds[2] = {H, Is / 32}, ss[1] = {H};
+    {   // down scales: {H, K blocks}, boxes 128 x (256 / B)
+        const uint32_t box[2] = {128, static_cast<uint32_t>(256 / B)};
+        const uint64_t dw[2] = {H, E * (I / B)}, sw[1] = {H};
+        const uint64_t ds[2] = {H, Is / B}, ss[1] = {H};
         ok = ok && make_map_nd(&dn->sc, U8, W.down_sc, 2, dw, sw, box, NOSW) &&
              make_map_nd(&dn->scs, U8, W.s_down_sc, 2, ds, ss, box, NOSW);
     }
@@ -353,6 +370,11 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         const void* scales[] = {W.gate_up_sc, W.down_sc, W.s_gate_up_sc, W.s_down_sc};
         for (const void* p : scales)
             if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    }
+    if (W.nv) {
+        const void* gs[] = {W.g_gate_up, W.g_down, W.g_s_gate_up, W.g_s_down};
+        for (const void* p : gs)
+            if (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
     }
     const void* optional[] = {topk_ids_out, topk_w_out, expert_counts_out};
     for (const void* p : optional)
@@ -442,6 +464,12 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     GemmArgs gd = ga;
     ga.rowtiles = rt_gu;
     gd.rowtiles = rt_dn;
+    if (W.nv) {
+        ga.msc = W.g_gate_up;
+        ga.msc_s = W.g_s_gate_up;
+        gd.msc = W.g_down;
+        gd.msc_s = W.g_s_down;
+    }
     ga.sched = meta + META_SCHED_GU;
     gd.sched = meta + META_SCHED_DN;
 
@@ -498,11 +526,11 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
             return MOE_ERR_CUDA;
     }
     mark_stage(3, st);
-    const cudaError_t e_gu = W.mx ? launch_gate_up_mx(bn_gu, mgu, ga, tiles_gu, num_sms, st)
+    const cudaError_t e_gu = W.mx ? launch_gate_up_mx(bn_gu, W.nv, mgu, ga, tiles_gu, num_sms, st)
                                   : launch_gate_up(bn_gu, gu, ga, tiles_gu, num_sms, st);
     if (e_gu != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(4, st);
-    const cudaError_t e_dn = W.mx ? launch_down_mx(bn_dn, mdn, gd, tiles_dn, num_sms, st)
+    const cudaError_t e_dn = W.mx ? launch_down_mx(bn_dn, W.nv, mdn, gd, tiles_dn, num_sms, st)
                                   : launch_down(bn_dn, dn, gd, tiles_dn, num_sms, st);
     if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(5, st);
@@ -581,6 +609,46 @@ MOE_API moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden,
     W.s_down_sc = static_cast<const uint8_t*>(ws_down_s);
     return forward_impl(d, hidden, router_logits, nullptr, nullptr, W, w_g, out, topk_ids_out,
                         topk_w_out, expert_counts_out, workspace, workspace_bytes, cuda_stream);
+}
+
+MOE_API moe_status moe_forward_nvfp4(
+    const moe_dims* d, const void* hidden, const float* router_logits, const void* w_gate_up_q,
+    const void* w_gate_up_s, const float* w_gate_up_g, const void* w_down_q, const void* w_down_s,
+    const float* w_down_g, const void* ws_gate_up_q, const void* ws_gate_up_s,
+    const float* ws_gate_up_g, const void* ws_down_q, const void* ws_down_s, const float* ws_down_g,
+    const void* w_g, void* out, int32_t* topk_ids_out, float* topk_w_out,
+    int32_t* expert_counts_out, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    ExpertWeights W{};
+    W.mx = true;
+    W.nv = true;
+    W.gate_up = w_gate_up_q;
+    W.down = w_down_q;
+    W.s_gate_up = ws_gate_up_q;
+    W.s_down = ws_down_q;
+    W.gate_up_sc = static_cast<const uint8_t*>(w_gate_up_s);
+    W.down_sc = static_cast<const uint8_t*>(w_down_s);
+    W.s_gate_up_sc = static_cast<const uint8_t*>(ws_gate_up_s);
+    W.s_down_sc = static_cast<const uint8_t*>(ws_down_s);
+    W.g_gate_up = w_gate_up_g;
+    W.g_down = w_down_g;
+    W.g_s_gate_up = ws_gate_up_g;
+    W.g_s_down = ws_down_g;
+    return forward_impl(d, hidden, router_logits, nullptr, nullptr, W, w_g, out, topk_ids_out,
+                        topk_w_out, expert_counts_out, workspace, workspace_bytes, cuda_stream);
+}
+
+MOE_API moe_status moe_nvfp4_dequant(const void* codes, const void* scales, int rows, int cols,
+                                     void* out, void* cuda_stream) {
+    if (rows < 0 || cols < 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    if (!codes || !scales || !out || !aligned16(codes) || !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    if (launch_nvfp4_dequant(static_cast<const uint8_t*>(codes),
+                             static_cast<const uint8_t*>(scales), rows, cols,
+                             static_cast<__nv_bfloat16*>(out),
+                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 MOE_API moe_status moe_mxfp8_dequant(const void* codes, const void* scales, int rows, int cols,

@@ -1,15 +1,19 @@
-// Grouped expert GEMMs with MXFP8 expert weights (OCP Microscaling formats:
-// E4M3 values, one UE8M0 power-of-two scale per 32 consecutive K values of a
-// weight row) and bf16 activations. The pages deploy the experts as block-FP8
-// banks ("qwen3_5_moe is TP=1-only ...", first comment) and as NVFP4 (same
-// page, second comment); power-of-two block scales keep every weight an
-// exact bf16 number, so the products and the fp32 accumulation are the bf16
-// path's.
+// Grouped expert GEMMs with block-quantised expert weights and bf16
+// activations. The pages deploy the experts as block-FP8 banks ("qwen3_5_moe
+// is TP=1-only ...", first comment) and as NVFP4 (same page, second comment):
+//   MXFP8 (OCP Microscaling formats): E4M3 values, one UE8M0 power-of-two
+//     scale per 32 consecutive K values of a weight row;
+//   NVFP4: E2M1 values (two per byte), one E4M3 scale per 16 consecutive K
+//     values, one fp32 scale per weight matrix (applied to the accumulators
+//     in the epilogues).
+// Either way every block-scaled weight is an exact bf16 number, so the
+// products and the fp32 accumulation are the bf16 path's.
 //
 // The layer's arithmetic is that of moe_gemm.cu (weights on the MMA's M
 // side, tokens on N, h as a bf16 hi/lo pair, fp32 y), with the weights
-// arriving as one byte per value:
-//   TMA -> shared memory: E4M3 codes (128-byte swizzle) and their scales;
+// arriving as one byte (MXFP8) or half a byte (NVFP4) per value:
+//   TMA -> shared memory: codes (128-byte swizzle; 64-byte for the NVFP4
+//     gate_up rows of 128 values) and their block scales;
 //   converter warps: codes -> bf16 (exact), written into TMEM with
 //     tcgen05.st, where the MMA reads its A operand (M = 128 weight rows on
 //     the 128 lanes, K packed two values per column);
@@ -33,19 +37,25 @@ namespace {
 constexpr int kCvtWarps = 8;                                  // two per TMEM lane quadrant
 constexpr int kFirstCvtWarp = 4 + kEpiWarps;                  // warp 12
 constexpr int kMxThreads = (kFirstCvtWarp + kCvtWarps) * 32;  // 640
-constexpr int kCodeRow = 128;                                 // bytes (K values) per code row
 
-template <int BN, bool GU>
+// NV: NVFP4 weights (else MXFP8).
+template <int BN, bool GU, bool NV>
 struct MxCfg {
     // K values per pipeline stage: gate_up 128 (gate and up rows, 32 KB of
     // codes), down 256 (32 KB of codes); each stage is one TMA request of
     // codes, one of scales and (down) one of h.
     static constexpr int KS = GU ? 128 : 256;
-    static constexpr int CODE_BYTES = 2 * kGemmBM * kCodeRow;
+    // Code rows (bytes) per stage: MXFP8 gate and up rows of 128 B (128 K), or
+    // two 128-B halves per weight row (down); NVFP4 gate and up rows of 64 B
+    // (128 K), or one 128-B row per weight row (down, 256 K).
+    static constexpr int CODE_ROW = (NV && GU) ? 64 : 128;
+    static constexpr int CODE_BYTES = NV ? 2 * kGemmBM * 64 : 2 * kGemmBM * 128;
+    static constexpr int SCALE_BLOCK = NV ? 16 : 32;  // K values per block scale
     // Token operand per stage: gate_up two 64-column sub-tiles of BN hidden
     // rows; down four 64-column panels of BN h_hi then BN h_lo rows.
     static constexpr int TOK_BYTES = GU ? 2 * BN * 128 : 4 * 2 * BN * 128;
-    static constexpr int SCALE_BYTES = 1024;  // gate_up [4 blocks][2 planes][128]; down [8][128]
+    // gate_up [KS/SCALE_BLOCK blocks][2 planes][128 rows]; down [KS/SCALE_BLOCK][128]
+    static constexpr int SCALE_BYTES = (GU ? 2 : 1) * (KS / SCALE_BLOCK) * kGemmBM;
     static constexpr int TOK_OFF = CODE_BYTES;
     static constexpr int SC_OFF = CODE_BYTES + TOK_BYTES;
     static constexpr int STAGE_BYTES = CODE_BYTES + TOK_BYTES + SCALE_BYTES;
@@ -78,7 +88,8 @@ struct MxCfg {
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     static_assert(STAGE_BYTES % 1024 == 0 && TOK_OFF % 1024 == 0 && (BN * 128) % 1024 == 0,
                   "swizzled tiles start on 1024-byte boundaries");
-    static_assert(BN == 16 || BN == 32 || BN == 64, "MXFP8 tile widths");
+    static_assert(BN == 16 || BN == 32 || BN == 64, "quantised-weight tile widths");
+    static_assert(SCALE_BYTES % 1024 == 0, "stage parts stay 1024-byte aligned");
 };
 
 // One converter thread's share of a stage: the 128 K values (8 chunks of 16
@@ -89,7 +100,7 @@ struct MxCfg {
 // before the first conversion.
 __device__ __forceinline__ void convert_row(uint32_t codes, int crow, uint32_t sc, int sc_stride,
                                             uint32_t ta) {
-    const uint32_t row = codes + static_cast<uint32_t>(crow) * kCodeRow;
+    const uint32_t row = codes + static_cast<uint32_t>(crow) * 128u;
     const uint32_t swz = static_cast<uint32_t>(crow & 7);
     uint4 v[8];
 #pragma unroll
@@ -112,10 +123,33 @@ __device__ __forceinline__ void convert_row(uint32_t codes, int crow, uint32_t s
     }
 }
 
+// NVFP4: one converter thread's share of a stage, the 128 K values (4 chunks
+// of 32 codes starting at chunk c_first of the code row at shared address
+// `row`, chunk c at position (c ^ swz)) of one weight row, scaled by the 8
+// E4M3 scale bytes at sc, sc + sc_stride, ... (one per 16 values), written
+// to TMEM columns ta .. ta + 63. All loads are issued before the first
+// conversion.
+__device__ __forceinline__ void convert_row_nv(uint32_t row, uint32_t swz, int c_first,
+                                               uint32_t sc, int sc_stride, uint32_t ta) {
+    uint4 v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        v[c] = ptx::ld_shared_v4u(row + ((static_cast<uint32_t>(c_first + c) ^ swz) << 4));
+    uint32_t s[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = ptx::ld_shared_u8(sc + j * sc_stride);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t out[16];
+        nv_dequant32(v[c], e4m3_to_bf16x2(s[2 * c]), e4m3_to_bf16x2(s[2 * c + 1]), out);
+        ptx::tmem_st_32x32b_x16(ta + 16 * c, out);
+    }
+}
+
 // Converter role, shared by both GEMMs. Per stage: wait for the codes and a
 // free TMEM weight stage, convert, make the TMEM writes visible to the MMA
 // issuer and release the stage to it.
-template <class C, bool GU>
+template <class C, bool GU, bool NV>
 __device__ __forceinline__ void converter_role(uint8_t* smem, Ctl* ctl, uint32_t tmem_base,
                                                int warp, int lane, const GemmArgs& a,
                                                volatile int* abort_flag, unsigned* err,
@@ -142,7 +176,19 @@ __device__ __forceinline__ void converter_role(uint8_t* smem, Ctl* ctl, uint32_t
             uint8_t* st = smem + s * C::STAGE_BYTES;
             const uint32_t codes = ptx::smem_u32(st);
             const uint32_t ta = lane_base + C::A_BASE + t * C::A_COLS + part * 64;
-            if constexpr (GU) {
+            if constexpr (NV && GU) {
+                // 64-byte rows [0, 128) gate, [128, 256) up (64-byte swizzle: chunk c of
+                // row p at c ^ ((p >> 1) & 3)); scales [block][plane][row]
+                const int p = part * kGemmBM + r;
+                convert_row_nv(codes + static_cast<uint32_t>(p) * 64u,
+                               static_cast<uint32_t>((p >> 1) & 3), 0,
+                               codes + C::SC_OFF + part * 128 + r, 256, ta);
+            } else if constexpr (NV) {
+                // 128-byte row r holds the stage's 256 K values; this part's chunks are
+                // 4 part .. 4 part + 3; scales [block][row]
+                convert_row_nv(codes + static_cast<uint32_t>(r) * 128u, static_cast<uint32_t>(r & 7),
+                               4 * part, codes + C::SC_OFF + (part * 8) * 128 + r, 128, ta);
+            } else if constexpr (GU) {
                 // rows [0, 128) gate, [128, 256) up; scales [block][plane][row]
                 convert_row(codes, part * kGemmBM + r, codes + C::SC_OFF + part * 128 + r, 256, ta);
             } else {
@@ -167,10 +213,10 @@ __device__ __forceinline__ void converter_role(uint8_t* smem, Ctl* ctl, uint32_t
 }
 
 // ================================================================ gate_up
-template <int BN>
+template <int BN, bool NV>
 __global__ void __launch_bounds__(kMxThreads, 1)
 gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
-    using C = MxCfg<BN, true>;
+    using C = MxCfg<BN, true, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -212,7 +258,7 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
                 const CUtensorMap* tsc = ti.shared ? &maps.scs : &maps.sc;
                 const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
-                const int blk0 = ti.shared ? 0 : ti.e * (a.H / 32);
+                const int blk0 = ti.shared ? 0 : ti.e * (a.H / C::SCALE_BLOCK);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                         ok = false;
@@ -221,9 +267,10 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
                     uint8_t* st = smem + s * C::STAGE_BYTES;
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
                     ptx::mbar_arrive_expect_tx(fb, C::CODE_BYTES + C::SCALE_BYTES);
-                    ptx::tma_load_3d(ptx::smem_u32(st), tw, fb, ks * C::KS, row_g, 0, pol);
+                    // x in bytes: 128 K values are 128 (MXFP8) or 64 (NVFP4) bytes
+                    ptx::tma_load_3d(ptx::smem_u32(st), tw, fb, ks * C::CODE_ROW, row_g, 0, pol);
                     ptx::tma_load_3d(ptx::smem_u32(st + C::SC_OFF), tsc, fb, ti.f * kGemmBM, 0,
-                                     blk0 + ks * (C::KS / 32), pol);
+                                     blk0 + ks * (C::KS / C::SCALE_BLOCK), pol);
                     armed |= 1u << s;
                     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) {
@@ -364,6 +411,7 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
             __nv_bfloat16* panel = (ti.shared ? a.hs_hi : a.h_hi) +
                                    static_cast<size_t>(i >> 6) * 2 * P * 64 + (i & 63);
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
+            const float msc = matrix_scale(a, ti);  // NVFP4 matrix scale (1 for MXFP8)
             for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
                 uint32_t g[kEpiRows], u[kEpiRows];
                 ptx::tmem_ld_32x32b_x16(tb + c0, g);
@@ -373,8 +421,8 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
 #pragma unroll
                 for (int n = 0; n < kEpiRows; ++n) {
                     if (n < rows) {
-                        const float gv = __uint_as_float(g[n]);
-                        const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
+                        const float gv = msc * __uint_as_float(g[n]);
+                        const float h = __fdividef(gv, 1.f + __expf(-gv)) * (msc * __uint_as_float(u[n]));
                         const __nv_bfloat16 hi = __float2bfloat16_rn(h);
                         const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * 64;
                         panel[o] = hi;
@@ -391,16 +439,16 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
             }
         }
     } else {  // --------------------------------------------- converters (warps 12-19)
-        converter_role<C, true>(smem, ctl, tmem_base, warp, lane, a, abort_flag, err, code);
+        converter_role<C, true, NV>(smem, ctl, tmem_base, warp, lane, a, abort_flag, err, code);
     }
     gemm_teardown<C>(tmem_base, warp);
 }
 
 // =================================================================== down
-template <int BN>
+template <int BN, bool NV>
 __global__ void __launch_bounds__(kMxThreads, 1)
 down_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
-    using C = MxCfg<BN, false>;
+    using C = MxCfg<BN, false, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -447,7 +495,7 @@ down_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
                 const CUtensorMap* tsc = ti.shared ? &maps.scs : &maps.sc;
                 const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
                 const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * kGemmBM;
-                const int blk0 = ti.shared ? 0 : ti.e * (a.I / 32);
+                const int blk0 = ti.shared ? 0 : ti.e * (a.I / C::SCALE_BLOCK);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                         ok = false;
@@ -457,9 +505,12 @@ down_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
                     ptx::mbar_arrive_expect_tx(fb, C::CODE_BYTES + C::TOK_BYTES + C::SCALE_BYTES);
                     // 128 rows x 256 K values (K past the end reads as zero codes)
-                    ptx::tma_load_3d(ptx::smem_u32(st), tw, fb, 0, 2 * ks, row_w, pol_w);
+                    if constexpr (NV)
+                        ptx::tma_load_2d(ptx::smem_u32(st), tw, fb, ks * 128, row_w, pol_w);
+                    else
+                        ptx::tma_load_3d(ptx::smem_u32(st), tw, fb, 0, 2 * ks, row_w, pol_w);
                     ptx::tma_load_2d(ptx::smem_u32(st + C::SC_OFF), tsc, fb, ti.f * kGemmBM,
-                                     blk0 + ks * (C::KS / 32), pol_w);
+                                     blk0 + ks * (C::KS / C::SCALE_BLOCK), pol_w);
                     // four 64-column panels of the tile's h_hi and h_lo rows
                     ptx::tma_load_4d(ptx::smem_u32(st + C::TOK_OFF), th, fb, 0, ti.p0, 0, 4 * ks,
                                      pol_h);
@@ -539,20 +590,20 @@ down_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
         down_epilogue<C, BN>(smem, ctl, tmem_base, warp, lane, &maps.st[0], a, abort_flag, err,
                              code);
     } else {  // --------------------------------------------- converters (warps 12-19)
-        converter_role<C, false>(smem, ctl, tmem_base, warp, lane, a, abort_flag, err, code);
+        converter_role<C, false, NV>(smem, ctl, tmem_base, warp, lane, a, abort_flag, err, code);
     }
     gemm_teardown<C>(tmem_base, warp);
 }
 
-template <int BN, bool GU>
+template <int BN, bool GU, bool NV>
 cudaError_t launch_mx_bn(const MxMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
                          cudaStream_t st) {
-    using C = MxCfg<BN, GU>;
+    using C = MxCfg<BN, GU, NV>;
     void (*kern)(MxMaps, GemmArgs);
     if constexpr (GU)
-        kern = gate_up_mx_kernel<BN>;
+        kern = gate_up_mx_kernel<BN, NV>;
     else
-        kern = down_mx_kernel<BN>;
+        kern = down_mx_kernel<BN, NV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
@@ -560,13 +611,13 @@ cudaError_t launch_mx_bn(const MxMaps& maps, const GemmArgs& a, int max_tiles, i
     return launch_kernel(kern, dim3(grid), dim3(kMxThreads), C::SMEM, st, true, maps, a);
 }
 
-template <bool GU>
+template <bool GU, bool NV>
 cudaError_t dispatch_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
                         cudaStream_t st) {
     switch (bn) {
-        case 16: return launch_mx_bn<16, GU>(maps, a, max_tiles, num_sms, st);
-        case 32: return launch_mx_bn<32, GU>(maps, a, max_tiles, num_sms, st);
-        case 64: return launch_mx_bn<64, GU>(maps, a, max_tiles, num_sms, st);
+        case 16: return launch_mx_bn<16, GU, NV>(maps, a, max_tiles, num_sms, st);
+        case 32: return launch_mx_bn<32, GU, NV>(maps, a, max_tiles, num_sms, st);
+        case 64: return launch_mx_bn<64, GU, NV>(maps, a, max_tiles, num_sms, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -589,18 +640,40 @@ __global__ void mxfp8_dequant_kernel(const uint8_t* __restrict__ codes,
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// NVFP4: one thread per 32 values (16 code bytes) of a row, the converter
+// warps' conversion, written out as bf16 (without the matrix scale).
+__global__ void nvfp4_dequant_kernel(const uint8_t* __restrict__ codes,
+                                     const uint8_t* __restrict__ scales, int rows, int cols,
+                                     __nv_bfloat16* __restrict__ out) {
+    const int chunks = cols / 32;
+    const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<size_t>(rows) * chunks) return;
+    const int r = static_cast<int>(idx / chunks), c = static_cast<int>(idx % chunks);
+    const uint4 v =
+        *reinterpret_cast<const uint4*>(codes + static_cast<size_t>(r) * (cols / 2) + c * 16);
+    const uint32_t s0 = scales[static_cast<size_t>(2 * c) * rows + r];
+    const uint32_t s1 = scales[static_cast<size_t>(2 * c + 1) * rows + r];
+    uint32_t o[16];
+    nv_dequant32(v, e4m3_to_bf16x2(s0), e4m3_to_bf16x2(s1), o);
+    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(r) * cols + c * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
 }  // namespace
 
 bool gemm_mx_bn_supported(int bn) { return bn == 16 || bn == 32 || bn == 64; }
 
-cudaError_t launch_gate_up_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
-                              int num_sms, cudaStream_t st) {
-    return dispatch_mx<true>(bn, maps, a, max_tiles, num_sms, st);
+cudaError_t launch_gate_up_mx(int bn, bool nvfp4, const MxMaps& maps, const GemmArgs& a,
+                              int max_tiles, int num_sms, cudaStream_t st) {
+    return nvfp4 ? dispatch_mx<true, true>(bn, maps, a, max_tiles, num_sms, st)
+                 : dispatch_mx<true, false>(bn, maps, a, max_tiles, num_sms, st);
 }
 
-cudaError_t launch_down_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
-                           int num_sms, cudaStream_t st) {
-    return dispatch_mx<false>(bn, maps, a, max_tiles, num_sms, st);
+cudaError_t launch_down_mx(int bn, bool nvfp4, const MxMaps& maps, const GemmArgs& a,
+                           int max_tiles, int num_sms, cudaStream_t st) {
+    return nvfp4 ? dispatch_mx<false, true>(bn, maps, a, max_tiles, num_sms, st)
+                 : dispatch_mx<false, false>(bn, maps, a, max_tiles, num_sms, st);
 }
 
 cudaError_t launch_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int rows, int cols,
@@ -615,4 +688,15 @@ cudaError_t launch_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, in
     return cudaGetLastError();
 }
 
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int rows, int cols,
+                                 __nv_bfloat16* out, cudaStream_t st) {
+    const size_t n = static_cast<size_t>(rows) * (cols / 32);
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const size_t blocks = (n + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFu) return cudaErrorInvalidValue;
+    nvfp4_dequant_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(codes, scales, rows,
+                                                                            cols, out);
+    return cudaGetLastError();
+}
 }  // namespace moe

@@ -105,6 +105,10 @@ struct GemmArgs {
     __nv_bfloat16* hs_lo;
     float* y;
     unsigned* err;
+    // NVFP4 weights: fp32 matrix scales of this GEMM's routed experts [E] and
+    // of the shared expert [1]; null for bf16 and MXFP8 weights.
+    const float* msc;
+    const float* msc_s;
 };
 
 struct GemmMaps {
@@ -127,8 +131,13 @@ struct GemmMaps {
     CUtensorMap st[4];
 };
 
-// TMA maps of the GEMMs with MXFP8 expert weights (moe_gemm_mx.cu). Codes
-// are bytes read with the 128-byte swizzle, scales bytes without swizzle.
+// TMA maps of the GEMMs with block-quantised expert weights (moe_gemm_mx.cu),
+// listed for MXFP8; NVFP4 differs in the code and scale maps only: gate_up
+// codes {H/2 bytes, rows, 2} in boxes 64 x 128 x 2 with the 64-byte swizzle,
+// scales (E4M3, one per 16 values) {I, 2, E*H/16} in boxes 128 x 2 x 8; down
+// codes {I/2 bytes, E*H rows} in boxes 128 x 128, scales {H, E*I/16} in boxes
+// 128 x 16. Codes are bytes read with the 128-byte swizzle, scales bytes
+// without swizzle.
 // gate_up: w / ws = codes of W_gate_up as {H, E*2I - I rows, 2} (plane
 //   stride I rows: gate, up) and of Ws_gate_up as {H, I_s, 2}, boxes
 //   128 x 128 x 2; sc / scs = their scales [E, H/32, 2I] as {I, 2, E*H/32}
@@ -163,13 +172,17 @@ cudaError_t launch_wait_limit_selftest(unsigned* err, cudaStream_t st);
 cudaError_t launch_down(int bn, const GemmMaps& maps, const GemmArgs& a, int max_tiles,
                         int num_sms, cudaStream_t st);
 
-// MXFP8 GEMMs (moe_gemm_mx.cu): tile widths 16, 32 and 64; H, I and I_s
-// multiples of 128.
+// GEMMs with block-quantised weights (moe_gemm_mx.cu): MXFP8, or NVFP4 with
+// `nvfp4`; tile widths 16, 32 and 64; H, I and I_s multiples of 128.
 bool gemm_mx_bn_supported(int bn);
-cudaError_t launch_gate_up_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
-                              int num_sms, cudaStream_t st);
-cudaError_t launch_down_mx(int bn, const MxMaps& maps, const GemmArgs& a, int max_tiles,
-                           int num_sms, cudaStream_t st);
+cudaError_t launch_gate_up_mx(int bn, bool nvfp4, const MxMaps& maps, const GemmArgs& a,
+                              int max_tiles, int num_sms, cudaStream_t st);
+cudaError_t launch_down_mx(int bn, bool nvfp4, const MxMaps& maps, const GemmArgs& a,
+                           int max_tiles, int num_sms, cudaStream_t st);
+// bf16 values (without the matrix scale) of an NVFP4 matrix [rows, cols]:
+// codes [rows, cols/2], scales [cols/16, rows].
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int rows, int cols,
+                                 __nv_bfloat16* out, cudaStream_t st);
 // Router GEMM (moe_router.cu): logits [T, E] fp32 = hidden [T, H] . W_router [E, H]^T,
 // as a split-K GEMM (tiles of 128 experts x bn tokens, `splits` K ranges) that
 // writes the partial sums [splits, T, E]; the routing kernels add them in a

@@ -139,3 +139,23 @@ def test_host_validation_router(lib):
     assert call(moe.make_dims(16, 96, 16, 4, 64, 64, 0)) == 2                 # H % 64
     assert call(moe.make_dims(0, 128, 16, 4, 64, 64, 0)) == 0                 # T = 0
     assert moe.workspace_size_router(ok) > moe.workspace_size(ok)
+
+
+def test_host_validation_nvfp4(lib):
+    import mixture_experts_ffn_03_gb300 as moe
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    ok = moe.make_dims(16, 128, 16, 4, 128, 128, 0)
+
+    def call(dims, **kw):
+        args = [fake] * 16
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return lib.moe_forward_nvfp4(ctypes.byref(dims), *args, None, None, None, fake,
+                                     ctypes.c_size_t(1 << 40), None)
+    assert call(moe.make_dims(16, 64, 16, 4, 128, 128, 0)) == 2              # H % 128
+    assert call(ok, a4=None) == 1                                             # no gate/up matrix scales
+    assert call(ok, a4=P((1 << 20) + 2)) == 1                                 # misaligned matrix scales
+    assert call(ok, a3=P((1 << 20) + 8)) == 1                                 # misaligned block scales
+    assert call(moe.make_dims(0, 128, 16, 4, 128, 128, 0)) == 0               # T = 0
+    assert lib.moe_nvfp4_dequant(fake, fake, 4, 48, fake, None) == 1          # cols % 32
