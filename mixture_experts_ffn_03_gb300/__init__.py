@@ -253,26 +253,45 @@ class MoELayer:
     """The layer's weights plus a reusable workspace on one CUDA device.
 
     ``forward(hidden, logits)`` enqueues one moe_forward on the current
-    stream; outputs are allocated by PyTorch unless ``out`` is given."""
+    stream; outputs are allocated by PyTorch unless ``out`` is given. The
+    subclasses differ only in how the expert weights are held and which
+    entry point ``_enqueue`` calls."""
+
+    entry = "moe_forward"
 
     def __init__(self, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int, score_fn: int):
         import torch
         self.w_gate_up, self.w_down = w_gate_up, w_down
         self.ws_gate_up, self.ws_down, self.w_g = ws_gate_up, ws_down, w_g
-        self.E, two_i, self.H = w_gate_up.shape
+        self.E, two_i, self.H = self._shape(w_gate_up)
         self.I = two_i // 2
-        self.I_s = ws_gate_up.shape[0] // 2
+        self.I_s = self._shape(ws_gate_up)[0] // 2
         self.k, self.score_fn = int(k), int(score_fn)
-        self.device = w_gate_up.device
+        self.device = self._first(w_gate_up).device
         self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
-        self._ws_T = -1
+
+    @staticmethod
+    def _first(w):
+        return w
+
+    def _shape(self, w):
+        """Logical shape of a weight: (E, 2I, H) for the routed gate/up
+        weights, (2I_s, H) for the shared ones."""
+        return tuple(self._first(w).shape)
+
+    def _workspace_size(self, dims: MoEDims) -> int:
+        return workspace_size(dims)
+
+    def _enqueue(self, dims, hidden, logits, out, ws, topk_ids, topk_w, counts, stream):
+        return forward_raw(dims, hidden, logits, self.w_gate_up, self.w_down, self.ws_gate_up,
+                           self.ws_down, self.w_g, out, ws, topk_ids, topk_w, counts, stream)
 
     def dims(self, T: int) -> MoEDims:
         return make_dims(T, self.H, self.E, self.k, self.I, self.I_s, self.score_fn)
 
     def workspace(self, T: int):
         import torch
-        need = workspace_size(self.dims(T))
+        need = self._workspace_size(self.dims(T))
         if self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
         return self._ws
@@ -284,11 +303,10 @@ class MoELayer:
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
         ws = self.workspace(T)
-        st = forward_raw(self.dims(T), hidden, logits, self.w_gate_up, self.w_down,
-                         self.ws_gate_up, self.ws_down, self.w_g, out, ws, topk_ids, topk_w,
-                         counts, stream)
+        st = self._enqueue(self.dims(T), hidden, logits, out, ws, topk_ids, topk_w, counts,
+                           stream)
         if st != MOE_OK:
-            raise MoEError(st, "moe_forward")
+            raise MoEError(st, self.entry)
         return out
 
     def forward_from_host(self, hidden_host, logits_host, out_host, stream=None):
@@ -319,30 +337,16 @@ class MoELayerMXFP8(MoELayer):
     w_gate_up, w_down, ws_gate_up, ws_down is a pair (codes uint8 [..., rows,
     K], scales uint8 [..., K/32, rows]); w_g stays bf16."""
 
-    def __init__(self, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int, score_fn: int):
-        import torch
-        self.w_gate_up, self.w_down = w_gate_up, w_down
-        self.ws_gate_up, self.ws_down, self.w_g = ws_gate_up, ws_down, w_g
-        self.E, two_i, self.H = w_gate_up[0].shape
-        self.I = two_i // 2
-        self.I_s = ws_gate_up[0].shape[0] // 2
-        self.k, self.score_fn = int(k), int(score_fn)
-        self.device = w_gate_up[0].device
-        self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+    entry = "moe_forward_mxfp8"
 
-    def forward(self, hidden, logits, out=None, topk_ids=None, topk_w=None, counts=None,
-                stream=None):
-        import torch
-        T = hidden.shape[0]
-        if out is None:
-            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
-        ws = self.workspace(T)
-        st = forward_mxfp8_raw(self.dims(T), hidden, logits, *self.w_gate_up, *self.w_down,
-                               *self.ws_gate_up, *self.ws_down, self.w_g, out, ws, topk_ids,
-                               topk_w, counts, stream)
-        if st != MOE_OK:
-            raise MoEError(st, "moe_forward_mxfp8")
-        return out
+    @staticmethod
+    def _first(w):
+        return w[0]
+
+    def _enqueue(self, dims, hidden, logits, out, ws, topk_ids, topk_w, counts, stream):
+        return forward_mxfp8_raw(dims, hidden, logits, *self.w_gate_up, *self.w_down,
+                                 *self.ws_gate_up, *self.ws_down, self.w_g, out, ws, topk_ids,
+                                 topk_w, counts, stream)
 
 
 class MoELayerNVFP4(MoELayer):
@@ -350,31 +354,20 @@ class MoELayerNVFP4(MoELayer):
     w_down, ws_gate_up, ws_down is a triple (codes uint8 [..., rows, K/2],
     scales uint8 [..., K/16, rows], g fp32 [E] or [1]); w_g stays bf16."""
 
-    def __init__(self, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int, score_fn: int):
-        import torch
-        self.w_gate_up, self.w_down = w_gate_up, w_down
-        self.ws_gate_up, self.ws_down, self.w_g = ws_gate_up, ws_down, w_g
-        self.E, two_i, half_h = w_gate_up[0].shape
-        self.H = 2 * half_h
-        self.I = two_i // 2
-        self.I_s = ws_gate_up[0].shape[0] // 2
-        self.k, self.score_fn = int(k), int(score_fn)
-        self.device = w_gate_up[0].device
-        self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+    entry = "moe_forward_nvfp4"
 
-    def forward(self, hidden, logits, out=None, topk_ids=None, topk_w=None, counts=None,
-                stream=None):
-        import torch
-        T = hidden.shape[0]
-        if out is None:
-            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
-        ws = self.workspace(T)
-        st = forward_nvfp4_raw(self.dims(T), hidden, logits, self.w_gate_up, self.w_down,
-                               self.ws_gate_up, self.ws_down, self.w_g, out, ws, topk_ids,
-                               topk_w, counts, stream)
-        if st != MOE_OK:
-            raise MoEError(st, "moe_forward_nvfp4")
-        return out
+    @staticmethod
+    def _first(w):
+        return w[0]
+
+    def _shape(self, w):
+        *lead, half_k = self._first(w).shape  # two E2M1 codes per byte along K
+        return (*lead, 2 * half_k)
+
+    def _enqueue(self, dims, hidden, logits, out, ws, topk_ids, topk_w, counts, stream):
+        return forward_nvfp4_raw(dims, hidden, logits, self.w_gate_up, self.w_down,
+                                 self.ws_gate_up, self.ws_down, self.w_g, out, ws, topk_ids,
+                                 topk_w, counts, stream)
 
 
 class MoELayerRouter(MoELayer):
@@ -382,31 +375,24 @@ class MoELayerRouter(MoELayer):
     forward(hidden) with w_router [E, H] bf16 held by the layer; the logits
     [T, E] fp32 are returned through `logits` when given."""
 
+    entry = "moe_forward_router"
+
     def __init__(self, w_router, w_gate_up, w_down, ws_gate_up, ws_down, w_g, k: int,
                  score_fn: int):
         super().__init__(w_gate_up, w_down, ws_gate_up, ws_down, w_g, k, score_fn)
         self.w_router = w_router
 
-    def workspace(self, T: int):
-        import torch
-        need = workspace_size_router(self.dims(T))
-        if self._ws.numel() < need:
-            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
-        return self._ws
+    def _workspace_size(self, dims: MoEDims) -> int:
+        return workspace_size_router(dims)
+
+    def _enqueue(self, dims, hidden, logits, out, ws, topk_ids, topk_w, counts, stream):
+        return forward_router_raw(dims, hidden, self.w_router, self.w_gate_up, self.w_down,
+                                  self.ws_gate_up, self.ws_down, self.w_g, out, ws, logits,
+                                  topk_ids, topk_w, counts, stream)
 
     def forward(self, hidden, logits=None, out=None, topk_ids=None, topk_w=None, counts=None,
                 stream=None):
-        import torch
-        T = hidden.shape[0]
-        if out is None:
-            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
-        ws = self.workspace(T)
-        st = forward_router_raw(self.dims(T), hidden, self.w_router, self.w_gate_up, self.w_down,
-                                self.ws_gate_up, self.ws_down, self.w_g, out, ws, logits,
-                                topk_ids, topk_w, counts, stream)
-        if st != MOE_OK:
-            raise MoEError(st, "moe_forward_router")
-        return out
+        return super().forward(hidden, logits, out, topk_ids, topk_w, counts, stream)
 
 
 class HostPipeline:
