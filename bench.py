@@ -4,8 +4,10 @@
 
 One step = one moe_forward (route, permute, gate_up GEMM, down GEMM, shared
 expert, combine) over the workload's T tokens, inputs resident in HBM. Each
-timed step is bracketed by CUDA events on the launching stream, with a 256 MB
-write between steps to flush L2. Per-kernel times come from events the
+timed step is bracketed by CUDA events on the launching stream; between steps
+L2 is flushed by a 256 MB write followed by a 256 MB read of a second buffer,
+so each step starts with no layer data in L2 and no dirty lines whose
+write-back would fall inside the step. Per-kernel times come from events the
 library records around each of its kernels on the same stream. Prints one
 JSON line (rank 0).
 
@@ -144,6 +146,8 @@ KERNEL_SOURCES = {
                           "moe_internal.cuh"),
     "moe_gate_up_nvfp4": ("moe_gemm_mx.cu", "mxfp8.cuh", "gemm_common.cuh", "ptx.cuh",
                           "moe_internal.cuh"),
+    "moe_expert_fused": ("moe_fused.cu", "moe_fused.cuh", "gemm_common.cuh", "ptx.cuh",
+                         "moe_internal.cuh"),
 }
 
 
@@ -261,6 +265,9 @@ def main():
                          "(moe_forward_nvfp4)")
     ap.add_argument("--router", action="store_true",
                     help="compute the router logits in the layer from W_router (moe_forward_router)")
+    ap.add_argument("--fusion", action="store_true",
+                    help="allow the fused gate_up + down launch (bf16 weights, decode-sized "
+                         "batches; off by default)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -282,6 +289,7 @@ def main():
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     moe.load_library()
+    moe.set_expert_fusion(args.fusion)
 
     mx = args.weights == "mxfp8"
     nv = args.weights == "nvfp4"
@@ -311,7 +319,16 @@ def main():
     stream = torch.cuda.Stream(dev)
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
     counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2(i):
+        # Write 256 MB (evicts the layer's data), then read another 256 MB so the
+        # written lines leave L2 before the step: their write-back would
+        # otherwise take DRAM bandwidth inside the next timed step.
+        flush_w.fill_(i & 0xFF)
+        torch.sum(flush_r, dim=(0,), out=flush_sink)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -325,6 +342,18 @@ def main():
         work["flops"] += 2.0 * T * cfg.E * cfg.H
         work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * T * cfg.E
     gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
+    if mx or nv:
+        n_launch = moe.launch_count_quantized(layer.dims(T))
+    else:
+        n_launch = (moe.launch_count_router if args.router else moe.launch_count)(layer.dims(T))
+        with moe.expert_fusion(False):
+            n_separate = (moe.launch_count_router if args.router else moe.launch_count)(layer.dims(T))
+    fused = not (mx or nv) and n_launch < n_separate
+    if fused:
+        # gate_up and down run as one launch (stage 3 of the per-kernel events)
+        gu_kernel = "moe_expert_fused"
+        work["gate_up_bytes"] += work["down_bytes"]
+        work["gate_up_flops"] += work["down_flops"]
 
     K = args.steps
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -347,7 +376,7 @@ def main():
     wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(i)
             step_ev[i][0].record(stream)
             layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
             step_ev[i][1].record(stream)
@@ -364,7 +393,7 @@ def main():
     # pass of K steps and not part of the step timing above).
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(i)
             moe.set_stage_events(stage_ev[i])
             layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
     moe.set_stage_events(None)
@@ -393,7 +422,7 @@ def main():
                 for _ in range(K)]
         with torch.cuda.stream(stream):
             for i in range(K):
-                flush.fill_(i & 0xFF)
+                flush_l2(i)
                 g_ev[i][0].record(stream)
                 g.replay()
                 g_ev[i][1].record(stream)
@@ -418,7 +447,7 @@ def main():
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(i)
             e2e_ev[i][0].record(stream)
             layer.forward_from_host(h_host, l_host, o_host, stream=stream)
             e2e_ev[i][1].record(stream)
@@ -458,13 +487,15 @@ def main():
         roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=achieved / peaks["hbm_gbs"],
                     traffic=read_traffic(gu_kernel, cfg.name),
-                    kernel=f"{gu_kernel} grouped GEMM", peak_source=peaks["source"])
+                    kernel=f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if fused else ""),
+                    peak_source=peaks["source"])
     else:
         achieved = work["gate_up_flops"] / (gu_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
                     frac=achieved / peak, traffic=read_traffic(gu_kernel, cfg.name),
-                    kernel=f"{gu_kernel} grouped GEMM", peak_source=peaks["source"])
+                    kernel=f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if fused else ""),
+                    peak_source=peaks["source"])
     t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9),
                  work["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
     layer_roof = dict(bound="hbm" if hbm_bound else "tensor", roofline_ms=t_roof * 1e3,
@@ -485,16 +516,18 @@ def main():
         config=dict(workload=workload_name(cfg), seed=0, weights=args.weights,
                     router="in the layer (moe_forward_router)" if args.router else "logits input",
                     parallelism="replicas" if world > 1 else "1gpu",
-                    l2="flushed: 256 MB write between timed steps", launch="stream",
+                    l2="flushed between timed steps: 256 MB write, then 256 MB read of a "
+                       "second buffer (no dirty lines left)", launch="stream",
+                    experts="one fused gate_up + down launch" if fused else "gate_up and down launches",
                     wall_s=round(wall, 3)),
         roofline=roof, layer_roofline=layer_roof, kernel_us=kernels,
         kernel_timing="separate pass of K steps with library-recorded events around each kernel",
-        down_gbs=work["down_bytes"] / (dn_ms / 1e3) / 1e9,
+        down_gbs=None if fused else work["down_bytes"] / (dn_ms / 1e3) / 1e9,
         e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h,
                  mode="serving loop (moe.HostPipeline): transfers overlap neighbouring steps' compute",
                  serial_value=world * T * K / (e2e_serial_ms / 1e3)),
-        gpu_launches=(moe.launch_count_router if args.router else moe.launch_count)(layer.dims(T)) * K,
+        gpu_launches=n_launch * K,
         clocks=clocks, cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
         inp_cpu = {n: t.cpu() for n, t in inp.items() if t is not None}

@@ -255,8 +255,11 @@ typedef struct {
 
 moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layout);
 
-/* Number of kernels one moe_forward enqueues (route, count/scan, scatter,
- * gate_up GEMM, down GEMM, combine). */
+/* Stages of one moe_forward, each at most one kernel (route, count/scan,
+ * scatter, gate_up GEMM, down GEMM, combine). Stages that a smaller batch
+ * merges into the one before are empty: routing and the permute share one
+ * launch when T*k <= 2048, and the fused expert launch (moe_set_expert_fusion,
+ * when enabled) runs in the gate_up stage, leaving the down stage empty. */
 #define MOE_NUM_STAGES 6
 
 /* Optional per-kernel timing. `events` points to MOE_NUM_STAGES + 1
@@ -268,10 +271,35 @@ moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layou
  * MOE_ERR_INVALID_ARG unless n_events is 0 or MOE_NUM_STAGES + 1. */
 moe_status moe_set_stage_events(void* const* events, int n_events);
 
-/* Number of kernels one moe_forward with these sizes launches (4 when
- * T*k <= 2048: routing and the permute share one launch; else 6), or 0 for
- * invalid sizes or T = 0. */
+/* Number of kernels one moe_forward with these sizes launches from the
+ * calling host thread, or 0 for invalid sizes or T = 0: routing (1 launch
+ * when T*k <= 2048, else 3), the expert GEMMs (1 launch when they run fused,
+ * else 2) and the combine. */
 int moe_launch_count(const moe_dims* d);
+
+/* The same for moe_forward_mxfp8 and moe_forward_nvfp4 (their expert GEMMs
+ * always take two launches); 0 also for sizes those entry points reject. */
+int moe_launch_count_quantized(const moe_dims* d);
+
+/* Fused expert phase (bf16 weights: moe_forward and moe_forward_router).
+ * When enabled (per host thread; off by default) and the batch's gate_up and
+ * down token tiles have the same width of at most 64 tokens (decode-sized
+ * batches: about T*k/E <= 51 tokens per expert), the two grouped GEMMs run
+ * as one persistent launch. Its tile sequence holds the gate_up tiles and
+ * then the down tiles; a down tile waits on a device counter (bounded in
+ * time, like every wait in the library) for the gate_up tiles of its row
+ * tile. That removes the idle tail of the gate_up launch and the refill of
+ * the down pipeline. The arithmetic is the same as the two launches', so the
+ * results are bitwise identical. Measured on GB300 it is no faster than
+ * the two launches at decode and about 4 % slower on wide batches, hence
+ * off by default. The wait needs every CTA of the launch
+ * resident at once (one per SM); if another kernel holds SMs for longer
+ * than the wait limit, the layer reports MOE_ERR_DEVICE_TIMEOUT through
+ * moe_device_status. Source: "Add Qwen3.5-35B-A3B (support vision and text
+ * input)", Description (the routed experts and the shared expert); the
+ * fusion is an implementation choice. */
+void moe_set_expert_fusion(int enable);
+int moe_get_expert_fusion(void);
 
 /* Self-test of the kernels' bounded waits (failure detection without a GPU
  * fault): clears the status word at the start of `workspace` (256-byte

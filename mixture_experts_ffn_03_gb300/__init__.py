@@ -31,7 +31,8 @@ EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_statu
             "moe_workspace_layout", "moe_set_stage_events", "moe_launch_count",
             "moe_selftest_wait_limit", "moe_forward_mxfp8", "moe_mxfp8_dequant",
             "moe_forward_router", "moe_workspace_size_router", "moe_launch_count_router",
-            "moe_forward_nvfp4", "moe_nvfp4_dequant"]
+            "moe_forward_nvfp4", "moe_nvfp4_dequant", "moe_launch_count_quantized",
+            "moe_set_expert_fusion", "moe_get_expert_fusion"]
 NUM_STAGES = 6
 STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
 
@@ -97,6 +98,12 @@ def load_library(path: str = LIB_PATH):
     lib.moe_workspace_size_router.restype = ctypes.c_size_t
     lib.moe_launch_count_router.argtypes = [ctypes.POINTER(MoEDims)]
     lib.moe_launch_count_router.restype = ctypes.c_int
+    lib.moe_launch_count_quantized.argtypes = [ctypes.POINTER(MoEDims)]
+    lib.moe_launch_count_quantized.restype = ctypes.c_int
+    lib.moe_set_expert_fusion.argtypes = [ctypes.c_int]
+    lib.moe_set_expert_fusion.restype = None
+    lib.moe_get_expert_fusion.argtypes = []
+    lib.moe_get_expert_fusion.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -118,8 +125,40 @@ def workspace_layout(dims: MoEDims) -> MoEWorkspaceLayout:
 
 
 def launch_count(dims: MoEDims) -> int:
-    """Kernels one moe_forward launches for these sizes."""
+    """Kernels one moe_forward launches for these sizes (from this thread)."""
     return int(load_library().moe_launch_count(ctypes.byref(dims)))
+
+
+def launch_count_quantized(dims: MoEDims) -> int:
+    """Kernels one moe_forward_mxfp8 / moe_forward_nvfp4 launches for these sizes."""
+    return int(load_library().moe_launch_count_quantized(ctypes.byref(dims)))
+
+
+def set_expert_fusion(enable: bool) -> None:
+    """Allow or forbid (the default) the fused gate_up + down launch for bf16
+    weights on decode-sized batches, for calls from this host thread."""
+    load_library().moe_set_expert_fusion(1 if enable else 0)
+
+
+def get_expert_fusion() -> bool:
+    return bool(load_library().moe_get_expert_fusion())
+
+
+class expert_fusion:
+    """Context manager: `with expert_fusion(False): ...` runs the block with
+    the fused expert launch forbidden (or allowed), then restores the setting."""
+
+    def __init__(self, enable: bool):
+        self.enable = bool(enable)
+
+    def __enter__(self):
+        self.prev = get_expert_fusion()
+        set_expert_fusion(self.enable)
+        return self
+
+    def __exit__(self, *exc):
+        set_expert_fusion(self.prev)
+        return False
 
 
 def status_string(status: int) -> str:

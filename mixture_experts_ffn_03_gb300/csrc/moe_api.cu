@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "moe.h"
+#include "moe_fused.cuh"
 #include "moe_internal.cuh"
 
 #define MOE_API extern "C" __attribute__((visibility("default")))
@@ -19,7 +20,7 @@ constexpr int kMaxDevices = 64;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t meta, topk_ids, topk_w, gate_logit, counts, offsets, perm, inv, blockhist;
+    size_t meta, ready, topk_ids, topk_w, gate_logit, counts, offsets, perm, inv, blockhist;
     size_t rt_gu, rt_dn, h_hi, h_lo, hs_hi, hs_lo, y, total;
 };
 
@@ -53,6 +54,7 @@ Layout layout_of(const moe_dims& d) {
     const size_t T = d.T, H = d.H, E = d.E, I = d.I, Is = d.I_s, tk = T * d.k;
     const size_t nb = (T + kCountTokens - 1) / kCountTokens;
     L.meta = take(META_WORDS * sizeof(int));
+    L.ready = take((tk + T) * 4);  // right after the status block: one memset clears both
     L.topk_ids = take(tk * 4);
     L.topk_w = take(tk * 4);
     L.gate_logit = take(T * 4);
@@ -207,6 +209,34 @@ int pick_bn(size_t tk, int E, int cap, bool gate_up) {
         if (w >= 1.25 * mean) break;
     }
     return bn;
+}
+
+// Per host thread: may moe_forward / moe_forward_router run gate_up and down
+// as one launch (moe_set_expert_fusion)? Off by default: measured on GB300,
+// the fused launch is no faster at decode (the programmatic dependent launch
+// already overlaps the boundary) and slower on wide batches (its down steps
+// share the gate_up-sized ring and keep fewer bytes in flight).
+thread_local bool tl_fusion = false;
+
+// Token-tile widths of the two bf16 GEMMs, and whether they run fused.
+struct BnPlan {
+    int gu, dn;
+    bool fused;
+};
+
+BnPlan bn_plan(size_t tk, int E, bool mx) {
+    BnPlan p;
+    p.gu = pick_bn(tk, E, mx ? 64 : 256, true);
+    p.dn = pick_bn(tk, E, mx ? 64 : 128, false);
+    p.fused = !mx && tl_fusion && p.gu == p.dn && p.gu <= kFusedMaxBN;
+    return p;
+}
+
+// Kernels one forward launches: routing (one launch, or route + count/scan +
+// scatter), the expert GEMMs (one fused launch or two), the combine.
+int launches_of(const moe_dims& d, bool mx) {
+    const size_t tk = static_cast<size_t>(d.T) * d.k;
+    return (route_small_fits(d.T, d.E, d.k) ? 1 : 3) + (bn_plan(tk, d.E, mx).fused ? 1 : 2) + 1;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -408,8 +438,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
 
     // The MXFP8 GEMMs keep the weights on the MMA's M side at every size and
     // take tiles of at most 64 tokens.
-    const int bn_gu = pick_bn(tk, E, W.mx ? 64 : 256, true);
-    const int bn_dn = pick_bn(tk, E, W.mx ? 64 : 128, false);
+    const BnPlan plan = bn_plan(tk, E, W.mx);
+    const int bn_gu = plan.gu, bn_dn = plan.dn;
     const int num_sms = sm_count();
     if (num_sms <= 0) return MOE_ERR_CUDA;
 
@@ -483,8 +513,11 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     const int tiles_gu = static_cast<int>(max_gu < cap ? max_gu : cap);
     const int tiles_dn = static_cast<int>(max_dn < cap ? max_dn : cap);
 
-    // Status words (error flags, tile counts, completion ticket) start at zero.
-    if (cudaMemsetAsync(meta, 0, META_WORDS * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // Status words (error flags, tile counts, completion ticket) start at zero,
+    // and so do the fused launch's row-tile readiness counters that follow them.
+    const size_t zero_bytes = plan.fused ? L.ready - L.meta + (tk + T) * sizeof(int)
+                                         : META_WORDS * sizeof(int);
+    if (cudaMemsetAsync(meta, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(0, st);
     LogitSrc lsrc{router_logits, 1, 0, nullptr};
     if (w_router) {
@@ -526,14 +559,24 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
             return MOE_ERR_CUDA;
     }
     mark_stage(3, st);
-    const cudaError_t e_gu = W.mx ? launch_gate_up_mx(bn_gu, W.nv, mgu, ga, tiles_gu, num_sms, st)
-                                  : launch_gate_up(bn_gu, gu, ga, tiles_gu, num_sms, st);
-    if (e_gu != cudaSuccess) return MOE_ERR_CUDA;
-    mark_stage(4, st);
-    const cudaError_t e_dn = W.mx ? launch_down_mx(bn_dn, W.nv, mdn, gd, tiles_dn, num_sms, st)
-                                  : launch_down(bn_dn, dn, gd, tiles_dn, num_sms, st);
-    if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
-    mark_stage(5, st);
+    if (plan.fused) {
+        // gate_up and down in one launch; its time is stage 4's, stage 5 is empty.
+        int* ready = reinterpret_cast<int*>(ws + L.ready);
+        const int tiles = tiles_gu > cap - tiles_dn ? cap : tiles_gu + tiles_dn;
+        if (launch_expert_fused(bn_gu, gu, dn, ga, ready, tiles, num_sms, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark_stage(4, st);
+        mark_stage(5, st);
+    } else {
+        const cudaError_t e_gu = W.mx ? launch_gate_up_mx(bn_gu, W.nv, mgu, ga, tiles_gu, num_sms, st)
+                                      : launch_gate_up(bn_gu, gu, ga, tiles_gu, num_sms, st);
+        if (e_gu != cudaSuccess) return MOE_ERR_CUDA;
+        mark_stage(4, st);
+        const cudaError_t e_dn = W.mx ? launch_down_mx(bn_dn, W.nv, mdn, gd, tiles_dn, num_sms, st)
+                                      : launch_down(bn_dn, dn, gd, tiles_dn, num_sms, st);
+        if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
+        mark_stage(5, st);
+    }
     // 128-token down tiles leave y as 24-bit floats, the other widths as fp32.
     if ((launch_combine(T, H, k, y, !W.mx && bn_dn == 128, topk_w, inv,
                         static_cast<__nv_bfloat16*>(out), st)) != cudaSuccess)
@@ -585,7 +628,7 @@ MOE_API size_t moe_workspace_size_router(const moe_dims* d) {
 
 MOE_API int moe_launch_count_router(const moe_dims* d) {
     if (!dims_valid(d) || !dims_supported(d) || d->T == 0) return 0;
-    return (route_small_fits(d->T, d->E, d->k) ? 4 : 6) + 1;
+    return launches_of(*d, false) + 1;
 }
 
 MOE_API moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden,
@@ -667,8 +710,17 @@ MOE_API moe_status moe_mxfp8_dequant(const void* codes, const void* scales, int 
 
 MOE_API int moe_launch_count(const moe_dims* d) {
     if (!dims_valid(d) || !dims_supported(d) || d->T == 0) return 0;
-    return route_small_fits(d->T, d->E, d->k) ? 4 : 6;
+    return launches_of(*d, false);
 }
+
+MOE_API int moe_launch_count_quantized(const moe_dims* d) {
+    if (!dims_valid(d) || !dims_supported(d) || !dims_supported_mx(d) || d->T == 0) return 0;
+    return launches_of(*d, true);
+}
+
+MOE_API void moe_set_expert_fusion(int enable) { tl_fusion = enable != 0; }
+
+MOE_API int moe_get_expert_fusion(void) { return tl_fusion ? 1 : 0; }
 
 MOE_API moe_status moe_set_stage_events(void* const* events, int n_events) {
     if (n_events == 0 || events == nullptr) {

@@ -88,9 +88,21 @@ def test_host_validation(lib):
     assert _call(lib, moe.make_dims(0, 128, 16, 4, 64, 64, 0)) == 0        # T = 0: no work
     for s in range(7):
         assert moe.status_string(s)
-    assert moe.launch_count(moe.make_dims(64, 2048, 256, 8, 512, 512, 1)) == 4   # T*k <= 2048
+    decode = moe.make_dims(64, 2048, 256, 8, 512, 512, 1)
+    assert not moe.get_expert_fusion()                                      # off by default
+    assert moe.launch_count(decode) == 4                                    # T*k <= 2048
+    assert moe.launch_count_router(decode) == 5
+    with moe.expert_fusion(True):
+        assert moe.get_expert_fusion()
+        assert moe.launch_count(decode) == 3  # one routing launch, fused experts, combine
+        assert moe.launch_count_router(decode) == 4
+        assert moe.launch_count_quantized(decode) == 4                      # never fused
+        assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 6  # BN 160/128
+        assert moe.launch_count(moe.make_dims(512, 2048, 256, 8, 512, 512, 0)) == 5   # BN 32/32
+    assert not moe.get_expert_fusion()
     assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 6
     assert moe.launch_count(moe.make_dims(0, 2048, 256, 8, 512, 512, 0)) == 0
+    assert moe.launch_count_quantized(moe.make_dims(64, 2048, 256, 8, 192, 512, 1)) == 0
 
 
 def _call_mx(lib, dims, **kw):
