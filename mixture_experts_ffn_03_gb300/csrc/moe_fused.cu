@@ -3,13 +3,17 @@
 // (the same MMA shapes, the same accumulation order, the same epilogues), so
 // its results are bitwise those of the two separate launches.
 //
-// Why: with separate launches every SM that runs out of gate_up tiles idles
+// Aim: with separate launches every SM that runs out of gate_up tiles idles
 // until the last gate_up tile anywhere is done (the down grid may start only
 // then), and the down pipeline then fills from empty. Here one tile sequence
 // holds the gate_up tiles and after them the down tiles; an SM that finishes
 // its gate_up work goes straight on to down tiles, whose weights do not
 // depend on gate_up at all, and only the h operand of a down tile waits for
-// its row tile's gate_up tiles.
+// its row tile's gate_up tiles. Measured on GB300 the gain does not
+// materialise: the separate launches already overlap through programmatic
+// dependent launch, and a down step here uses 20 KB of a 34 KB stage (fewer
+// bytes in flight than the down kernel's own ring), so the launch is opt-in
+// (moe_set_expert_fusion).
 //
 // Dependency: a down tile of row tile r reads h over all I features of r, so
 // it needs every gate_up tile of r. Each epilogue warp that finishes its part
