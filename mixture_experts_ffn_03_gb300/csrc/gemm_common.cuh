@@ -241,17 +241,114 @@ __device__ __forceinline__ void drain_tma(Ctl* ctl, uint32_t armed, uint32_t par
 
 // Scale of the tile's weight matrix: the fp32 matrix scale of NVFP4 weights
 // (per routed expert, or the shared expert's), 1 for bf16 and MXFP8 weights.
+// Bit 0 of Tile::shared marks the shared expert (other bits may tag the tile).
 __device__ __forceinline__ float matrix_scale(const GemmArgs& a, const Tile& ti) {
     if (!a.msc) return 1.f;
-    return ti.shared ? a.msc_s[0] : a.msc[ti.e];
+    return (ti.shared & 1) ? a.msc_s[0] : a.msc[ti.e];
 }
 
-// Epilogue role of the down GEMMs with the weights on M (warps 4-11), with
-// the same chunking as the gate_up epilogue: warp we owns 32 output features
-// (TMEM lanes 32*(warp % 4)..) and every other 16-column chunk; full chunks
-// go out as fp32 TMA box stores of y through st_y, ragged tails as plain
-// stores. Shared
-// expert rows are scaled by their token's gate sigmoid(x . w_g).
+// One gate_up tile with the tokens on TMEM lanes (tokens on the MMA's M side,
+// 128 gate then 128 up accumulator columns from `slot`), drained by epilogue
+// warp (q, half): it owns the 32 token rows 32q.. and the features
+// [64 half, +64) of the tile, and writes h = silu(gate) * up as bf16 hi/lo
+// pairs (h_hi = bf16(h), h_lo = bf16(h - h_hi)) with 16-byte stores of its
+// own row. Warp-uniform; the whole warp calls it.
+__device__ __forceinline__ void gate_up_ts_epilogue_tile(const Tile& ti, uint32_t slot, int q,
+                                                         int half, int lane, const GemmArgs& a) {
+    const int r0 = q * 32;  // first token row of this warp's lane quadrant
+    if (r0 >= ti.n_rows) return;
+    const bool sh = (ti.shared & 1) != 0;
+    const int n_feat = sh ? a.I_s : a.I;
+    const bool row_ok = r0 + lane < ti.n_rows;
+    const size_t prow = static_cast<size_t>(ti.p0 + r0 + lane) * n_feat;
+    __nv_bfloat16* dhi = sh ? a.hs_hi : a.h_hi;
+    __nv_bfloat16* dlo = sh ? a.hs_lo : a.h_lo;
+    const uint32_t tb = slot + (static_cast<uint32_t>(r0) << 16);
+    for (int c = half * 64; c < half * 64 + 64; c += 32) {
+        const int fb = ti.f * kGemmBM + c;
+        if (fb >= n_feat) break;  // I, I_s are multiples of 64
+        uint32_t g[32], u[32];
+        ptx::tmem_ld_32x32b_x32(tb + c, g);
+        ptx::tmem_ld_32x32b_x32(tb + kGemmBM + c, u);
+        ptx::tmem_ld_wait();
+        if (row_ok) {
+            uint32_t hi2[16], lo2[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float g0 = __uint_as_float(g[2 * j]);
+                const float g1 = __uint_as_float(g[2 * j + 1]);
+                const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+                const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+                const __nv_bfloat162 hp = __floats2bfloat162_rn(h0, h1);
+                const __nv_bfloat162 lp =
+                    __floats2bfloat162_rn(h0 - __low2float(hp), h1 - __high2float(hp));
+                hi2[j] = *reinterpret_cast<const uint32_t*>(&hp);
+                lo2[j] = *reinterpret_cast<const uint32_t*>(&lp);
+            }
+            uint4* phi = reinterpret_cast<uint4*>(dhi + prow + fb);
+            uint4* plo = reinterpret_cast<uint4*>(dlo + prow + fb);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                phi[v] = make_uint4(hi2[4 * v], hi2[4 * v + 1], hi2[4 * v + 2], hi2[4 * v + 3]);
+                plo[v] = make_uint4(lo2[4 * v], lo2[4 * v + 1], lo2[4 * v + 2], lo2[4 * v + 3]);
+            }
+        }
+    }
+}
+
+// One down tile with the weights on M (W h_hi in accumulator columns [0, BN)
+// and W h_lo in [BN, 2 BN) from `slot`), drained by epilogue warp (q, half):
+// it owns 32 output features (TMEM lanes 32q..) and every other 16-column
+// chunk. Full chunks go out as fp32 TMA box stores of y through st_y, staged
+// in the warp's BUFS buffers at stg (nbuf counts the buffers used); ragged
+// tails as plain stores. Shared-expert rows are scaled by their token's gate
+// sigmoid(x . w_g), NVFP4 tiles by the matrix scale. Warp-uniform.
+template <int BN, int BUFS>
+__device__ __forceinline__ void down_epilogue_tile(const Tile& ti, uint32_t slot, int q, int half,
+                                                   int lane, uint8_t* stg, uint32_t& nbuf,
+                                                   const CUtensorMap* st_y, const GemmArgs& a) {
+    const bool sh = (ti.shared & 1) != 0;
+    const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
+    const bool warp_valid = h0 < a.H;               // H is a multiple of 64
+    const int row0 = sh ? a.T * a.k + ti.m0 : ti.p0;
+    const float msc = matrix_scale(a, ti);
+    const uint32_t tb = slot + (static_cast<uint32_t>(q * 32) << 16);
+    for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
+        uint32_t v[kEpiRows], vl[kEpiRows];
+        ptx::tmem_ld_32x32b_x16(tb + c0, v);        // W h_hi
+        ptx::tmem_ld_32x32b_x16(tb + BN + c0, vl);  // W h_lo
+        ptx::tmem_ld_wait();
+        if (!warp_valid) continue;
+        const int rows = min(kEpiRows, ti.n_rows - c0);
+        float val[kEpiRows];
+#pragma unroll
+        for (int n = 0; n < kEpiRows; ++n) {
+            val[n] = msc * (__uint_as_float(v[n]) + __uint_as_float(vl[n]));
+            if (sh && n < rows) val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
+        }
+        if (rows == kEpiRows) {
+            const uint32_t b = nbuf++ % BUFS;
+            float* sy = reinterpret_cast<float*>(stg + b * kStgBytes);
+            if (lane == 0) ptx::bulk_wait_read<BUFS - 1>();  // buffer b is free
+            __syncwarp();
+#pragma unroll
+            for (int n = 0; n < kEpiRows; ++n) sy[n * kEpiCols + lane] = val[n];
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(st_y, ptx::smem_u32(sy), h0, row0 + c0);
+                ptx::bulk_commit();
+            }
+        } else {
+#pragma unroll
+            for (int n = 0; n < kEpiRows; ++n)
+                if (n < rows) a.y[static_cast<size_t>(row0 + c0 + n) * a.H + h0 + lane] = val[n];
+        }
+    }
+}
+
+// Epilogue role of the down GEMMs with the weights on M (warps 4-11): the
+// tiles in queue order, each by down_epilogue_tile.
 template <class C, int BN>
 __device__ __forceinline__ void down_epilogue(uint8_t* smem, Ctl* ctl, uint32_t tmem_base, int warp,
                                               int lane, const CUtensorMap* st_y,
@@ -262,52 +359,14 @@ __device__ __forceinline__ void down_epilogue(uint8_t* smem, Ctl* ctl, uint32_t 
     uint32_t nbuf = 0;
     int as = 0;
     uint32_t aph = 0;
-    const int shared_row0 = a.T * a.k;
     int qs = 0;
     uint32_t qph = 0;
     Tile ti;
     while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
         if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
         ptx::tc_fence_after();
-        const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
-        const bool warp_valid = h0 < a.H;               // H is a multiple of 64
-        const int row0 = ti.shared ? shared_row0 + ti.m0 : ti.p0;
-        const float msc = matrix_scale(a, ti);
-        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
-        for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
-            uint32_t v[kEpiRows], vl[kEpiRows];
-            ptx::tmem_ld_32x32b_x16(tb + c0, v);        // W h_hi
-            ptx::tmem_ld_32x32b_x16(tb + BN + c0, vl);  // W h_lo
-            ptx::tmem_ld_wait();
-            if (!warp_valid) continue;
-            const int rows = min(kEpiRows, ti.n_rows - c0);
-            float val[kEpiRows];
-#pragma unroll
-            for (int n = 0; n < kEpiRows; ++n) {
-                val[n] = msc * (__uint_as_float(v[n]) + __uint_as_float(vl[n]));
-                if (ti.shared && n < rows)
-                    val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
-            }
-            if (rows == kEpiRows) {
-                const uint32_t b = nbuf++ % C::EPI_BUFS;
-                float* sy = reinterpret_cast<float*>(stg + b * kStgBytes);
-                if (lane == 0) ptx::bulk_wait_read<C::EPI_BUFS - 1>();  // buffer b is free
-                __syncwarp();
-#pragma unroll
-                for (int n = 0; n < kEpiRows; ++n) sy[n * kEpiCols + lane] = val[n];
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d(st_y, ptx::smem_u32(sy), h0, row0 + c0);
-                    ptx::bulk_commit();
-                }
-            } else {
-#pragma unroll
-                for (int n = 0; n < kEpiRows; ++n)
-                    if (n < rows)
-                        a.y[static_cast<size_t>(row0 + c0 + n) * a.H + h0 + lane] = val[n];
-            }
-        }
+        down_epilogue_tile<BN, C::EPI_BUFS>(ti, tmem_base + as * C::ACC_COLS, q, half, lane, stg,
+                                            nbuf, st_y, a);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));

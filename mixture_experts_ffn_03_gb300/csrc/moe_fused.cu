@@ -385,7 +385,7 @@ expert_fused_kernel(const __grid_constant__ GemmMaps gu, const __grid_constant__
     } else {  // ------------------------------------------- epilogue (warps 4-11)
         const int we = warp - 4, q = warp & 3, half = we >> 2;
         uint8_t* stg = smem + C::EPI_OFF + we * C::EPI_BUFS * kStgBytes;
-        const int shared_row0 = tk;
+        uint32_t nbuf = 0;
         int as = 0;
         uint32_t aph = 0;
         int qs = 0;
@@ -394,103 +394,19 @@ expert_fused_kernel(const __grid_constant__ GemmMaps gu, const __grid_constant__
         while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
-            const bool sh = (ti.shared & 1) != 0;
             const uint32_t slot = tmem_base + as * C::ACC_COLS;
-            if (!(ti.shared & kDownBit)) {
-                // gate_up: tokens on TMEM lanes; warp we owns the 32 token rows
-                // 32*(warp % 4).. and the features [64*(we / 4), +64) of the
-                // tile, and writes h = silu(gate) * up as bf16 hi/lo pairs.
-                const int r0 = q * 32;
-                if (r0 < ti.n_rows) {
-                    const int n_feat = sh ? a.I_s : a.I;
-                    const bool row_ok = r0 + lane < ti.n_rows;
-                    const size_t prow = static_cast<size_t>(ti.p0 + r0 + lane) * n_feat;
-                    __nv_bfloat16* dhi = sh ? a.hs_hi : a.h_hi;
-                    __nv_bfloat16* dlo = sh ? a.hs_lo : a.h_lo;
-                    const uint32_t tb = slot + (static_cast<uint32_t>(r0) << 16);
-                    for (int c = half * 64; c < half * 64 + 64; c += 32) {
-                        const int fb = ti.f * kGemmBM + c;
-                        if (fb >= n_feat) break;  // I, I_s are multiples of 64
-                        uint32_t g[32], u[32];
-                        ptx::tmem_ld_32x32b_x32(tb + c, g);
-                        ptx::tmem_ld_32x32b_x32(tb + kGemmBM + c, u);
-                        ptx::tmem_ld_wait();
-                        if (row_ok) {
-                            uint32_t hi2[16], lo2[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float g0 = __uint_as_float(g[2 * j]);
-                                const float g1 = __uint_as_float(g[2 * j + 1]);
-                                const float h0 =
-                                    __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(u[2 * j]);
-                                const float h1 = __fdividef(g1, 1.f + __expf(-g1)) *
-                                                 __uint_as_float(u[2 * j + 1]);
-                                const __nv_bfloat162 hp = __floats2bfloat162_rn(h0, h1);
-                                const __nv_bfloat162 lp = __floats2bfloat162_rn(
-                                    h0 - __low2float(hp), h1 - __high2float(hp));
-                                hi2[j] = *reinterpret_cast<const uint32_t*>(&hp);
-                                lo2[j] = *reinterpret_cast<const uint32_t*>(&lp);
-                            }
-                            uint4* phi = reinterpret_cast<uint4*>(dhi + prow + fb);
-                            uint4* plo = reinterpret_cast<uint4*>(dlo + prow + fb);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                phi[v] = make_uint4(hi2[4 * v], hi2[4 * v + 1], hi2[4 * v + 2],
-                                                    hi2[4 * v + 3]);
-                                plo[v] = make_uint4(lo2[4 * v], lo2[4 * v + 1], lo2[4 * v + 2],
-                                                    lo2[4 * v + 3]);
-                            }
-                        }
-                    }
-                }
+            if (!(ti.shared & kDownBit)) {  // the same epilogues as the separate kernels
+                gate_up_ts_epilogue_tile(ti, slot, q, half, lane, a);
                 // This warp's share of the tile's h is written: make it visible
                 // to the TMA loads of other CTAs, then count it for the row tile.
                 fence_proxy_async_global();
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) red_release_gpu_add(ready + (sh ? tk + ti.m0 : ti.p0), 1);
+                if (lane == 0)
+                    red_release_gpu_add(ready + ((ti.shared & 1) ? tk + ti.m0 : ti.p0), 1);
             } else {
-                // down: warp we drains TMEM lanes 32*(warp % 4).. (32 output
-                // features) for every other 16-column chunk; full chunks go out
-                // as fp32 TMA box stores of y, ragged ones as plain stores; the
-                // shared expert's rows are scaled by their gate sigmoid(x . w_g).
-                const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
-                const bool warp_valid = h0 < a.H;               // H is a multiple of 64
-                const int row0 = sh ? shared_row0 + ti.m0 : ti.p0;
-                const uint32_t tb = slot + (static_cast<uint32_t>(q * 32) << 16);
-                for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {
-                    uint32_t v[kEpiRows], vl[kEpiRows];
-                    ptx::tmem_ld_32x32b_x16(tb + c0, v);        // W h_hi
-                    ptx::tmem_ld_32x32b_x16(tb + BN + c0, vl);  // W h_lo
-                    ptx::tmem_ld_wait();
-                    if (!warp_valid) continue;
-                    const int rows = min(kEpiRows, ti.n_rows - c0);
-                    float val[kEpiRows];
-#pragma unroll
-                    for (int n = 0; n < kEpiRows; ++n) {
-                        val[n] = __uint_as_float(v[n]) + __uint_as_float(vl[n]);
-                        if (sh && n < rows)
-                            val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
-                    }
-                    if (rows == kEpiRows) {
-                        float* sy = reinterpret_cast<float*>(stg);
-                        if (lane == 0) ptx::bulk_wait_read<0>();  // the staging buffer is free
-                        __syncwarp();
-#pragma unroll
-                        for (int n = 0; n < kEpiRows; ++n) sy[n * kEpiCols + lane] = val[n];
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            ptx::tma_store_2d(&dn.st[0], ptx::smem_u32(sy), h0, row0 + c0);
-                            ptx::bulk_commit();
-                        }
-                    } else {
-#pragma unroll
-                        for (int n = 0; n < kEpiRows; ++n)
-                            if (n < rows)
-                                a.y[static_cast<size_t>(row0 + c0 + n) * a.H + h0 + lane] = val[n];
-                    }
-                }
+                down_epilogue_tile<BN, C::EPI_BUFS>(ti, slot, q, half, lane, stg, nbuf, &dn.st[0],
+                                                    a);
             }
             ptx::tc_fence_before();
             __syncwarp();

@@ -254,10 +254,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         }
         ptx::cp_async_wait_all();
     } else if constexpr (C::TS) {  // ------------------------- epilogue (warps 4-11)
-        // Tokens on TMEM lanes: warp we owns the 32 token rows 32*(warp % 4)..
-        // and the features [64*(we / 4), +64) of the tile; each thread computes
-        // its token's h for 32 features at a time and writes the bf16 hi/lo
-        // pairs as 16-byte vector stores of its own row.
+        // Tokens on TMEM lanes: gate_up_ts_epilogue_tile per tile.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
         int as = 0;
         uint32_t aph = 0;
@@ -267,47 +264,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
-            const int r0 = q * 32;  // first token row of this warp's lane quadrant
-            if (r0 < ti.n_rows) {
-                const int n_feat = ti.shared ? a.I_s : a.I;
-                const bool row_ok = r0 + lane < ti.n_rows;
-                const size_t prow = static_cast<size_t>(ti.p0 + r0 + lane) * n_feat;
-                __nv_bfloat16* dhi = ti.shared ? a.hs_hi : a.h_hi;
-                __nv_bfloat16* dlo = ti.shared ? a.hs_lo : a.h_lo;
-                const uint32_t tb =
-                    tmem_base + (static_cast<uint32_t>(r0) << 16) + as * C::ACC_COLS;
-                for (int c = half * 64; c < half * 64 + 64; c += 32) {
-                    const int fb = ti.f * kGemmBM + c;
-                    if (fb >= n_feat) break;  // I, I_s are multiples of 64
-                    uint32_t g[32], u[32];
-                    ptx::tmem_ld_32x32b_x32(tb + c, g);
-                    ptx::tmem_ld_32x32b_x32(tb + kGemmBM + c, u);
-                    ptx::tmem_ld_wait();
-                    if (row_ok) {
-                        uint32_t hi2[16], lo2[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float g0 = __uint_as_float(g[2 * j]);
-                            const float g1 = __uint_as_float(g[2 * j + 1]);
-                            const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(u[2 * j]);
-                            const float h1 =
-                                __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
-                            const __nv_bfloat162 hp = __floats2bfloat162_rn(h0, h1);
-                            const __nv_bfloat162 lp = __floats2bfloat162_rn(
-                                h0 - __low2float(hp), h1 - __high2float(hp));
-                            hi2[j] = *reinterpret_cast<const uint32_t*>(&hp);
-                            lo2[j] = *reinterpret_cast<const uint32_t*>(&lp);
-                        }
-                        uint4* ph = reinterpret_cast<uint4*>(dhi + prow + fb);
-                        uint4* pl = reinterpret_cast<uint4*>(dlo + prow + fb);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            ph[v] = make_uint4(hi2[4 * v], hi2[4 * v + 1], hi2[4 * v + 2], hi2[4 * v + 3]);
-                            pl[v] = make_uint4(lo2[4 * v], lo2[4 * v + 1], lo2[4 * v + 2], lo2[4 * v + 3]);
-                        }
-                    }
-                }
-            }
+            gate_up_ts_epilogue_tile(ti, tmem_base + as * C::ACC_COLS, q, half, lane, a);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
