@@ -343,12 +343,13 @@ def main():
         work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * T * cfg.E
     gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
     if mx or nv:
-        n_launch = moe.launch_count_quantized(layer.dims(T))
+        n_launch = n_separate = moe.launch_count_quantized(layer.dims(T))
     else:
-        n_launch = (moe.launch_count_router if args.router else moe.launch_count)(layer.dims(T))
+        count = moe.launch_count_router if args.router else moe.launch_count
+        n_launch = count(layer.dims(T))
         with moe.expert_fusion(False):
-            n_separate = (moe.launch_count_router if args.router else moe.launch_count)(layer.dims(T))
-    fused = not (mx or nv) and n_launch < n_separate
+            n_separate = count(layer.dims(T))
+    fused = n_launch < n_separate  # the fused expert launch ran (bf16, --fusion, decode-sized)
     if fused:
         # gate_up and down run as one launch (stage 3 of the per-kernel events)
         gu_kernel = "moe_expert_fused"

@@ -144,9 +144,9 @@ def get_expert_fusion() -> bool:
     return bool(load_library().moe_get_expert_fusion())
 
 
-class expert_fusion:
-    """Context manager: `with expert_fusion(False): ...` runs the block with
-    the fused expert launch forbidden (or allowed), then restores the setting."""
+class expert_fusion:  # noqa: N801 (used like a function: `with expert_fusion(True):`)
+    """Context manager: `with expert_fusion(True): ...` runs the block with
+    the fused expert launch allowed (or forbidden), then restores the setting."""
 
     def __init__(self, enable: bool):
         self.enable = bool(enable)
