@@ -171,3 +171,45 @@ def test_host_validation_nvfp4(lib):
     assert call(ok, a3=P((1 << 20) + 8)) == 1                                 # misaligned block scales
     assert call(moe.make_dims(0, 128, 16, 4, 128, 128, 0)) == 0               # T = 0
     assert lib.moe_nvfp4_dequant(fake, fake, 4, 48, fake, None) == 1          # cols % 32
+
+
+def _tile_width(tk, E, cap, gate_up):
+    """Token-tile width rule as documented in moe_api.cu: the smallest
+    supported width >= 1.25x the mean group size, capped; 160 for gate_up only."""
+    mean = tk / E
+    bn = 16
+    for w in (16, 32, 64, 128, 160, 256):
+        if w > cap or (w == 160 and not gate_up):
+            continue
+        bn = w
+        if w >= 1.25 * mean:
+            break
+    return bn
+
+
+def test_expert_fusion_applies_exactly_when_tile_widths_match(lib):
+    import itertools
+    import mixture_experts_ffn_03_gb300 as moe
+    for T, E, k in itertools.product((1, 7, 64, 300, 512, 2048, 4096), (8, 64, 256, 512),
+                                     (1, 2, 8)):
+        if k > E:
+            continue
+        d = moe.make_dims(T, 256, E, k, 128, 128, 0)
+        tk = T * k
+        gu, dn = _tile_width(tk, E, 256, True), _tile_width(tk, E, 128, False)
+        with moe.expert_fusion(True):
+            on = moe.launch_count(d)
+        off = moe.launch_count(d)
+        assert on == off - (1 if gu == dn and gu <= 64 else 0), (T, E, k, gu, dn)
+
+
+def test_expert_fusion_setting_is_per_host_thread(lib):
+    import threading
+    import mixture_experts_ffn_03_gb300 as moe
+    seen = []
+    with moe.expert_fusion(True):
+        t = threading.Thread(target=lambda: seen.append(moe.get_expert_fusion()))
+        t.start()
+        t.join()
+        assert moe.get_expert_fusion()
+    assert seen == [False]
