@@ -3,13 +3,16 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
 One step = one moe_forward (route, permute, gate_up GEMM, down GEMM, shared
-expert, combine) over the workload's T tokens, inputs resident in HBM. Each
-timed step is bracketed by CUDA events on the launching stream; between steps
-L2 is flushed by a 256 MB write followed by a 256 MB read of a second buffer,
-so each step starts with no layer data in L2 and no dirty lines whose
+expert, combine) over the workload's T tokens, inputs resident in HBM. The
+headline workload is the largest one that fits one GPU (wide: T=2048,
+H=4096, 512 experts, top-10, I=1024, ~13 GB of expert weights). Each timed
+step is bracketed by CUDA events on the launching stream; between steps L2 is
+flushed by a 256 MB write followed by a 256 MB read of a second buffer, so
+each step starts with no layer data in L2 and no dirty lines whose
 write-back would fall inside the step. Per-kernel times come from events the
-library records around each of its kernels on the same stream. Prints one
-JSON line (rank 0).
+library records around each of its kernels on the same stream. At one GPU the
+decode, prefill and skewed workloads are then timed the same way and
+reported under per_config. Prints one JSON line (rank 0).
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a
 bounded token sample per step), with the same metric and workload.
@@ -32,7 +35,7 @@ if ROOT not in sys.path:
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-DEFAULT_CONFIG = "decode"
+DEFAULT_CONFIG = "wide"
 
 
 def load_peaks():
@@ -222,10 +225,12 @@ def run_reference(args, cfg):
     return 0
 
 
-def time_cpu_baseline(cfg, inp_cpu, budget_s=12.0, router=False):
+def time_cpu_baseline(cfg, inp_cpu, budget_s=12.0, router=False, threads=None):
+    """The oracle on the host cores over a bounded token sample (about budget_s
+    of CPU work): tokens/s and the threads it used."""
     import numpy as np
     import oracle
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     n = min(cfg.T, threads)
     if router:  # the router's logits for the sampled tokens, then the layer
         def run(toks):
@@ -252,6 +257,206 @@ def time_cpu_baseline(cfg, inp_cpu, budget_s=12.0, router=False):
                        f"{dt:.1f} s")
 
 
+# Workloads timed after the headline one, each with the same step timing and
+# L2 flush, and reported under per_config (one GPU, bf16 weights only).
+PER_CONFIG = ("decode", "prefill", "skewed")
+
+
+def make_layer(args, cfg, dev):
+    """Seeded inputs on the device and the layer object for the chosen weights."""
+    from mixture_experts_ffn_03_gb300 import workloads as wl
+    import mixture_experts_ffn_03_gb300 as moe
+    if args.router:
+        inp = wl.make_inputs_router(cfg, seed=0, device=str(dev))
+        layer = moe.MoELayerRouter(inp["w_router"], inp["w_gate_up"], inp["w_down"],
+                                   inp["ws_gate_up"], inp["ws_down"], inp["w_g"], cfg.k,
+                                   cfg.score_fn)
+        inp["logits"] = None
+    elif args.weights == "nvfp4":
+        inp = wl.make_inputs_nvfp4(cfg, seed=0, device=str(dev))
+        tri = lambda n: (inp[n + "_q"], inp[n + "_s"], inp[n + "_g"])  # noqa: E731
+        layer = moe.MoELayerNVFP4(tri("w_gate_up"), tri("w_down"), tri("ws_gate_up"),
+                                  tri("ws_down"), inp["w_g"], cfg.k, cfg.score_fn)
+    elif args.weights == "mxfp8":
+        inp = wl.make_inputs_mxfp8(cfg, seed=0, device=str(dev))
+        pair = lambda n: (inp[n + "_q"], inp[n + "_s"])  # noqa: E731
+        layer = moe.MoELayerMXFP8(pair("w_gate_up"), pair("w_down"), pair("ws_gate_up"),
+                                  pair("ws_down"), inp["w_g"], cfg.k, cfg.score_fn)
+    else:
+        inp = wl.make_inputs(cfg, seed=0, device=str(dev))
+        layer = moe.MoELayer(inp["w_gate_up"], inp["w_down"], inp["ws_gate_up"], inp["ws_down"],
+                             inp["w_g"], cfg.k, cfg.score_fn)
+    return inp, layer
+
+
+class L2Flush:
+    """Between timed steps: write 256 MB (evicts the layer's data), then read
+    another 256 MB so the written lines leave L2 before the step; their
+    write-back would otherwise take DRAM bandwidth inside the next step."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self, i):
+        import torch
+        self.w.fill_(i & 0xFF)
+        torch.sum(self.r, dim=(0,), out=self.sink)
+
+
+def measure(args, cfg, dev, layer, inp, stream, flush, K, sampler=None, dist=None):
+    """Warm-up, then K timed steps (CUDA events on the launching stream around
+    each step), then a separate pass of K steps with the library's per-kernel
+    events. Returns the step times, per-stage times, routing counts and the
+    launch accounting."""
+    import torch
+    import mixture_experts_ffn_03_gb300 as moe
+    mx, nv = args.weights == "mxfp8", args.weights == "nvfp4"
+    T = cfg.T
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            layer.forward(inp["hidden"], inp["logits"], out=out, counts=counts, stream=stream)
+    st = moe.device_status(layer.workspace(T), stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.status_string(st))
+    if mx or nv:
+        n_launch = n_separate = moe.launch_count_quantized(layer.dims(T))
+    else:
+        count = moe.launch_count_router if args.router else moe.launch_count
+        n_launch = count(layer.dims(T))
+        with moe.expert_fusion(False):
+            n_separate = count(layer.dims(T))
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
+                for _ in range(K)]
+    # torch creates CUDA events lazily; record each once so the handles exist.
+    with torch.cuda.stream(stream):
+        for evs in stage_ev:
+            for e in evs:
+                e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    # Timed region: K steps, each bracketed by events on the launching stream.
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler is not None:
+        sampler.start()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush(i)
+            step_ev[i][0].record(stream)
+            layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
+            step_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler is not None else None
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+
+    # Per-kernel pass: the library records events around each of its kernels
+    # on the same stream (this serialises the kernels, so it is a separate
+    # pass of K steps and not part of the step timing above).
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush(i)
+            moe.set_stage_events(stage_ev[i])
+            layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
+    moe.set_stage_events(None)
+    torch.cuda.synchronize(dev)
+    st = moe.device_status(layer.workspace(T), stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(moe.status_string(st))
+    stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev]
+                for j in range(moe.NUM_STAGES)]
+    return dict(step_ms=step_ms, stage_ms=stage_ms, counts=counts.cpu().tolist(), out=out,
+                n_launch=n_launch, fused=n_launch < n_separate, wall=wall, clocks=clocks)
+
+
+def work_of(args, cfg, m):
+    """Algorithmic work of one step and the name of the dominant kernel."""
+    mx, nv = args.weights == "mxfp8", args.weights == "nvfp4"
+    work = algorithmic_work(cfg, m["counts"],
+                            wbytes=1.0 + 1.0 / 32 if mx else (0.5 + 1.0 / 16 if nv else 2.0))
+    if args.router:  # W_router read and x . W_router^T computed instead of logits read
+        work["flops"] += 2.0 * cfg.T * cfg.E * cfg.H
+        work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * cfg.T * cfg.E
+    gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
+    if m["fused"]:
+        # gate_up and down run as one launch (stage 3 of the per-kernel events)
+        gu_kernel = "moe_expert_fused"
+        work["gate_up_bytes"] += work["down_bytes"]
+        work["gate_up_flops"] += work["down_flops"]
+    return work, gu_kernel
+
+
+def rooflines(cfg, work, m, peaks, gu_kernel):
+    """`roofline` of the dominant kernel (gate_up, or the fused expert launch)
+    and `layer_roofline` of the whole step."""
+    ms_step = sum(m["step_ms"]) / len(m["step_ms"])
+    gu_ms = statistics.mean(m["stage_ms"][3])
+    hbm_bound = work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (
+        peaks["bf16_tflops_sustained"] * 1e12)
+    kname = f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if m["fused"] else "")
+    if hbm_bound:
+        achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
+        roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=achieved / peaks["hbm_gbs"], traffic=read_traffic(gu_kernel, cfg.name),
+                    kernel=kname, peak_source=peaks["source"])
+    else:
+        achieved = work["gate_up_flops"] / (gu_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
+                    frac=achieved / peak, traffic=read_traffic(gu_kernel, cfg.name),
+                    kernel=kname, peak_source=peaks["source"])
+    t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 work["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
+    layer_roof = dict(bound="hbm" if hbm_bound else "tensor", roofline_ms=t_roof * 1e3,
+                      frac=t_roof * 1e3 / ms_step, bytes=work["bytes"], flops=work["flops"],
+                      experts_touched=work["touched"],
+                      frac_vs_nominal_8tbs=(work["bytes"] / 8e12 * 1e3) / ms_step)
+    return roof, layer_roof
+
+
+def kernel_us(m):
+    import mixture_experts_ffn_03_gb300 as moe
+    return {n: round(statistics.mean(v) * 1e3, 2) for n, v in zip(moe.STAGE_NAMES, m["stage_ms"])}
+
+
+def measure_per_config(args, dev, stream, flush, peaks, names):
+    """The other workloads at one GPU: ms/step, tokens/s, the layer and
+    dominant-kernel roofline fractions and the per-kernel times."""
+    import torch
+    from mixture_experts_ffn_03_gb300 import workloads as wl
+    res = {}
+    for name in names:
+        cfg = wl.CONFIGS[name]
+        inp, layer = make_layer(args, cfg, dev)
+        m = measure(args, cfg, dev, layer, inp, stream, flush, args.steps)
+        work, gu_kernel = work_of(args, cfg, m)
+        roof, layer_roof = rooflines(cfg, work, m, peaks, gu_kernel)
+        ms = sum(m["step_ms"]) / len(m["step_ms"])
+        res[name] = dict(workload=workload_name(cfg), ms_per_step=ms, value=cfg.T / (ms / 1e3),
+                         unit="tokens/s",
+                         layer_roofline=dict(bound=layer_roof["bound"],
+                                             roofline_ms=layer_roof["roofline_ms"],
+                                             frac=layer_roof["frac"]),
+                         roofline=dict(bound=roof["bound"], kernel=roof["kernel"],
+                                       achieved=roof["achieved"], unit=roof["unit"],
+                                       frac=roof["frac"]),
+                         kernel_us=kernel_us(m), gpu_launches=m["n_launch"] * args.steps)
+        del inp, layer, m
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -260,6 +465,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the --config workload (skip per_config)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
                     help="expert weight format: bf16, MXFP8 (moe_forward_mxfp8) or NVFP4 "
                          "(moe_forward_nvfp4)")
@@ -295,117 +502,18 @@ def main():
     nv = args.weights == "nvfp4"
     if (mx or nv) and args.router:
         raise SystemExit("--router runs with bf16 expert weights")
-    if args.router:
-        inp = wl.make_inputs_router(cfg, seed=0, device=str(dev))
-        layer = moe.MoELayerRouter(inp["w_router"], inp["w_gate_up"], inp["w_down"],
-                                   inp["ws_gate_up"], inp["ws_down"], inp["w_g"], cfg.k,
-                                   cfg.score_fn)
-        inp["logits"] = None
-    elif nv:
-        inp = wl.make_inputs_nvfp4(cfg, seed=0, device=str(dev))
-        tri = lambda n: (inp[n + "_q"], inp[n + "_s"], inp[n + "_g"])  # noqa: E731
-        layer = moe.MoELayerNVFP4(tri("w_gate_up"), tri("w_down"), tri("ws_gate_up"),
-                                  tri("ws_down"), inp["w_g"], cfg.k, cfg.score_fn)
-    elif mx:
-        inp = wl.make_inputs_mxfp8(cfg, seed=0, device=str(dev))
-        pair = lambda n: (inp[n + "_q"], inp[n + "_s"])  # noqa: E731
-        layer = moe.MoELayerMXFP8(pair("w_gate_up"), pair("w_down"), pair("ws_gate_up"),
-                                  pair("ws_down"), inp["w_g"], cfg.k, cfg.score_fn)
-    else:
-        inp = wl.make_inputs(cfg, seed=0, device=str(dev))
-        layer = moe.MoELayer(inp["w_gate_up"], inp["w_down"], inp["ws_gate_up"], inp["ws_down"],
-                             inp["w_g"], cfg.k, cfg.score_fn)
+    inp, layer = make_layer(args, cfg, dev)
     T = cfg.T
-    stream = torch.cuda.Stream(dev)
-    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
-    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
-
-    def flush_l2(i):
-        # Write 256 MB (evicts the layer's data), then read another 256 MB so the
-        # written lines leave L2 before the step: their write-back would
-        # otherwise take DRAM bandwidth inside the next timed step.
-        flush_w.fill_(i & 0xFF)
-        torch.sum(flush_r, dim=(0,), out=flush_sink)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            layer.forward(inp["hidden"], inp["logits"], out=out, counts=counts, stream=stream)
-    st = moe.device_status(layer.workspace(T), stream)
-    if st != moe.MOE_OK:
-        raise RuntimeError(moe.status_string(st))
-    work = algorithmic_work(cfg, counts.cpu().tolist(),
-                            wbytes=1.0 + 1.0 / 32 if mx else (0.5 + 1.0 / 16 if nv else 2.0))
-    if args.router:  # W_router read and x . W_router^T computed instead of logits read
-        work["flops"] += 2.0 * T * cfg.E * cfg.H
-        work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * T * cfg.E
-    gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
-    if mx or nv:
-        n_launch = n_separate = moe.launch_count_quantized(layer.dims(T))
-    else:
-        count = moe.launch_count_router if args.router else moe.launch_count
-        n_launch = count(layer.dims(T))
-        with moe.expert_fusion(False):
-            n_separate = count(layer.dims(T))
-    fused = n_launch < n_separate  # the fused expert launch ran (bf16, --fusion, decode-sized)
-    if fused:
-        # gate_up and down run as one launch (stage 3 of the per-kernel events)
-        gu_kernel = "moe_expert_fused"
-        work["gate_up_bytes"] += work["down_bytes"]
-        work["gate_up_flops"] += work["down_flops"]
-
     K = args.steps
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
-                for _ in range(K)]
-    # torch creates CUDA events lazily; record each once so the handles exist.
-    with torch.cuda.stream(stream):
-        for evs in stage_ev:
-            for e in evs:
-                e.record(stream)
-    torch.cuda.synchronize(dev)
-
-    # Timed region: K steps, each bracketed by events on the launching stream.
-    sampler = ClockSampler(dev.index)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    sampler.start()
-    wall0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            flush_l2(i)
-            step_ev[i][0].record(stream)
-            layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
-            step_ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
-    if dist is not None:
-        dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    total_ms = sum(step_ms)
-
-    # Per-kernel pass: the library records events around each of its kernels
-    # on the same stream (this serialises the kernels, so it is a separate
-    # pass of K steps and not part of the step timing above).
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            flush_l2(i)
-            moe.set_stage_events(stage_ev[i])
-            layer.forward(inp["hidden"], inp["logits"], out=out, stream=stream)
-    moe.set_stage_events(None)
-    torch.cuda.synchronize(dev)
-    st = moe.device_status(layer.workspace(T), stream)
-    if st != moe.MOE_OK:
-        raise RuntimeError(moe.status_string(st))
-    stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev]
-                for j in range(moe.NUM_STAGES)]
+    stream = torch.cuda.Stream(dev)
+    flush = L2Flush(dev)
+    m = measure(args, cfg, dev, layer, inp, stream, flush, K, sampler=ClockSampler(dev.index),
+                dist=dist)
+    out = m["out"]
+    total_ms = sum(m["step_ms"])
     if dist is not None:
         total_ms = max_over_ranks(total_ms, dist, dev)
+    work, gu_kernel = work_of(args, cfg, m)
 
     # The same step replayed as a CUDA graph (launch overhead removed).
     graph = None
@@ -423,13 +531,14 @@ def main():
                 for _ in range(K)]
         with torch.cuda.stream(stream):
             for i in range(K):
-                flush_l2(i)
+                flush(i)
                 g_ev[i][0].record(stream)
                 g.replay()
                 g_ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
         g_ms = sum(a.elapsed_time(b) for a, b in g_ev) / K
         graph = dict(ms_per_step=g_ms, value=T / (g_ms / 1e3), unit="tokens/s")
+        del g
     except Exception as exc:  # capture unsupported here: report, do not fail the bench
         graph = dict(error=str(exc)[:200])
 
@@ -448,7 +557,7 @@ def main():
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush_l2(i)
+            flush(i)
             e2e_ev[i][0].record(stream)
             layer.forward_from_host(h_host, l_host, o_host, stream=stream)
             e2e_ev[i][1].record(stream)
@@ -470,6 +579,7 @@ def main():
     p1.record(pipe.xs)
     pipe.drain()
     e2e_ms = p0.elapsed_time(p1)
+    del pipe
 
     if rank != 0:
         if dist is not None:
@@ -479,31 +589,9 @@ def main():
     peaks = load_peaks()
     value = job_tokens_per_s(world, T, K, total_ms)
     ms_step = total_ms / K
-    gu_ms = statistics.mean(stage_ms[3])
-    dn_ms = statistics.mean(stage_ms[4])
-    hbm_bound = work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (
-        peaks["bf16_tflops_sustained"] * 1e12)
-    if hbm_bound:
-        achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
-        roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
-                    frac=achieved / peaks["hbm_gbs"],
-                    traffic=read_traffic(gu_kernel, cfg.name),
-                    kernel=f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if fused else ""),
-                    peak_source=peaks["source"])
-    else:
-        achieved = work["gate_up_flops"] / (gu_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
-                    frac=achieved / peak, traffic=read_traffic(gu_kernel, cfg.name),
-                    kernel=f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if fused else ""),
-                    peak_source=peaks["source"])
-    t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9),
-                 work["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
-    layer_roof = dict(bound="hbm" if hbm_bound else "tensor", roofline_ms=t_roof * 1e3,
-                      frac=t_roof * 1e3 / ms_step, bytes=work["bytes"], flops=work["flops"],
-                      experts_touched=work["touched"],
-                      frac_vs_nominal_8tbs=(work["bytes"] / 8e12 * 1e3) / ms_step)
-    kernels = {n: round(statistics.mean(v) * 1e3, 2) for n, v in zip(moe.STAGE_NAMES, stage_ms)}
+    roof, layer_roof = rooflines(cfg, work, m, peaks, gu_kernel)
+    layer_roof["frac"] = layer_roof["roofline_ms"] / ms_step  # the slowest rank's time
+    dn_ms = statistics.mean(m["stage_ms"][4])
     h2d = T * cfg.H * 2 + (0 if args.router else T * cfg.E * 4)
     d2h = T * cfg.H * 2
     line = dict(
@@ -519,17 +607,18 @@ def main():
                     parallelism="replicas" if world > 1 else "1gpu",
                     l2="flushed between timed steps: 256 MB write, then 256 MB read of a "
                        "second buffer (no dirty lines left)", launch="stream",
-                    experts="one fused gate_up + down launch" if fused else "gate_up and down launches",
-                    wall_s=round(wall, 3)),
-        roofline=roof, layer_roofline=layer_roof, kernel_us=kernels,
+                    experts=("one fused gate_up + down launch" if m["fused"]
+                             else "gate_up and down launches"),
+                    wall_s=round(m["wall"], 3)),
+        roofline=roof, layer_roofline=layer_roof, kernel_us=kernel_us(m),
         kernel_timing="separate pass of K steps with library-recorded events around each kernel",
-        down_gbs=None if fused else work["down_bytes"] / (dn_ms / 1e3) / 1e9,
+        down_gbs=None if m["fused"] else work["down_bytes"] / (dn_ms / 1e3) / 1e9,
         e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h,
                  mode="serving loop (moe.HostPipeline): transfers overlap neighbouring steps' compute",
                  serial_value=world * T * K / (e2e_serial_ms / 1e3)),
-        gpu_launches=n_launch * K,
-        clocks=clocks, cuda_graph=graph)
+        gpu_launches=m["n_launch"] * K,
+        clocks=m["clocks"], cuda_graph=graph)
     if world == 1 and not args.no_cpu_baseline:
         inp_cpu = {n: t.cpu() for n, t in inp.items() if t is not None}
         if mx or nv:
@@ -541,6 +630,23 @@ def main():
                 bits = deq(oracle._np(inp_cpu.pop(n + "_q")), oracle._np(inp_cpu.pop(n + "_s")))
                 inp_cpu[n] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
         line["cpu_baseline"] = time_cpu_baseline(cfg, inp_cpu, router=args.router)
+        del inp_cpu
+    del inp, layer, m, out
+    torch.cuda.empty_cache()
+    others = [n for n in PER_CONFIG if n != cfg.name]
+    if world == 1 and not args.no_per_config and others:
+        line["per_config"] = measure_per_config(args, dev, stream, flush, peaks, others)
+        line["per_config_timing"] = ("same step timing, L2 flush and per-kernel pass as the "
+                                     "headline, K steps each, after the headline's timed region")
+    if world == 1 and not args.no_cpu_baseline and not (mx or nv or args.router):
+        # the oracle on one host core, on the decode workload
+        dcfg = wl.CONFIGS["decode"]
+        d_cpu = wl.make_inputs(dcfg, seed=0, device=str(dev))
+        d_cpu = {n: t.cpu() for n, t in d_cpu.items()}
+        line["cpu_baseline"]["single_core"] = dict(
+            workload=workload_name(dcfg),
+            **time_cpu_baseline(dcfg, d_cpu, budget_s=8.0, threads=1))
+        del d_cpu
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

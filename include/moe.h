@@ -329,12 +329,15 @@ moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream);
  * MOE_STATIC_HIST_WORDS int32 words (1 MiB) plus a 256-byte header; every
  * GPU that loads the library holds it until the process exits. Sizes with
  * ceil(T / 256) * E > MOE_STATIC_HIST_WORDS return MOE_ERR_CAPACITY (for
- * E = 256: T <= 262144). The call allocates no memory and calls no
- * allocating library routine. The first call on each device looks up the
- * array's device address (with that device current); make that first call
- * before any stream capture. All calls share the array: calls that overlap
- * on the GPU race and give wrong counts. Enqueued on cuda_stream without a
- * host synchronisation.
+ * E = 256: T <= 262144). Limits as for moe_forward otherwise: 1 <= k <= 32,
+ * k <= E <= 1024 (else MOE_ERR_INVALID_ARG), so T * k stays below 2^27. The
+ * call allocates no memory and calls no allocating library routine. Every
+ * call looks up the array's device address in the current device's context
+ * (so the address stays valid after a cudaDeviceReset); the first call on a
+ * device may also load the library's device code there, so make it before
+ * any stream capture. All calls share the array: calls that overlap on the
+ * GPU race and give wrong counts. Enqueued on cuda_stream without a host
+ * synchronisation.
  */
 #define MOE_STATIC_HIST_WORDS (1 << 18)
 moe_status moe_expert_counts_static(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,

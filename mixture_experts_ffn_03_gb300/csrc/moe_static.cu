@@ -13,8 +13,6 @@
 // library holds it (1 MiB + 256 bytes) until the process exits. All calls
 // share it, so calls that overlap on the GPU (different streams, or the same
 // scratch used from several host threads without ordering) race on it.
-#include <mutex>
-
 #include "moe.h"
 #include "moe_internal.cuh"
 
@@ -26,25 +24,15 @@ namespace {
 constexpr int kTicketWords = 64;  // word 0: completion ticket; rest padding
 static __device__ __align__(256) int g_static_scratch[kTicketWords + MOE_STATIC_HIST_WORDS];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-int* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of g_static_scratch on the current device, looked up once
-// per device (host code must not use the symbol's name as an address).
+// Device address of g_static_scratch in the current device's context. Host
+// code must not use the symbol's name as an address. The address is looked
+// up on every call (a cheap runtime query) rather than cached, so it stays
+// right after the context is destroyed and recreated (cudaDeviceReset).
 cudaError_t scratch_address(int** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<int*>(p);
-    }
-    *out = g_scratch_addr[dev];
+    *out = static_cast<int*>(p);
     return cudaSuccess;
 }
 
@@ -122,7 +110,8 @@ using namespace moe;
 MOE_API moe_status moe_expert_counts_static(const int32_t* topk_ids, int32_t T, int32_t k,
                                             int32_t E, int32_t* counts_out,
                                             int32_t* offsets_out, void* cuda_stream) {
-    if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024 || !counts_out) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024 || k > E || !counts_out)
+        return MOE_ERR_INVALID_ARG;
     if (T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
     const long blocks = (static_cast<long>(T) + kCountTokens - 1) / kCountTokens;
     if (blocks * E > MOE_STATIC_HIST_WORDS) return MOE_ERR_CAPACITY;

@@ -111,7 +111,7 @@ def test_mx_small_cases(moe, cfg):
     run_mx_case(moe, cfg, wl.make_inputs_mxfp8(cfg, seed=0))
 
 
-@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", 32)])
+@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", None)])
 def test_mx_full_size(moe, name, n_check):
     cfg = wl.CONFIGS[name]
     inp = wl.make_inputs_mxfp8(cfg, seed=0, device="cuda")

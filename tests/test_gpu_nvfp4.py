@@ -100,7 +100,7 @@ def test_nv_small_cases(moe, cfg):
     run_nv_case(moe, cfg, wl.make_inputs_nvfp4(cfg, seed=0))
 
 
-@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", 32)])
+@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", None)])
 def test_nv_full_size(moe, name, n_check):
     cfg = wl.CONFIGS[name]
     run_nv_case(moe, cfg, wl.make_inputs_nvfp4(cfg, seed=0, device="cuda"), n_check)

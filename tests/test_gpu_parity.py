@@ -3,8 +3,8 @@
 Bar: expert ids, per-expert counts, offsets and the sorted slot order are
 bit-exact; every checked output element satisfies
 |gpu - oracle| <= 1e-2 |oracle| + 1e-3 RMS(oracle), RMS over the checked rows.
-Small cases check every token; the full-size workloads check every token's
-routing and a sample of tokens' outputs (the oracle evaluates tokens one by one).
+Every case checks every token, the full-size workloads included (the oracle
+takes a few seconds each on the host cores).
 """
 from __future__ import annotations
 
@@ -171,12 +171,42 @@ def test_deterministic_repeat(moe):
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", 48), ("wide", 24),
-                                          ("skewed", 48)])
-def test_full_size_workloads(moe, name, n_check):
+@pytest.mark.parametrize("name", ["decode", "prefill", "wide", "skewed"])
+def test_full_size_workloads(moe, name):
+    """Every token of every workload at its full size: all row-tile widths,
+    the ragged last tile of every expert, empty experts next to hot ones."""
     cfg = wl.CONFIGS[name]
     inp = wl.make_inputs(cfg, seed=0, device="cuda")
-    run_case(moe, cfg, inp, n_check)
+    run_case(moe, cfg, inp)
+
+
+# Large magnitudes. Gate pre-activations spread over about +-100 (weights
+# N(0, 2.5) on N(0, 1) hidden rows of width 256): SiLU saturates at both ends,
+# 1 + exp(-g) overflows fp32 for g < -88.7 and exceeds 2^126 just above it.
+# Scaling W_down and Ws_down by 2^+-100 (exact in bf16) moves every expert
+# output and the layer output to ~1e30 or ~1e-30 with the same relative
+# rounding, through the fp32 and the 24-bit y paths (large groups: 128-token
+# down tiles; small groups: fp32 y).
+MAGNITUDE_CASES = [
+    ("saturating_small_groups", 60, 16, 4, 1.0),
+    ("saturating_large_groups", 640, 8, 2, 1.0),
+    ("huge_outputs", 640, 8, 2, 2.0 ** 100),
+    ("tiny_outputs", 60, 16, 4, 2.0 ** -100),
+]
+
+
+@pytest.mark.parametrize("name,T,E,k,down_scale", MAGNITUDE_CASES, ids=lambda v: str(v))
+def test_large_magnitudes(moe, name, T, E, k, down_scale):
+    cfg = wl.MoEConfig(name, T=T, H=256, E=E, k=k, I=128, I_s=128, score_fn=wl.SOFTMAX)
+    inp = wl.make_inputs(cfg, seed=9)
+    g = torch.Generator().manual_seed(19)
+    for n in ("w_gate_up", "ws_gate_up"):
+        inp[n] = (torch.randn(inp[n].shape, generator=g) * 2.5).to(torch.bfloat16)
+    for n in ("w_down", "ws_down"):
+        inp[n] = (torch.randn(inp[n].shape, generator=g) * 2.5 * down_scale).to(torch.bfloat16)
+    pre = inp["hidden"][:, None, :].float() @ inp["w_gate_up"][:, :cfg.I, :].float().transpose(1, 2)
+    assert float(pre.max()) > 60 and float(pre.min()) < -88.8   # both saturation ranges occur
+    run_case(moe, cfg, inp)
 
 
 def test_single_expert(moe):

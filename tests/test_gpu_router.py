@@ -94,7 +94,7 @@ def test_router_small_cases(moe, cfg):
     check_router_case(moe, cfg, wl.make_inputs_router(cfg, seed=0))
 
 
-@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", 32), ("wide", 16)])
+@pytest.mark.parametrize("name,n_check", [("decode", None), ("prefill", None), ("wide", None)])
 def test_router_full_size(moe, name, n_check):
     cfg = wl.CONFIGS[name]
     check_router_case(moe, cfg, wl.make_inputs_router(cfg, seed=0, device="cuda"), n_check)

@@ -2,9 +2,11 @@
 
 It serves callers that cannot allocate device memory (no workspace can be
 passed to them, or cudaMalloc is not allowed where they run); its scratch is
-a fixed array inside the library. These tests call it through the C ABI and
-compare it with moe_forward's own per-expert counts and offsets for the same
-routing, on consecutive calls that share the fixed scratch.
+a fixed array inside the library. These tests call it through the C ABI on
+consecutive calls that share the fixed scratch, and compare it with
+moe_forward's own per-expert counts and offsets for the same routing and
+with a numpy histogram of the ids (computed on the host, independent of
+the GPU code).
 """
 from __future__ import annotations
 
@@ -50,6 +52,11 @@ def test_rejects_oversize_and_bad_args_on_host(lib):
     assert f(fake, 16, 0, 16, fake, None, None) == MOE_ERR_INVALID_ARG
     assert f(fake, 16, 4, 2048, fake, None, None) == MOE_ERR_INVALID_ARG
     assert f(fake, 16, 4, 16, None, None, None) == MOE_ERR_INVALID_ARG
+    # more experts per token than experts, and E = 1 with k = 32 (which would
+    # otherwise let T * k reach 2^31 within the scratch capacity)
+    assert f(fake, 16, 5, 4, fake, None, None) == MOE_ERR_INVALID_ARG
+    assert f(fake, 1 << 26, 32, 1, fake, None, None) == MOE_ERR_INVALID_ARG
+    assert f(fake, 16, 33, 64, fake, None, None) == MOE_ERR_INVALID_ARG
 
 
 def reference_routing(moe, cfg, seed):
@@ -67,24 +74,41 @@ def reference_routing(moe, cfg, seed):
     return ids, counts, offsets
 
 
+def host_counts(ids, E):
+    """Counts and exclusive offsets of a [T, k] id table, by numpy on the host."""
+    c = np.bincount(ids.cpu().numpy().ravel(), minlength=E).astype(np.int32)
+    return c, np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+
+
 @pytest.mark.gpu
 def test_static_counts_match_moe_forward_on_consecutive_calls(lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import mixture_experts_ffn_03_gb300 as moe
     stream = torch.cuda.current_stream()
-    cases = [wl.CONFIGS["tiny"], wl.CONFIGS["skewed"].with_tokens(2048)]
+    cases = [
+        wl.CONFIGS["tiny"],
+        wl.CONFIGS["skewed"].with_tokens(2048),
+        # four experts per thread in the last block's scan (E = 1024), k = 32
+        wl.MoEConfig("e1024_k32", T=700, H=64, E=1024, k=32, I=64, I_s=64, score_fn=wl.SOFTMAX),
+        # E not a multiple of 256: two experts per thread, the last thread partly idle
+        wl.MoEConfig("e300", T=1000, H=64, E=300, k=6, I=64, I_s=64, score_fn=wl.SIGMOID),
+    ]
     for cfg in cases:
         ids, counts_ref, offsets_ref = reference_routing(moe, cfg, seed=3)
+        c_host, o_host = host_counts(ids, cfg.E)
+        assert np.array_equal(counts_ref.cpu().numpy(), c_host)
+        assert np.array_equal(offsets_ref.cpu().numpy(), o_host)
         for _ in range(2):  # two calls in a row share the fixed scratch
             counts = torch.full((cfg.E,), -7, dtype=torch.int32, device="cuda")
             offsets = torch.full((cfg.E + 1,), -7, dtype=torch.int32, device="cuda")
             st = call_static(lib, ids, cfg.T, cfg.k, cfg.E, counts, offsets, stream)
             assert st == MOE_OK, moe.status_string(st)
             torch.cuda.synchronize()
+            assert np.array_equal(counts.cpu().numpy(), c_host), cfg.name
+            assert np.array_equal(offsets.cpu().numpy(), o_host), cfg.name
             assert torch.equal(counts, counts_ref)
             assert torch.equal(offsets, offsets_ref)
-            assert int(counts.sum()) == cfg.T * cfg.k
     # Zero tokens: all counts and offsets are zero.
     counts = torch.full((16,), -7, dtype=torch.int32, device="cuda")
     offsets = torch.full((17,), -7, dtype=torch.int32, device="cuda")
