@@ -390,7 +390,7 @@ def work_of(args, cfg, m):
         work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * cfg.T * cfg.E
     gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
     if m["fused"]:
-        # gate_up and down run as one launch (stage 3 of the per-kernel events)
+        # gate_up and down run as one launch (the gate_up stage of the per-kernel events)
         gu_kernel = "moe_expert_fused"
         work["gate_up_bytes"] += work["down_bytes"]
         work["gate_up_flops"] += work["down_flops"]
@@ -401,7 +401,7 @@ def rooflines(cfg, work, m, peaks, gu_kernel):
     """`roofline` of the dominant kernel (gate_up, or the fused expert launch)
     and `layer_roofline` of the whole step."""
     ms_step = sum(m["step_ms"]) / len(m["step_ms"])
-    gu_ms = statistics.mean(m["stage_ms"][3])
+    gu_ms = statistics.mean(m["stage_ms"][2])
     hbm_bound = work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (
         peaks["bf16_tflops_sustained"] * 1e12)
     kname = f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if m["fused"] else "")
@@ -591,7 +591,7 @@ def main():
     ms_step = total_ms / K
     roof, layer_roof = rooflines(cfg, work, m, peaks, gu_kernel)
     layer_roof["frac"] = layer_roof["roofline_ms"] / ms_step  # the slowest rank's time
-    dn_ms = statistics.mean(m["stage_ms"][4])
+    dn_ms = statistics.mean(m["stage_ms"][3])
     h2d = T * cfg.H * 2 + (0 if args.router else T * cfg.E * 4)
     d2h = T * cfg.H * 2
     line = dict(

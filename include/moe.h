@@ -255,12 +255,13 @@ typedef struct {
 
 moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layout);
 
-/* Stages of one moe_forward, each at most one kernel (route, count/scan,
- * scatter, gate_up GEMM, down GEMM, combine). Stages that a smaller batch
- * merges into the one before are empty: routing and the permute share one
- * launch when T*k <= 2048, and the fused expert launch (moe_set_expert_fusion,
- * when enabled) runs in the gate_up stage, leaving the down stage empty. */
-#define MOE_NUM_STAGES 6
+/* Stages of one moe_forward, each at most one kernel: routing (with the
+ * per-expert histograms and their scan when T*k > 2048; the whole permute
+ * when T*k <= 2048), scatter, gate_up GEMM, down GEMM, combine. A stage that
+ * a batch merges into the one before is empty: the scatter stage when
+ * T*k <= 2048, and the down stage when the fused expert launch
+ * (moe_set_expert_fusion, when enabled) runs in the gate_up stage. */
+#define MOE_NUM_STAGES 5
 
 /* Optional per-kernel timing. `events` points to MOE_NUM_STAGES + 1
  * cudaEvent_t handles (passed as void*) created by the caller; while set,
@@ -273,7 +274,7 @@ moe_status moe_set_stage_events(void* const* events, int n_events);
 
 /* Number of kernels one moe_forward with these sizes launches from the
  * calling host thread, or 0 for invalid sizes or T = 0: routing (1 launch
- * when T*k <= 2048, else 3), the expert GEMMs (1 launch when they run fused,
+ * when T*k <= 2048, else 2), the expert GEMMs (1 launch when they run fused,
  * else 2) and the combine. */
 int moe_launch_count(const moe_dims* d);
 

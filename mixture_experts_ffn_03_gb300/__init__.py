@@ -33,8 +33,8 @@ EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_statu
             "moe_forward_router", "moe_workspace_size_router", "moe_launch_count_router",
             "moe_forward_nvfp4", "moe_nvfp4_dequant", "moe_launch_count_quantized",
             "moe_set_expert_fusion", "moe_get_expert_fusion"]
-NUM_STAGES = 6
-STAGE_NAMES = ["route", "count_scan", "scatter", "gate_up", "down", "combine"]
+NUM_STAGES = 5
+STAGE_NAMES = ["route", "scatter", "gate_up", "down", "combine"]
 
 
 class MoEDims(ctypes.Structure):

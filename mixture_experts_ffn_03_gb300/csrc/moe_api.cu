@@ -1,6 +1,6 @@
 // C ABI of libmoe: argument checks, workspace carving, TMA descriptors and
-// the launch sequence route -> count/scan -> scatter -> gate_up -> down ->
-// combine on the caller's stream. See include/moe.h for the contract.
+// the launch sequence route (+ histogram/scan) -> scatter -> gate_up -> down
+// -> combine on the caller's stream. See include/moe.h for the contract.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -53,8 +53,12 @@ Layout layout_of(const moe_dims& d) {
     };
     const size_t T = d.T, H = d.H, E = d.E, I = d.I, Is = d.I_s, tk = T * d.k;
     const size_t nb = (T + kCountTokens - 1) / kCountTokens;
+    // The status block, the large-batch routing's block histograms and the
+    // fused launch's readiness counters are adjacent: one memset clears what
+    // a call needs of them.
     L.meta = take(META_WORDS * sizeof(int));
-    L.ready = take((tk + T) * 4);  // right after the status block: one memset clears both
+    L.blockhist = take(nb * E * 4);
+    L.ready = take((tk + T) * 4);
     L.topk_ids = take(tk * 4);
     L.topk_w = take(tk * 4);
     L.gate_logit = take(T * 4);
@@ -62,7 +66,6 @@ Layout layout_of(const moe_dims& d) {
     L.offsets = take((E + 1) * 4);
     L.perm = take(tk * 4);
     L.inv = take(tk * 4);
-    L.blockhist = take(nb * E * 4);
     L.rt_gu = take(max_row_tiles(tk, E, 16) * sizeof(int4));
     L.rt_dn = take(max_row_tiles(tk, E, 16) * sizeof(int4));
     L.h_hi = take(tk * I * 2);
@@ -232,11 +235,11 @@ BnPlan bn_plan(size_t tk, int E, bool mx) {
     return p;
 }
 
-// Kernels one forward launches: routing (one launch, or route + count/scan +
-// scatter), the expert GEMMs (one fused launch or two), the combine.
+// Kernels one forward launches: routing (one launch, or route with the block
+// histograms + scatter), the expert GEMMs (one fused launch or two), the combine.
 int launches_of(const moe_dims& d, bool mx) {
     const size_t tk = static_cast<size_t>(d.T) * d.k;
-    return (route_small_fits(d.T, d.E, d.k) ? 1 : 3) + (bn_plan(tk, d.E, mx).fused ? 1 : 2) + 1;
+    return (route_small_fits(d.T, d.E, d.k) ? 1 : 2) + (bn_plan(tk, d.E, mx).fused ? 1 : 2) + 1;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -514,9 +517,15 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     const int tiles_dn = static_cast<int>(max_dn < cap ? max_dn : cap);
 
     // Status words (error flags, tile counts, completion ticket) start at zero,
-    // and so do the fused launch's row-tile readiness counters that follow them.
-    const size_t zero_bytes = plan.fused ? L.ready - L.meta + (tk + T) * sizeof(int)
-                                         : META_WORDS * sizeof(int);
+    // and so do the large-batch routing's block histograms and the fused
+    // launch's row-tile readiness counters that follow them.
+    const bool small_route = route_small_fits(T, E, k);
+    const size_t zero_bytes =
+        plan.fused ? L.ready - L.meta + (tk + T) * sizeof(int)
+                   : (small_route ? META_WORDS * sizeof(int)
+                                  : L.blockhist - L.meta +
+                                        static_cast<size_t>((T + kCountTokens - 1) / kCountTokens) *
+                                            E * sizeof(int));
     if (cudaMemsetAsync(meta, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(0, st);
     LogitSrc lsrc{router_logits, 1, 0, nullptr};
@@ -534,8 +543,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         lsrc = LogitSrc{partial, rp.splits, static_cast<size_t>(T) * E, logits_out};
     }
     const bool route_pdl = w_router != nullptr;
-    if (route_small_fits(T, E, k)) {
-        // Routing and the whole permute in one launch; stages 1 and 2 are empty.
+    if (small_route) {
+        // Routing and the whole permute in one launch; stage 1 is empty.
         if ((launch_route_permute(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, route_pdl,
                                   static_cast<const __nv_bfloat16*>(hidden),
                                   static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w,
@@ -543,45 +552,43 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
                                   topk_ids_out, topk_w_out, expert_counts_out, st)) != cudaSuccess)
             return MOE_ERR_CUDA;
         mark_stage(1, st);
-        mark_stage(2, st);
     } else {
-        if ((launch_route(T, H, E, k, d->score_fn, lsrc, route_pdl,
-                          static_cast<const __nv_bfloat16*>(hidden),
-                          static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w, gate_logit,
-                          topk_ids_out, topk_w_out, st)) != cudaSuccess)
+        // Routing with the block histograms and their scan in one launch, then
+        // the scatter (stage 1).
+        if ((launch_route_count(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, route_pdl,
+                                static_cast<const __nv_bfloat16*>(hidden),
+                                static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w,
+                                gate_logit, blockhist, counts, offsets, rt_gu, rt_dn, meta,
+                                topk_ids_out, topk_w_out, expert_counts_out, st)) != cudaSuccess)
             return MOE_ERR_CUDA;
         mark_stage(1, st);
-        if ((launch_count_scan(T, E, k, bn_gu, bn_dn, topk_ids, blockhist, counts, offsets, rt_gu,
-                               rt_dn, meta, expert_counts_out, st)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        mark_stage(2, st);
         if ((launch_scatter(T, E, k, topk_ids, blockhist, offsets, perm, inv, st)) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    mark_stage(3, st);
+    mark_stage(2, st);
     if (plan.fused) {
-        // gate_up and down in one launch; its time is stage 4's, stage 5 is empty.
+        // gate_up and down in one launch; its time is stage 2's, stage 3 is empty.
         int* ready = reinterpret_cast<int*>(ws + L.ready);
         const int tiles = tiles_gu > cap - tiles_dn ? cap : tiles_gu + tiles_dn;
         if (launch_expert_fused(bn_gu, gu, dn, ga, ready, tiles, num_sms, st) != cudaSuccess)
             return MOE_ERR_CUDA;
+        mark_stage(3, st);
         mark_stage(4, st);
-        mark_stage(5, st);
     } else {
         const cudaError_t e_gu = W.mx ? launch_gate_up_mx(bn_gu, W.nv, mgu, ga, tiles_gu, num_sms, st)
                                       : launch_gate_up(bn_gu, gu, ga, tiles_gu, num_sms, st);
         if (e_gu != cudaSuccess) return MOE_ERR_CUDA;
-        mark_stage(4, st);
+        mark_stage(3, st);
         const cudaError_t e_dn = W.mx ? launch_down_mx(bn_dn, W.nv, mdn, gd, tiles_dn, num_sms, st)
                                       : launch_down(bn_dn, dn, gd, tiles_dn, num_sms, st);
         if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
-        mark_stage(5, st);
+        mark_stage(4, st);
     }
     // 128-token down tiles leave y as 24-bit floats, the other widths as fp32.
     if ((launch_combine(T, H, k, y, !W.mx && bn_dn == 128, topk_w, inv,
                         static_cast<__nv_bfloat16*>(out), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
-    mark_stage(6, st);
+    mark_stage(5, st);
     return MOE_OK;
 }
 

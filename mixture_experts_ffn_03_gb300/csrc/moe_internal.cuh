@@ -41,7 +41,7 @@ enum : int {
     META_ERR = 0,          // device error flags
     META_RT_GU = 1,        // routed row tiles of the gate_up GEMM
     META_RT_DN = 2,        // routed row tiles of the down GEMM
-    META_TICKET = 3,       // block-completion counter of the count/scan kernel
+    META_TICKET = 3,       // block-completion counter of the routing launch
     META_SCHED_GU = 4,     // tiles claimed by the gate_up GEMM's CTAs (past their first)
     META_SCHED_DN = 5,     // tiles claimed by the down GEMM's CTAs
     META_WORDS = 64,
@@ -76,13 +76,15 @@ cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int b
                                  float* gate_logit, int* counts, int* offsets, int* perm,
                                  int* inv, int4* rt_gu, int4* rt_dn, int* meta, int* ids_out,
                                  float* w_out, int* counts_out, cudaStream_t st);
-cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const LogitSrc& logits, bool pdl,
-                         const __nv_bfloat16* hidden, const __nv_bfloat16* w_g, int* topk_ids,
-                         float* topk_w, float* gate_logit, int* ids_out, float* w_out,
-                         cudaStream_t st);
-cudaError_t launch_count_scan(int T, int E, int k, int bn_gu, int bn_dn, const int* topk_ids,
-                              int* blockhist, int* counts, int* offsets, int4* rt_gu,
-                              int4* rt_dn, int* meta, int* counts_out, cudaStream_t st);
+// Large batches: routing plus per-block expert histograms (blockhist, zero
+// at launch), scanned by the last CTA into counts, offsets, row tiles and
+// per-block bases; then the stable scatter of the slots.
+cudaError_t launch_route_count(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                               const LogitSrc& logits, bool pdl, const __nv_bfloat16* hidden,
+                               const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
+                               float* gate_logit, int* blockhist, int* counts, int* offsets,
+                               int4* rt_gu, int4* rt_dn, int* meta, int* ids_out, float* w_out,
+                               int* counts_out, cudaStream_t st);
 cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
                            const int* offsets, int* perm, int* inv, cudaStream_t st);
 cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,

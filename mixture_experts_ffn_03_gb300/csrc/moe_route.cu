@@ -18,8 +18,8 @@
 // Routing runs one warp per token. Batches with T*k <= kSmallSlots then
 // permute inside the same launch: the last CTA to finish routing (a completion
 // ticket) builds the whole sorted order (route_permute_kernel). Larger batches
-// use route_kernel, count_scan_kernel (per-block histograms; the last block
-// scans) and scatter_kernel.
+// take two launches: route_count_kernel (routing plus per-block expert
+// histograms; the last CTA scans them) and scatter_kernel.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -221,8 +221,9 @@ __device__ __forceinline__ void ordered_scatter(const int* ids, long a0, long a1
 }
 
 // Routing of one token per warp; writes ids, weights and the gate logit.
+// Lane j < k returns the token's j-th selected expert.
 template <int EPL>
-__device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int score_fn,
+__device__ __forceinline__ int route_and_store(int t, int H, int E, int k, int score_fn,
                                                 const LogitSrc& logits,
                                                 const __nv_bfloat16* __restrict__ hidden,
                                                 const __nv_bfloat16* __restrict__ w_g,
@@ -271,6 +272,7 @@ __device__ __forceinline__ void route_and_store(int t, int H, int E, int k, int 
         if (ids_out) ids_out[o] = my_e;
         if (w_out) w_out[o] = my_w;
     }
+    return my_e;
 }
 
 // ------------------------------------------------------------ small batches
@@ -366,50 +368,19 @@ route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn
 }
 
 // ------------------------------------------------------------ large batches
-template <int EPL>
-__global__ void __launch_bounds__(kRouteWarps * 32)
-route_kernel(int T, int H, int E, int k, int score_fn, const LogitSrc logits,
-             const __nv_bfloat16* __restrict__ hidden, const __nv_bfloat16* __restrict__ w_g,
-             int* __restrict__ topk_ids, float* __restrict__ topk_w,
-             float* __restrict__ gate_logit, int* __restrict__ ids_out,
-             float* __restrict__ w_out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ptx::griddep_launch_dependents();
-    ptx::griddep_wait();  // no-op unless launched behind the router GEMM
-    const int t = blockIdx.x * kRouteWarps + warp;
-    if (t >= T) return;
-    route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w, gate_logit,
-                         ids_out, w_out, lane);
-}
-
-__global__ void __launch_bounds__(256)
-count_scan_kernel(int T, int E, int k, int bn_gu, int bn_dn, const int* __restrict__ topk_ids,
-                  int* __restrict__ blockhist, int* __restrict__ counts,
-                  int* __restrict__ offsets, int4* __restrict__ rt_gu, int4* __restrict__ rt_dn,
-                  int* __restrict__ meta, int* __restrict__ counts_out) {
-    extern __shared__ int s_hist[];  // [E]
-    __shared__ int s_warp[8];
-    __shared__ int s_is_last;
+// Last CTA of the large-batch routing launch: every block histogram
+// blockhist[b][e] (slots of expert e among tokens [256 b, 256 b + 256)) is
+// complete. Thread tid owns the experts [tid*ept, tid*ept + ept), so expert
+// order is thread order: counts, exclusive offsets, both GEMMs' row tiles,
+// and each block's base inside each expert (written over its histogram).
+// Called by all 256 threads of the CTA.
+__device__ __forceinline__ void scan_block_hist(int nb, int E, int bn_gu, int bn_dn,
+                                                int* __restrict__ blockhist,
+                                                int* __restrict__ counts,
+                                                int* __restrict__ offsets, int4* __restrict__ rt_gu,
+                                                int4* __restrict__ rt_dn, int* __restrict__ meta,
+                                                int* __restrict__ counts_out, int* s_warp) {
     const int tid = threadIdx.x;
-    ptx::griddep_launch_dependents();
-    for (int e = tid; e < E; e += 256) s_hist[e] = 0;
-    __syncthreads();
-    ptx::griddep_wait();
-    const long a0 = static_cast<long>(blockIdx.x) * kCountTokens * k;
-    const long a1 = min(static_cast<long>(T) * k, a0 + static_cast<long>(kCountTokens) * k);
-    for (long a = a0 + tid; a < a1; a += 256) atomicAdd(&s_hist[topk_ids[a]], 1);
-    __syncthreads();
-    for (int e = tid; e < E; e += 256) blockhist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_is_last = (atomicAdd(&meta[META_TICKET], 1) == static_cast<int>(gridDim.x) - 1);
-    __syncthreads();
-    if (!s_is_last) return;
-    __threadfence();
-
-    // Last block: every histogram is visible. Thread tid owns the experts
-    // [tid*ept, tid*ept + ept), so expert order is thread order.
-    const int nb = gridDim.x;
     const int ept = (E + 255) / 256;  // <= 4 for E <= 1024
     int local[4] = {0, 0, 0, 0};
     int mine = 0;
@@ -462,6 +433,43 @@ count_scan_kernel(int T, int E, int k, int bn_gu, int bn_dn, const int* __restri
         }
         if (tid == 0) meta[g == 0 ? META_RT_GU : META_RT_DN] = tot_tiles;
     }
+}
+
+// Routing of one token per warp plus the per-expert histogram of each block
+// of 256 tokens, accumulated with integer atomics (the sums do not depend on
+// their order) into blockhist, which starts at zero. The last CTA to finish
+// (a completion ticket) scans the histograms: counts, offsets, row tiles and
+// per-block bases for scatter_kernel.
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                   const LogitSrc logits, const __nv_bfloat16* __restrict__ hidden,
+                   const __nv_bfloat16* __restrict__ w_g, int* __restrict__ topk_ids,
+                   float* __restrict__ topk_w, float* __restrict__ gate_logit,
+                   int* __restrict__ blockhist, int* __restrict__ counts,
+                   int* __restrict__ offsets, int4* __restrict__ rt_gu, int4* __restrict__ rt_dn,
+                   int* __restrict__ meta, int* __restrict__ ids_out, float* __restrict__ w_out,
+                   int* __restrict__ counts_out) {
+    __shared__ int s_warp[kRouteWarps];
+    __shared__ int s_is_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();  // no-op unless launched behind the router GEMM
+    const int t = blockIdx.x * kRouteWarps + warp;
+    if (t < T) {
+        const int e = route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids,
+                                           topk_w, gate_logit, ids_out, w_out, lane);
+        if (lane < k) atomicAdd(&blockhist[static_cast<size_t>(t / kCountTokens) * E + e], 1);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_is_last = (atomicAdd(&meta[META_TICKET], 1) == static_cast<int>(gridDim.x) - 1);
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+    const int nb = (T + kCountTokens - 1) / kCountTokens;
+    scan_block_hist(nb, E, bn_gu, bn_dn, blockhist, counts, offsets, rt_gu, rt_dn, meta,
+                    counts_out, s_warp);
     if (tid == 0) meta[META_TICKET] = 0;
 }
 
@@ -666,26 +674,20 @@ cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int b
 #undef MOE_LAUNCH_RP
 }
 
-cudaError_t launch_route(int T, int H, int E, int k, int score_fn, const LogitSrc& logits, bool pdl,
-                         const __nv_bfloat16* hidden, const __nv_bfloat16* w_g, int* topk_ids,
-                         float* topk_w, float* gate_logit, int* ids_out, float* w_out,
-                         cudaStream_t st) {
+cudaError_t launch_route_count(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                               const LogitSrc& logits, bool pdl, const __nv_bfloat16* hidden,
+                               const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
+                               float* gate_logit, int* blockhist, int* counts, int* offsets,
+                               int4* rt_gu, int4* rt_dn, int* meta, int* ids_out, float* w_out,
+                               int* counts_out, cudaStream_t st) {
     const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
-#define MOE_LAUNCH_R(N)                                                                      \
-    return launch_kernel(route_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), 0, st, pdl,   \
-                         T, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w,         \
-                         gate_logit, ids_out, w_out)
-    MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_R)
-#undef MOE_LAUNCH_R
-}
-
-cudaError_t launch_count_scan(int T, int E, int k, int bn_gu, int bn_dn, const int* topk_ids,
-                              int* blockhist, int* counts, int* offsets, int4* rt_gu,
-                              int4* rt_dn, int* meta, int* counts_out, cudaStream_t st) {
-    const int blocks = (T + kCountTokens - 1) / kCountTokens;
-    return launch_kernel(count_scan_kernel, dim3(blocks), dim3(256), E * sizeof(int), st, true, T,
-                         E, k, bn_gu, bn_dn, topk_ids, blockhist, counts, offsets, rt_gu, rt_dn,
-                         meta, counts_out);
+#define MOE_LAUNCH_RC(N)                                                                        \
+    return launch_kernel(route_count_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), 0, st,  \
+                         pdl, T, H, E, k, score_fn, bn_gu, bn_dn, logits, hidden, w_g,           \
+                         topk_ids, topk_w, gate_logit, blockhist, counts, offsets, rt_gu, rt_dn, \
+                         meta, ids_out, w_out, counts_out)
+    MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_RC)
+#undef MOE_LAUNCH_RC
 }
 
 cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,

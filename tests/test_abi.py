@@ -97,10 +97,10 @@ def test_host_validation(lib):
         assert moe.launch_count(decode) == 3  # one routing launch, fused experts, combine
         assert moe.launch_count_router(decode) == 4
         assert moe.launch_count_quantized(decode) == 4                      # never fused
-        assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 6  # BN 160/128
-        assert moe.launch_count(moe.make_dims(512, 2048, 256, 8, 512, 512, 0)) == 5   # BN 32/32
+        assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 5  # BN 160/128
+        assert moe.launch_count(moe.make_dims(512, 2048, 256, 8, 512, 512, 0)) == 4   # BN 32/32
     assert not moe.get_expert_fusion()
-    assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 6
+    assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 5
     assert moe.launch_count(moe.make_dims(0, 2048, 256, 8, 512, 512, 0)) == 0
     assert moe.launch_count_quantized(moe.make_dims(64, 2048, 256, 8, 192, 512, 1)) == 0
 
