@@ -465,12 +465,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
              make_map(&dn.ws, W.s_down, Is, H, dn_w_rows) &&
              make_pair_map(&dn.h, h_hi, I, tk, L.h_lo - L.h_hi, bn_dn) &&
              make_pair_map(&dn.hs, hs_hi, Is, T, L.hs_lo - L.hs_hi, bn_dn);
-        const CUtensorMapDataType BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-        ok = ok && make_store_map(&gu.st[0], h_hi, BF16, 2, I, tk) &&
-             make_store_map(&gu.st[1], h_lo, BF16, 2, I, tk) &&
-             make_store_map(&gu.st[2], hs_hi, BF16, 2, Is, T) &&
-             make_store_map(&gu.st[3], hs_lo, BF16, 2, Is, T) &&
-             make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
+        ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
              make_y24_store_map(&dn.st[1], y, H, tk + T);
     }
     if (!ok) return MOE_ERR_CUDA;

@@ -26,7 +26,7 @@
 // issues the MMAs, warps 2-3 gather hidden rows with cp.async (gate_up only),
 // warps 4-11 drain TMEM in the epilogue (warp w reads TMEM lanes
 // 32*(w%4)..; two warps per lane quadrant split the columns) and write
-// results through shared memory with TMA stores.
+// results with 16-byte stores (h) or TMA box stores through shared memory (y).
 // Every wait on a pipeline barrier gives up after a time limit, sets an error
 // bit in the workspace status word and lets the CTA finish cleanly.
 #include "gemm_common.cuh"
@@ -46,13 +46,14 @@ struct Cfg {
     static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
     static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : (A_BYTES + 2 * B_BYTES);
     static constexpr int CTL_BYTES = 1024;
-    // Store staging: two buffers per epilogue warp, or one when that buys the
-    // pipeline a fourth stage.
+    // Store staging: gate_up stages each chunk in one buffer per epilogue warp
+    // and writes it with plain stores; down uses TMA stores from two buffers
+    // per warp, or one when that buys the pipeline a fourth stage.
     static constexpr int STAGES_2BUF =
         (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * 2 * kStgBytes) / STAGE_BYTES;
     static constexpr int STAGES_1BUF =
         (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * kStgBytes) / STAGE_BYTES;
-    static constexpr int EPI_BUFS = (STAGES_2BUF < 4 && STAGES_1BUF >= 4) ? 1 : 2;
+    static constexpr int EPI_BUFS = (GU || (STAGES_2BUF < 4 && STAGES_1BUF >= 4)) ? 1 : 2;
     static constexpr int EPI_BYTES = TS ? 0 : kEpiWarps * EPI_BUFS * kStgBytes;
     // TS: the MMA reads the token tile as 128 rows although only BN are loaded
     // (results of the extra rows are never used), so 16 KB - B_BYTES of
@@ -275,12 +276,14 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         }
     } else {  // ------------------------------------------- epilogue (warps 4-11)
         // Warp we drains TMEM lanes 32*(warp % 4).. (32 intermediate features)
-        // for the 16-column chunks 16*(we / 4) + 32*j of each tile. Full chunks
-        // are staged in the warp's own shared buffers and written with TMA box
-        // stores; a ragged last chunk is written with plain stores.
+        // for the 16-column chunks 16*(we / 4) + 32*j of each tile. Each chunk
+        // is transposed through the warp's own shared buffer (token rows of 32
+        // features, 64 bytes each) and written with 16-byte stores, four lanes
+        // per row: no store waits on an earlier one, so the accumulator is
+        // released as soon as the last chunk has been read out of TMEM.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
-        uint8_t* stg = smem + C::EPI_OFF + we * C::EPI_BUFS * kStgBytes;
-        uint32_t nbuf = 0;
+        __nv_bfloat16* shi = reinterpret_cast<__nv_bfloat16*>(smem + C::EPI_OFF + we * kStgBytes);
+        __nv_bfloat16* slo = shi + kEpiRows * kEpiCols;
         int as = 0;
         uint32_t aph = 0;
         int qs = 0;
@@ -292,8 +295,6 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             const int n_feat = ti.shared ? a.I_s : a.I;
             const int i0 = ti.f * kGemmBM + q * kEpiCols;  // feature of lane 0
             const bool warp_valid = i0 < n_feat;            // I, I_s are multiples of 64
-            const CUtensorMap* m_hi = ti.shared ? &maps.st[2] : &maps.st[0];
-            const CUtensorMap* m_lo = ti.shared ? &maps.st[3] : &maps.st[1];
             __nv_bfloat16* dhi = ti.shared ? a.hs_hi : a.h_hi;
             __nv_bfloat16* dlo = ti.shared ? a.hs_lo : a.h_lo;
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
@@ -304,38 +305,25 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 ptx::tmem_ld_wait();
                 if (!warp_valid) continue;
                 const int rows = min(kEpiRows, ti.n_rows - c0);
-                if (rows == kEpiRows) {
-                    const uint32_t b = nbuf++ % C::EPI_BUFS;
-                    __nv_bfloat16* shi = reinterpret_cast<__nv_bfloat16*>(stg + b * kStgBytes);
-                    __nv_bfloat16* slo = shi + kEpiRows * kEpiCols;
-                    if (lane == 0) ptx::bulk_wait_read<C::EPI_BUFS - 1>();  // buffer b is free
-                    __syncwarp();
+                __syncwarp();  // the previous chunk's rows have been read back
 #pragma unroll
-                    for (int n = 0; n < kEpiRows; ++n) {
-                        const float gv = __uint_as_float(g[n]);
-                        const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                        shi[n * kEpiCols + lane] = hi;
-                        slo[n * kEpiCols + lane] = __float2bfloat16_rn(h - __bfloat162float(hi));
-                    }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(m_hi, ptx::smem_u32(shi), i0, ti.p0 + c0);
-                        ptx::tma_store_2d(m_lo, ptx::smem_u32(slo), i0, ti.p0 + c0);
-                        ptx::bulk_commit();
-                    }
-                } else {
+                for (int n = 0; n < kEpiRows; ++n) {
+                    const float gv = __uint_as_float(g[n]);
+                    const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                    shi[n * kEpiCols + lane] = hi;
+                    slo[n * kEpiCols + lane] = __float2bfloat16_rn(h - __bfloat162float(hi));
+                }
+                __syncwarp();
+                // 16 rows x 64 bytes per plane: lane l moves 16-byte pieces l and l + 32
+                // (row v / 4, features 8 (v % 4) ..) of both planes.
 #pragma unroll
-                    for (int n = 0; n < kEpiRows; ++n) {
-                        if (n < rows) {
-                            const float gv = __uint_as_float(g[n]);
-                            const float h = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[n]);
-                            const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                            const size_t o = static_cast<size_t>(ti.p0 + c0 + n) * n_feat + i0 + lane;
-                            dhi[o] = hi;
-                            dlo[o] = __float2bfloat16_rn(h - __bfloat162float(hi));
-                        }
+                for (int v = lane; v < kEpiRows * 4; v += 32) {
+                    const int r = v >> 2, part = v & 3;
+                    if (r < rows) {
+                        const size_t o = static_cast<size_t>(ti.p0 + c0 + r) * n_feat + i0 + part * 8;
+                        *reinterpret_cast<uint4*>(dhi + o) = reinterpret_cast<const uint4*>(shi)[v];
+                        *reinterpret_cast<uint4*>(dlo + o) = reinterpret_cast<const uint4*>(slo)[v];
                     }
                 }
             }
@@ -347,7 +335,6 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 aph ^= 1u;
             }
         }
-        if (lane == 0) ptx::bulk_wait_all();
     }
     gemm_teardown<C>(tmem_base, warp);
 }

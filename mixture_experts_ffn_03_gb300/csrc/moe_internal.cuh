@@ -47,6 +47,7 @@ enum : int {
     META_WORDS = 64,
 };
 
+constexpr int kMaxExperts = 1024;       // routed experts per layer at most
 constexpr int kRouteWarps = 8;          // tokens per route block (one warp each)
 constexpr int kSmallSlots = 2048;       // T*k up to which the routing launch also permutes
 constexpr int kCountTokens = 256;       // tokens per histogram block
@@ -127,9 +128,10 @@ struct GemmMaps {
     CUtensorMap ws;
     CUtensorMap h;
     CUtensorMap hs;
-    // Epilogue stores (no swizzle), box of 32 columns x kEpiRows rows:
-    // gate_up: st[0..3] = h_hi, h_lo, hs_hi, hs_lo; down: st[0] = y [T*k + T, H].
-    // down with tokens on M: st[1] = y in 32 x 32 boxes with the 128-byte swizzle.
+    // Epilogue stores of the down GEMM: st[0] = y [T*k + T, H] fp32 in boxes of
+    // 32 columns x kEpiRows rows (no swizzle); with tokens on M, st[1] = y as
+    // 24-bit floats in boxes of 96 bytes x 32 rows. (The gate_up epilogues
+    // write h with plain stores.)
     CUtensorMap st[4];
 };
 

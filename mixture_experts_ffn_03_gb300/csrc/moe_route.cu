@@ -373,13 +373,15 @@ route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn
 // complete. Thread tid owns the experts [tid*ept, tid*ept + ept), so expert
 // order is thread order: counts, exclusive offsets, both GEMMs' row tiles,
 // and each block's base inside each expert (written over its histogram).
-// Called by all 256 threads of the CTA.
+// Called by all 256 threads of the CTA; s_off and s_tstart are shared
+// arrays of E + 1 ints.
 __device__ __forceinline__ void scan_block_hist(int nb, int E, int bn_gu, int bn_dn,
                                                 int* __restrict__ blockhist,
                                                 int* __restrict__ counts,
                                                 int* __restrict__ offsets, int4* __restrict__ rt_gu,
                                                 int4* __restrict__ rt_dn, int* __restrict__ meta,
-                                                int* __restrict__ counts_out, int* s_warp) {
+                                                int* __restrict__ counts_out, int* s_warp,
+                                                int* s_off, int* s_tstart) {
     const int tid = threadIdx.x;
     const int ept = (E + 255) / 256;  // <= 4 for E <= 1024
     int local[4] = {0, 0, 0, 0};
@@ -417,21 +419,46 @@ __device__ __forceinline__ void scan_block_hist(int nb, int E, int bn_gu, int bn
     }
     if (tid == 0) offsets[E] = total;
 
+    // Row tiles, written by all threads: a hot expert (thousands of tokens)
+    // owns many tiles, which one thread would write one by one. s_off holds
+    // the offsets, s_tstart each expert's first tile index.
+    for (int r = 0, off = first_off; r < ept; ++r) {
+        const int e = tid * ept + r;
+        if (e >= E) break;
+        s_off[e] = off;
+        off += local[r];
+    }
+    if (tid == 0) s_off[E] = total;
     for (int g = 0; g < 2; ++g) {
         const int bn = g == 0 ? bn_gu : bn_dn;
         int nt = 0;
         for (int r = 0; r < ept; ++r) nt += (local[r] + bn - 1) / bn;
         int tot_tiles;
         int pos = block_excl_scan<8>(nt, s_warp, &tot_tiles);
-        int off = first_off;
         for (int r = 0; r < ept; ++r) {
             const int e = tid * ept + r;
             if (e >= E) break;
-            write_row_tiles(g == 0 ? rt_gu : rt_dn, pos, e, local[r], off, bn);
+            s_tstart[e] = pos;
             pos += (local[r] + bn - 1) / bn;
-            off += local[r];
+        }
+        if (tid == 0) s_tstart[E] = tot_tiles;
+        __syncthreads();
+        int4* rt = g == 0 ? rt_gu : rt_dn;
+        for (int i = tid; i < tot_tiles; i += blockDim.x) {
+            // the expert of tile i: the largest e with s_tstart[e] <= i (experts
+            // without tiles share their start with the next expert that has some)
+            int lo = 0, hi = E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_tstart[mid] <= i) lo = mid;
+                else hi = mid - 1;
+            }
+            const int m0 = (i - s_tstart[lo]) * bn;
+            const int n_e = s_off[lo + 1] - s_off[lo];
+            rt[i] = make_int4(lo, m0, min(bn, n_e - m0), s_off[lo] + m0);
         }
         if (tid == 0) meta[g == 0 ? META_RT_GU : META_RT_DN] = tot_tiles;
+        __syncthreads();  // s_tstart is rewritten for the next GEMM
     }
 }
 
@@ -452,6 +479,8 @@ route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_d
                    int* __restrict__ counts_out) {
     __shared__ int s_warp[kRouteWarps];
     __shared__ int s_is_last;
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_tstart[kMaxExperts + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // no-op unless launched behind the router GEMM
@@ -469,7 +498,7 @@ route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_d
     __threadfence();
     const int nb = (T + kCountTokens - 1) / kCountTokens;
     scan_block_hist(nb, E, bn_gu, bn_dn, blockhist, counts, offsets, rt_gu, rt_dn, meta,
-                    counts_out, s_warp);
+                    counts_out, s_warp, s_off, s_tstart);
     if (tid == 0) meta[META_TICKET] = 0;
 }
 
