@@ -112,7 +112,10 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 
     if (warp == 0) {
         if (lane == 0) {  // ---------------------------------- TMA producer
-            const uint64_t pol = ptx::policy_evict_normal();
+            // Each weight tile is read by one tile (decode, prefill, wide) or by the
+            // few row tiles of a hot expert, which run at about the same time:
+            // evict it first, so that the hidden rows, read k times, stay in L2.
+            const uint64_t pol = ptx::policy_evict_first();
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
             bool ok = true;
@@ -232,6 +235,9 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 trow[j] = t;
             }
             const __nv_bfloat16* col = a.hidden + c * 8;
+            // Each hidden row is gathered by the k experts of its token: keep it
+            // in L2. The 256-byte L2 prefetch also brings in the row's next K step.
+            const uint64_t pol_x = ptx::policy_evict_last();
             for (int ks = 0; ks < ksteps; ++ks) {
                 if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                     ok = false;
@@ -243,8 +249,8 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 for (int j = 0; j < RPT; ++j) {
                     const int r = r_first + 8 * j;
                     if (r < ti.n_rows)
-                        ptx::cp_async_16(sb + r * 128 + swz,
-                                         src + static_cast<size_t>(trow[j]) * a.H);
+                        ptx::cp_async_16_hint(sb + r * 128 + swz,
+                                              src + static_cast<size_t>(trow[j]) * a.H, pol_x);
                 }
                 ptx::cp_async_arrive_noinc(bar_addr(&ctl->full_b[s]));
                 if (++s == C::STAGES) {

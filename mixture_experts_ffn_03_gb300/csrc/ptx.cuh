@@ -171,6 +171,12 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16-byte cp.async with an L2 cache policy and a 256-byte L2 prefetch size.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint.L2::256B [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(src), "l"(pol)
+                 : "memory");
+}
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 // The barrier's expected count includes this arrival (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
