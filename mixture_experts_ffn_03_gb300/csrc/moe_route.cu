@@ -467,8 +467,10 @@ __device__ __forceinline__ void scan_block_hist(int nb, int E, int bn_gu, int bn
 // their order) into blockhist, which starts at zero. The last CTA to finish
 // (a completion ticket) scans the histograms: counts, offsets, row tiles and
 // per-block bases for scatter_kernel.
+// At most 64 registers: four CTAs per SM, so a 4096-token batch routes in
+// one wave.
 template <int EPL>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+__global__ void __launch_bounds__(kRouteWarps * 32, 4)
 route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
                    const LogitSrc logits, const __nv_bfloat16* __restrict__ hidden,
                    const __nv_bfloat16* __restrict__ w_g, int* __restrict__ topk_ids,
@@ -634,7 +636,7 @@ combine_y24_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
         const float w = topk_w[tk + j];
         const int p = inv[tk + j];
