@@ -4,8 +4,6 @@
 // TMEM set-up and the down GEMM's epilogue role.
 #pragma once
 
-#include <type_traits>
-
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -34,7 +32,6 @@ struct Ctl {
     uint64_t full_a[kMaxStages];  // TMA bytes landed
     uint64_t full_b[kMaxStages];  // gathered rows landed (gate_up)
     uint64_t empty[kMaxStages];   // MMAs reading the stage completed
-    uint64_t empty_b[kMaxStages]; // second TMA ring (down, tokens on M): MMAs done with a stage
     uint64_t tfull[2];            // accumulator ready for the epilogue
     uint64_t tempty[2];           // accumulator drained
     uint64_t drain;               // MMA completion on the abort path
@@ -187,32 +184,16 @@ __device__ __forceinline__ bool tq_read(Ctl* ctl, int& s, uint32_t& ph, Tile& ti
     return ti.n_rows >= 0;
 }
 
-// Stages of a configuration's second TMA ring (C::W_STAGES; 0 when it has
-// none and full_b counts the 64 row-gather threads instead).
-template <class C, class = void>
-struct SecondRing {
-    static constexpr int kStages = 0;
-};
-template <class C>
-struct SecondRing<C, std::void_t<decltype(C::W_STAGES)>> {
-    static constexpr int kStages = C::W_STAGES;
-};
-
 // Common set-up: barriers, TMEM allocation. Returns the TMEM base address.
 // C is the kernel's shared-memory / TMEM configuration.
 // tq_consumers: warps (or single threads) that read each tile descriptor.
 template <class C>
 __device__ __forceinline__ uint32_t gemm_setup(Ctl* ctl, int warp, int tq_consumers) {
-    constexpr int kRing2 = SecondRing<C>::kStages;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar_addr(&ctl->full_a[s]), 1);
-            if (kRing2 == 0) ptx::mbar_init(bar_addr(&ctl->full_b[s]), 64);
+            ptx::mbar_init(bar_addr(&ctl->full_b[s]), 64);
             ptx::mbar_init(bar_addr(&ctl->empty[s]), 1);
-        }
-        for (int s = 0; s < kRing2; ++s) {
-            ptx::mbar_init(bar_addr(&ctl->full_b[s]), 1);
-            ptx::mbar_init(bar_addr(&ctl->empty_b[s]), 1);
         }
         for (int s = 0; s < C::ACC_STAGES; ++s) {
             ptx::mbar_init(bar_addr(&ctl->tfull[s]), 1);
@@ -250,18 +231,12 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, int warp) {
     }
 }
 
-// Abort path of a TMA producer: wait (bounded) until the last load armed on
-// every stage of its ring (full barriers `full`) has landed, so no copy is in
-// flight when the CTA exits.
-template <int STAGES>
-__device__ __forceinline__ void drain_tma(const uint64_t* full, uint32_t armed,
-                                          uint32_t parity_bits) {
-    for (int s = 0; s < STAGES; ++s)
-        if (armed & (1u << s)) wait_bounded(bar_addr(&full[s]), (parity_bits >> s) & 1u);
-}
+// Abort path of the TMA producer: wait (bounded) until the last load armed on
+// every stage has landed, so no copy is in flight when the CTA exits.
 template <int STAGES>
 __device__ __forceinline__ void drain_tma(Ctl* ctl, uint32_t armed, uint32_t parity_bits) {
-    drain_tma<STAGES>(ctl->full_a, armed, parity_bits);
+    for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) wait_bounded(bar_addr(&ctl->full_a[s]), (parity_bits >> s) & 1u);
 }
 
 // Scale of the tile's weight matrix: the fp32 matrix scale of NVFP4 weights

@@ -172,6 +172,20 @@ bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// y of 128-token down tiles: rows of H 24-bit floats (3 bytes each, byte
+// tensor [outer, 3 * inner]) written in boxes of 96 bytes x 32 rows.
+bool make_y24_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {3 * inner, outer};
+    cuuint64_t strides[1] = {3 * inner};
+    cuuint32_t box[2] = {96, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cache[kMaxDevices] = {0};
     int dev = 0;
@@ -451,7 +465,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
              make_map(&dn.ws, W.s_down, Is, H, dn_w_rows) &&
              make_pair_map(&dn.h, h_hi, I, tk, L.h_lo - L.h_hi, bn_dn) &&
              make_pair_map(&dn.hs, hs_hi, Is, T, L.hs_lo - L.hs_hi, bn_dn);
-        ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T);
+        ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
+             make_y24_store_map(&dn.st[1], y, H, tk + T);
     }
     if (!ok) return MOE_ERR_CUDA;
 

@@ -489,32 +489,28 @@ __device__ __forceinline__ uint32_t y24_round(uint32_t b) {
 // once per 256 output features (twice as few as with the weights on M) and the
 // epilogue drains a single accumulator. Used when groups are large enough to
 // fill most of the 128 token rows.
-//
-// The operands come through two TMA rings with their own producer threads: the
-// h tiles (mostly served from L2, where the gate_up GEMM left them) in three
-// stages and the weight tiles (streamed from HBM) in four, so the weights are
-// requested one K step further ahead. The epilogue writes y with direct
-// 16-byte stores, which leaves all of shared memory to the two rings.
 struct DownTs {
     static constexpr int BM = 128;                          // token rows per tile (MMA M)
     static constexpr int NF = 256;                          // output features per tile (MMA N)
     static constexpr int A_BYTES = BM * kGemmBK * 2;        // 16 KB: h_hi or h_lo tile
-    static constexpr int H_BYTES = 2 * A_BYTES;             // h_hi + h_lo tiles (one request)
-    static constexpr int W_BYTES = NF * kGemmBK * 2;        // 32 KB: weight tile (one request)
-    static constexpr int STAGES = 3;                        // h ring
-    static constexpr int W_STAGES = 4;                      // weight ring
+    static constexpr int W_BYTES = NF * kGemmBK * 2;        // 32 KB: weight tile (two boxes)
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + W_BYTES;
+    static constexpr int STG_BYTES = 32 * 32 * 4;           // one warp's store box (32 rows x 96 B used)
+    static constexpr int EPI_BYTES = kEpiWarps * STG_BYTES;
     static constexpr int CTL_BYTES = 1024;
-    static constexpr int W_OFF = STAGES * H_BYTES;          // 1024-byte aligned (swizzled boxes)
-    static constexpr int CTL_OFF = W_OFF + W_STAGES * W_BYTES;
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - EPI_BYTES - CTL_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES;    // 1024-byte aligned (swizzled boxes)
+    static constexpr int CTL_OFF = EPI_OFF + EPI_BYTES;
     static constexpr int SMEM = 1024 + CTL_OFF + CTL_BYTES;
     static constexpr int ACC_COLS = NF;
     static constexpr int A_STAGES = 0;
     static constexpr int CONVERTER_WARPS = 0;
     static constexpr int ACC_STAGES = 2;
     static constexpr int TMEM_COLS = 512;
-    static_assert(W_STAGES <= kMaxStages && STAGES <= kMaxStages, "barrier arrays");
+    static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
-    static_assert(W_OFF % 1024 == 0 && H_BYTES % 1024 == 0, "swizzled tile alignment");
+    static_assert(EPI_OFF % 1024 == 0 && STG_BYTES % 1024 == 0, "swizzled staging alignment");
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -527,15 +523,13 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tmap(&maps.h);
-        ptx::prefetch_tmap(&maps.hs);
-    }
-    if (warp == 2 && lane == 0) {
         ptx::prefetch_tmap(&maps.w);
         ptx::prefetch_tmap(&maps.ws);
+        ptx::prefetch_tmap(&maps.h);
+        ptx::prefetch_tmap(&maps.hs);
+        ptx::prefetch_tmap(&maps.st[1]);
     }
-    // tile descriptors are read by the MMA issuer, the weight producer and 8 epilogue warps
-    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + 1 + kEpiWarps);
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + kEpiWarps);
     ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
 
     const int R = a.meta[META_RT_DN];
@@ -547,7 +541,8 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     const unsigned code = ERR_DOWN_TIMEOUT;
 
     if (warp == 0) {
-        if (lane == 0) {  // ------------------------- tile schedule + h producer
+        if (lane == 0) {  // ---------------------------------- TMA producer
+            const uint64_t pol_w = ptx::policy_evict_normal();
             const uint64_t pol_h = ptx::policy_evict_last();  // h rows are re-read per feature block
             int s = 0;
             uint32_t ph = 0, armed = 0, parity_bits = 0;
@@ -561,17 +556,22 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                  ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
                 sch.prefetch(a);
                 const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
                 const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
+                // Rows past this expert's H (a ragged last block) read the next
+                // expert's rows or zero fill; their columns are never stored.
+                const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * C::NF;
                 for (int ks = 0; ks < ksteps; ++ks) {
                     if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = ptx::smem_u32(smem + s * C::H_BYTES);
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
-                    ptx::mbar_arrive_expect_tx(fb, C::H_BYTES);
-                    // the tile's h_hi rows, then its h_lo rows (two planes, one request)
+                    ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    // h_hi then h_lo tile (one request), then 256 weight rows (one request)
                     ptx::tma_load_3d(sa, th, fb, ks * kGemmBK, ti.p0, 0, pol_h);
+                    ptx::tma_load_2d(sa + 2 * C::A_BYTES, tw, fb, ks * kGemmBK, row_w, pol_w);
                     armed |= 1u << s;
                     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) {
@@ -580,48 +580,12 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     }
                 }
             }
-            if (!ok) drain_tma<C::STAGES>(ctl->full_a, armed, parity_bits);
-        }
-    } else if (warp == 2) {
-        if (lane == 0) {  // -------------------------------- weight producer
-            // Each weight tile is read by the row tiles of one expert, which run
-            // at about the same time: evict it first.
-            const uint64_t pol_w = ptx::policy_evict_first();
-            int s = 0;
-            uint32_t ph = 0, armed = 0, parity_bits = 0;
-            bool ok = true;
-            int qs = 0;
-            uint32_t qph = 0;
-            Tile ti;
-            while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
-                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
-                const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
-                // Rows past this expert's H (a ragged last block) read the next
-                // expert's rows or zero fill; their columns are never stored.
-                const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * C::NF;
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    if (!wait_bar(bar_addr(&ctl->empty_b[s]), ph ^ 1u, abort_flag, err, code)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sw = ptx::smem_u32(smem + C::W_OFF + s * C::W_BYTES);
-                    const uint32_t fb = bar_addr(&ctl->full_b[s]);
-                    ptx::mbar_arrive_expect_tx(fb, C::W_BYTES);
-                    ptx::tma_load_2d(sw, tw, fb, ks * kGemmBK, row_w, pol_w);
-                    armed |= 1u << s;
-                    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
-                    if (++s == C::W_STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (!ok) drain_tma<C::W_STAGES>(ctl->full_b, armed, parity_bits);
+            if (!ok) drain_tma<C::STAGES>(ctl, armed, parity_bits);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ---------------------------------- MMA issuer
-            int s = 0, as = 0, sw = 0;
-            uint32_t ph = 0, aph = 0, wph = 0;
+            int s = 0, as = 0;
+            uint32_t ph = 0, aph = 0;
             bool ok = true;
             int qs = 0;
             uint32_t qph = 0;
@@ -637,17 +601,15 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + as * C::ACC_COLS;
                 for (int ks = 0; ks < ksteps; ++ks) {
-                    if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code) ||
-                        !wait_bar(bar_addr(&ctl->full_b[sw]), wph, abort_flag, err, code)) {
+                    if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_u32(smem + s * C::H_BYTES);
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint64_t dhi = ptx::smem_desc_sw128(sa);
                     const uint64_t dlo = ptx::smem_desc_sw128(sa + C::A_BYTES);
-                    const uint64_t dw =
-                        ptx::smem_desc_sw128(ptx::smem_u32(smem + C::W_OFF + sw * C::W_BYTES));
+                    const uint64_t dw = ptx::smem_desc_sw128(sa + 2 * C::A_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < kGemmBK / 16; ++kk) {
                         const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
@@ -655,14 +617,9 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                         ptx::mma_bf16_ss(d, dlo + 2 * kk, dw + 2 * kk, idesc, 1u);
                     }
                     ptx::mma_commit(bar_addr(&ctl->empty[s]));
-                    ptx::mma_commit(bar_addr(&ctl->empty_b[sw]));
                     if (++s == C::STAGES) {
                         s = 0;
                         ph ^= 1u;
-                    }
-                    if (++sw == C::W_STAGES) {
-                        sw = 0;
-                        wph ^= 1u;
                     }
                 }
                 if (!ok) break;
@@ -680,10 +637,13 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     } else if (warp >= 4) {  // ------------------------------ epilogue (warps 4-11)
         // Tokens on TMEM lanes: warp we owns the token rows 32*(warp % 4).. and
         // the features [128*(we / 4), +128) of the tile, drained 32 at a time.
-        // Each thread packs 32 consecutive features of its token's y row into
-        // 24-bit floats (96 contiguous bytes) and writes them with six 16-byte
-        // stores.
+        // Each thread packs 32 consecutive features of its token's y row (24-bit
+        // floats, 96 bytes) into the warp's staging box, which goes out as one
+        // 96-byte x 32-row TMA store; a warp whose token rows are only partly
+        // valid stores its valid rows directly.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
+        uint8_t* stg = smem + C::EPI_OFF + we * C::STG_BYTES;
+        const uint32_t stg_u32 = ptx::smem_u32(stg);
         int as = 0;
         uint32_t aph = 0;
         const int shared_row0 = a.T * a.k;
@@ -703,27 +663,43 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     scale = 1.f / (1.f + expf(-a.gate_logit[ti.m0 + r0 + lane]));
                 const uint32_t tb =
                     tmem_base + (static_cast<uint32_t>(r0) << 16) + as * C::ACC_COLS;
-                uint8_t* yrow = reinterpret_cast<uint8_t*>(a.y) +
-                                static_cast<size_t>(row0 + lane) * 3 * a.H;
                 for (int col = half * (C::NF / 2); col < half * (C::NF / 2) + C::NF / 2; col += 32) {
                     if (col >= n_f) break;
                     const int f0 = ti.f * C::NF + col;
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(tb + col, v);
+                    // The thread's 32 values of its token's y row, rounded to 24-bit
+                    // floats and packed into 96 bytes (24 words).
                     ptx::tmem_ld_wait();
-                    if (lane < rows_valid) {
-                        uint32_t w[24];
+                    uint32_t w[24];
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            const uint32_t b0 = y24_round(__float_as_uint(__uint_as_float(v[4 * g]) * scale));
-                            const uint32_t b1 = y24_round(__float_as_uint(__uint_as_float(v[4 * g + 1]) * scale));
-                            const uint32_t b2 = y24_round(__float_as_uint(__uint_as_float(v[4 * g + 2]) * scale));
-                            const uint32_t b3 = y24_round(__float_as_uint(__uint_as_float(v[4 * g + 3]) * scale));
-                            w[3 * g] = __byte_perm(b0, b1, 0x5321);
-                            w[3 * g + 1] = __byte_perm(b1, b2, 0x6532);
-                            w[3 * g + 2] = __byte_perm(b2, b3, 0x7653);
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t r0 = y24_round(__float_as_uint(__uint_as_float(v[4 * q]) * scale));
+                        const uint32_t r1 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 1]) * scale));
+                        const uint32_t r2 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 2]) * scale));
+                        const uint32_t r3 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 3]) * scale));
+                        w[3 * q] = __byte_perm(r0, r1, 0x5321);
+                        w[3 * q + 1] = __byte_perm(r1, r2, 0x6532);
+                        w[3 * q + 2] = __byte_perm(r2, r3, 0x7653);
+                    }
+                    if (rows_valid >= 32) {
+                        if (lane == 0) ptx::bulk_wait_read<0>();  // staging box free again
+                        __syncwarp();
+                        const uint32_t row_addr = stg_u32 + lane * 96;
+#pragma unroll
+                        for (int j = 0; j < 6; ++j)
+                            ptx::st_shared_v4u(row_addr + 16 * j, w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                                               w[4 * j + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&maps.st[1], stg_u32, 3 * f0, row0);
+                            ptx::bulk_commit();
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + 3 * f0);
+                    } else if (lane < rows_valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            reinterpret_cast<uint8_t*>(a.y) + static_cast<size_t>(row0 + lane) * 3 * a.H +
+                            3 * f0);
 #pragma unroll
                         for (int j = 0; j < 6; ++j)
                             dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
@@ -738,6 +714,7 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 aph ^= 1u;
             }
         }
+        if (lane == 0) ptx::bulk_wait_all();
     }
     gemm_teardown<C>(tmem_base, warp);
 }

@@ -128,10 +128,10 @@ struct GemmMaps {
     CUtensorMap ws;
     CUtensorMap h;
     CUtensorMap hs;
-    // Epilogue stores of the down GEMM with the weights on M: st[0] = y
-    // [T*k + T, H] fp32 in boxes of 32 columns x kEpiRows rows (no swizzle).
-    // (The gate_up epilogues and the tokens-on-M down epilogue write with
-    // plain stores.)
+    // Epilogue stores of the down GEMM: st[0] = y [T*k + T, H] fp32 in boxes of
+    // 32 columns x kEpiRows rows (no swizzle); with tokens on M, st[1] = y as
+    // 24-bit floats in boxes of 96 bytes x 32 rows. (The gate_up epilogues
+    // write h with plain stores.)
     CUtensorMap st[4];
 };
 
