@@ -313,6 +313,87 @@ int moe_get_expert_fusion(void);
 moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream);
 
 /*
+ * Expert parallelism: the layer spread over G ranks (one GPU each), rank g
+ * owning the contiguous block of routed experts [g E/G, (g+1) E/G) and a copy
+ * of the shared expert; every rank brings its own tokens. The pages run the
+ * experts this way ("FastAFD" pull request, What the model needed: expert
+ * workers at EP 4; "qwen3_5_moe is TP=1-only ...", first comment: routed
+ * experts sharded across ranks). Per rank, with the two exchanges done by the
+ * caller (e.g. an NCCL all-to-all) between the calls:
+ *   1. moe_ep_dispatch: routing and the permute of the rank's tokens over all
+ *      E experts (as in moe_forward), then the hidden rows of its (token,
+ *      slot) pairs in expert-sorted order into x_send, and the number of rows
+ *      per expert into send_counts. The rows bound for rank g are the
+ *      contiguous range of x_send that holds experts [g E/G, (g+1) E/G).
+ *   2. exchange: rank g receives, from every source rank s in rank order,
+ *      that range of s's x_send and s's counts of g's experts: x_recv [R, H]
+ *      (R rows in total) and recv_counts [G, E/G] (row s: source s).
+ *   3. moe_ep_experts: the rank's routed experts on the received rows (the
+ *      grouped gate_up and down GEMMs of moe_forward) and the shared expert,
+ *      gated by sigmoid(x . w_g), on the rank's own tokens. Results in the
+ *      workspace (moe_ep_workspace_layout: y): rows [0, R) the expert output
+ *      of the received rows, in x_recv's order; rows [R, R + T) the rank's
+ *      gated shared-expert rows. All fp32 [., H].
+ *   4. exchange back: rows [0, R) of y return to their source ranks (the
+ *      reverse of step 2), landing in y_back [T k, H] fp32 in the order of
+ *      the rank's own x_send.
+ *   5. moe_ep_combine: out = bf16(sum_j w_j y_back[slot j] + shared row),
+ *      summed in fp32 in slot order, as in moe_forward (gather, no atomics).
+ * moe_forward's results on the same tokens follow from the same arithmetic,
+ * except that y is always fp32 here (no 24-bit y) and the tile widths depend
+ * on the received rows, so outputs agree with moe_forward within the parity
+ * tolerance rather than bit for bit.
+ */
+typedef struct {
+    int32_t T;        /* this rank's tokens (0 <= T <= 2^22) */
+    int32_t H, E, k, I, I_s, score_fn;  /* as moe_dims; E counts all ranks' experts */
+    int32_t G;        /* ranks: 1 <= G <= E, E a multiple of G */
+    int32_t R_max;    /* most rows this rank may receive (0 .. 2^27); sizes the workspace */
+} moe_ep_dims;
+
+/* Byte offsets inside an expert-parallel workspace (see moe_workspace_layout
+ * for the routing arrays): y [R_max + T, H] fp32 holds the expert rows of the
+ * last moe_ep_experts call (rows [0, R): received rows, rows [R, R + T): the
+ * gated shared-expert rows of the rank's tokens). */
+typedef struct {
+    size_t topk_ids, topk_w, gate_logit, counts, offsets, perm, inv, y;
+    size_t total;
+} moe_ep_layout_t;
+
+/* Workspace bytes of one rank (0 for invalid sizes); 256-byte aligned device
+ * memory, no initialisation needed. One workspace serves the three calls of a
+ * step and must not be shared with concurrent calls. */
+size_t moe_ep_workspace_size(const moe_ep_dims* d);
+moe_status moe_ep_workspace_layout(const moe_ep_dims* d, moe_ep_layout_t* layout);
+
+/* Step 1. hidden [T, H] bf16, router_logits [T, E] fp32, w_g [H] bf16 as in
+ * moe_forward; x_send [T k, H] bf16 and send_counts [E] int32 written;
+ * topk_ids_out / topk_w_out [T, k] optional (NULL). T = 0 writes zero counts.
+ * Returns MOE_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE as moe_forward. */
+moe_status moe_ep_dispatch(const moe_ep_dims* d, const void* hidden, const float* router_logits,
+                           const void* w_g, void* x_send, int32_t* send_counts,
+                           int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                           size_t workspace_bytes, void* cuda_stream);
+
+/* Step 3. R received rows (0 <= R <= R_max, else MOE_ERR_INVALID_ARG);
+ * x_recv [R, H] bf16 (may be NULL when R = 0); recv_counts [G, E/G] int32 in
+ * device memory; hidden [T, H] bf16: the rank's own tokens (the same array
+ * given to moe_ep_dispatch, whose gate logits the workspace keeps); the
+ * rank's expert weights w_gate_up [E/G, 2I, H], w_down [E/G, H, I] bf16 and
+ * the shared expert's ws_gate_up [2I_s, H], ws_down [H, I_s]. Counts that are
+ * negative or do not add up to R are detected on the device: no received row
+ * is processed and moe_device_status() returns MOE_ERR_INVALID_ARG. */
+moe_status moe_ep_experts(const moe_ep_dims* d, int32_t R, const void* x_recv,
+                          const int32_t* recv_counts, const void* hidden, const void* w_gate_up,
+                          const void* w_down, const void* ws_gate_up, const void* ws_down,
+                          void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Step 5. R as given to moe_ep_experts; y_back [T k, H] fp32 (the returned
+ * rows, in x_send's order); out [T, H] bf16 written. */
+moe_status moe_ep_combine(const moe_ep_dims* d, int32_t R, const float* y_back, void* out,
+                          void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Allocation-free expert histogram. The pages have no counterpart to this
  * entry point; it exists for callers that cannot allocate device memory,
  * for example a plugin behind a fixed interface that receives only its

@@ -310,7 +310,7 @@ __device__ __forceinline__ void down_epilogue_tile(const Tile& ti, uint32_t slot
     const bool sh = (ti.shared & 1) != 0;
     const int h0 = ti.f * kGemmBM + q * kEpiCols;  // output feature of lane 0
     const bool warp_valid = h0 < a.H;               // H is a multiple of 64
-    const int row0 = sh ? a.T * a.k + ti.m0 : ti.p0;
+    const int row0 = sh ? a.P + ti.m0 : ti.p0;
     const float msc = matrix_scale(a, ti);
     const uint32_t tb = slot + (static_cast<uint32_t>(q * 32) << 16);
     for (int c0 = half * kEpiRows; c0 < ti.n_rows; c0 += 2 * kEpiRows) {

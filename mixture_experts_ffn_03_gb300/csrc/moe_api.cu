@@ -3,6 +3,7 @@
 // -> combine on the caller's stream. See include/moe.h for the contract.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "moe.h"
@@ -379,6 +380,56 @@ bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, ch
     return ok;
 }
 
+// Device arrays the routing and permute kernels write.
+struct RouteBufs {
+    int* topk_ids;
+    float* topk_w;
+    float* gate_logit;
+    int* blockhist;
+    int* counts;
+    int* offsets;
+    int* perm;
+    int* inv;
+    int4* rt_gu;
+    int4* rt_dn;
+    int* meta;
+};
+
+// Routing and the permute (stage 0, and the scatter as stage 1): one launch
+// when T*k <= 2048, else routing with the block histograms, then the scatter.
+// The status words (and, for large batches, the block histograms) must be
+// zero.
+cudaError_t enqueue_routing(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                            const LogitSrc& lsrc, bool pdl, const void* hidden, const void* w_g,
+                            const RouteBufs& b, int* ids_out, float* w_out, int* counts_out,
+                            cudaStream_t st) {
+    const auto* x = static_cast<const __nv_bfloat16*>(hidden);
+    const auto* g = static_cast<const __nv_bfloat16*>(w_g);
+    cudaError_t e;
+    if (route_small_fits(T, E, k)) {
+        e = launch_route_permute(T, H, E, k, score_fn, bn_gu, bn_dn, lsrc, pdl, x, g, b.topk_ids,
+                                 b.topk_w, b.gate_logit, b.counts, b.offsets, b.perm, b.inv,
+                                 b.rt_gu, b.rt_dn, b.meta, ids_out, w_out, counts_out, st);
+        mark_stage(1, st);
+        return e;
+    }
+    e = launch_route_count(T, H, E, k, score_fn, bn_gu, bn_dn, lsrc, pdl, x, g, b.topk_ids,
+                           b.topk_w, b.gate_logit, b.blockhist, b.counts, b.offsets, b.rt_gu,
+                           b.rt_dn, b.meta, ids_out, w_out, counts_out, st);
+    if (e != cudaSuccess) return e;
+    mark_stage(1, st);
+    return launch_scatter(T, E, k, b.topk_ids, b.blockhist, b.offsets, b.perm, b.inv, st);
+}
+
+// Bytes of the status block (and the block histograms of large batches) a
+// call must clear before routing T tokens; the histograms follow the status
+// block in every workspace layout.
+size_t routing_zero_bytes(const Layout& L, int T, int E, int k) {
+    if (route_small_fits(T, E, k)) return META_WORDS * sizeof(int);
+    return L.blockhist - L.meta +
+           static_cast<size_t>((T + kCountTokens - 1) / kCountTokens) * E * sizeof(int);
+}
+
 // w_router == nullptr: router_logits are an input. Otherwise the layer first
 // computes them from w_router [E, H] into logits_out (if given) or its
 // workspace (router_logits must then be null).
@@ -477,6 +528,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     ga.k = k;
     ga.I = I;
     ga.I_s = Is;
+    ga.P = static_cast<int>(tk);
     ga.hidden = static_cast<const __nv_bfloat16*>(hidden);
     ga.perm = perm;
     ga.counts = counts;
@@ -514,13 +566,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     // Status words (error flags, tile counts, completion ticket) start at zero,
     // and so do the large-batch routing's block histograms and the fused
     // launch's row-tile readiness counters that follow them.
-    const bool small_route = route_small_fits(T, E, k);
-    const size_t zero_bytes =
-        plan.fused ? L.ready - L.meta + (tk + T) * sizeof(int)
-                   : (small_route ? META_WORDS * sizeof(int)
-                                  : L.blockhist - L.meta +
-                                        static_cast<size_t>((T + kCountTokens - 1) / kCountTokens) *
-                                            E * sizeof(int));
+    const size_t zero_bytes = plan.fused ? L.ready - L.meta + (tk + T) * sizeof(int)
+                                         : routing_zero_bytes(L, T, E, k);
     if (cudaMemsetAsync(meta, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     mark_stage(0, st);
     LogitSrc lsrc{router_logits, 1, 0, nullptr};
@@ -537,29 +584,11 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
             return MOE_ERR_CUDA;
         lsrc = LogitSrc{partial, rp.splits, static_cast<size_t>(T) * E, logits_out};
     }
-    const bool route_pdl = w_router != nullptr;
-    if (small_route) {
-        // Routing and the whole permute in one launch; stage 1 is empty.
-        if ((launch_route_permute(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, route_pdl,
-                                  static_cast<const __nv_bfloat16*>(hidden),
-                                  static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w,
-                                  gate_logit, counts, offsets, perm, inv, rt_gu, rt_dn, meta,
-                                  topk_ids_out, topk_w_out, expert_counts_out, st)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        mark_stage(1, st);
-    } else {
-        // Routing with the block histograms and their scan in one launch, then
-        // the scatter (stage 1).
-        if ((launch_route_count(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, route_pdl,
-                                static_cast<const __nv_bfloat16*>(hidden),
-                                static_cast<const __nv_bfloat16*>(w_g), topk_ids, topk_w,
-                                gate_logit, blockhist, counts, offsets, rt_gu, rt_dn, meta,
-                                topk_ids_out, topk_w_out, expert_counts_out, st)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        mark_stage(1, st);
-        if ((launch_scatter(T, E, k, topk_ids, blockhist, offsets, perm, inv, st)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
+    const RouteBufs rb{topk_ids, topk_w, gate_logit, blockhist, counts, offsets,
+                       perm,     inv,    rt_gu,      rt_dn,     meta};
+    if (enqueue_routing(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, w_router != nullptr, hidden,
+                        w_g, rb, topk_ids_out, topk_w_out, expert_counts_out, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     mark_stage(2, st);
     if (plan.fused) {
         // gate_up and down in one launch; its time is stage 2's, stage 3 is empty.
@@ -756,5 +785,257 @@ MOE_API moe_status moe_device_status(const void* workspace, void* cuda_stream) {
     if (cudaMemcpy(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (flags & ERR_EP_COUNTS) return MOE_ERR_INVALID_ARG;
     return flags ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+// ================================================================ expert parallelism
+namespace moe {
+namespace {
+
+bool ep_dims_valid(const moe_ep_dims* d) {
+    if (!d) return false;
+    const moe_dims base{d->T, d->H, d->E, d->k, d->I, d->I_s, d->score_fn};
+    if (!dims_valid(&base)) return false;
+    if (d->G < 1 || d->G > d->E || d->E % d->G != 0) return false;
+    if (d->R_max < 0 || d->R_max > (1 << 27)) return false;
+    return true;
+}
+
+bool ep_dims_supported(const moe_ep_dims* d) {
+    const moe_dims base{d->T, d->H, d->E, d->k, d->I, d->I_s, d->score_fn};
+    return dims_supported(&base);
+}
+
+// Workspace of one rank: the routing arrays of its T tokens (the first part
+// of the single-GPU layout, status block first), then the GEMM arrays sized
+// for R_max received rows plus the rank's T shared-expert rows.
+struct EpLayout {
+    size_t meta, blockhist, topk_ids, topk_w, gate_logit, counts, offsets, perm, inv;
+    size_t rt_gu, rt_dn, h_hi, h_lo, hs_hi, hs_lo, y, total;
+};
+
+EpLayout ep_layout_of(const moe_ep_dims& d) {
+    EpLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + (bytes ? bytes : 1), kAlign);
+        return o;
+    };
+    const size_t T = d.T, H = d.H, E = d.E, I = d.I, Is = d.I_s, tk = T * d.k, R = d.R_max;
+    const size_t nb = (T + kCountTokens - 1) / kCountTokens;
+    L.meta = take(META_WORDS * sizeof(int));
+    L.blockhist = take(nb * E * 4);
+    L.topk_ids = take(tk * 4);
+    L.topk_w = take(tk * 4);
+    L.gate_logit = take(T * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take(tk * 4);
+    L.inv = take(tk * 4);
+    // row tiles: those the routing writes for the local batch, or those of the
+    // received rows (G * E / G segments), whichever list is longer
+    const size_t rt = std::max(max_row_tiles(tk, E, 16), max_row_tiles(R, E, 16));
+    L.rt_gu = take(rt * sizeof(int4));
+    L.rt_dn = take(rt * sizeof(int4));
+    L.h_hi = take(R * I * 2);
+    L.h_lo = take(R * I * 2);
+    L.hs_hi = take(T * Is * 2);
+    L.hs_lo = take(T * Is * 2);
+    L.y = take((R + T) * H * 4);
+    L.total = off;
+    return L;
+}
+
+bool ep_workspace_ok(const moe_ep_dims& d, const void* workspace, size_t bytes) {
+    return workspace && bytes >= ep_layout_of(d).total &&
+           (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) == 0;
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_API size_t moe_ep_workspace_size(const moe_ep_dims* d) {
+    if (!ep_dims_valid(d)) return 0;
+    return ep_layout_of(*d).total;
+}
+
+MOE_API moe_status moe_ep_workspace_layout(const moe_ep_dims* d, moe_ep_layout_t* out) {
+    if (!ep_dims_valid(d) || !out) return MOE_ERR_INVALID_ARG;
+    const EpLayout L = ep_layout_of(*d);
+    out->topk_ids = L.topk_ids;
+    out->topk_w = L.topk_w;
+    out->gate_logit = L.gate_logit;
+    out->counts = L.counts;
+    out->offsets = L.offsets;
+    out->perm = L.perm;
+    out->inv = L.inv;
+    out->y = L.y;
+    out->total = L.total;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_ep_dispatch(const moe_ep_dims* d, const void* hidden,
+                                   const float* router_logits, const void* w_g, void* x_send,
+                                   int32_t* send_counts, int32_t* topk_ids_out,
+                                   float* topk_w_out, void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream) {
+    if (!ep_dims_valid(d)) return MOE_ERR_INVALID_ARG;
+    if (!ep_dims_supported(d)) return MOE_ERR_UNSUPPORTED;
+    if (!send_counts || (reinterpret_cast<uintptr_t>(send_counts) & 3u)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (d->T == 0) {  // nothing routed: every count is zero
+        return cudaMemsetAsync(send_counts, 0, sizeof(int32_t) * d->E, st) == cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
+    }
+    const void* required[] = {hidden, router_logits, w_g, x_send};
+    for (const void* p : required)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const void* optional[] = {topk_ids_out, topk_w_out};
+    for (const void* p : optional)
+        if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
+    if (!ep_workspace_ok(*d, workspace, workspace_bytes)) return MOE_ERR_WORKSPACE;
+    const int T = d->T, H = d->H, E = d->E, k = d->k;
+    const EpLayout L = ep_layout_of(*d);
+    char* ws = static_cast<char*>(workspace);
+    int* meta = reinterpret_cast<int*>(ws + L.meta);
+    const RouteBufs rb{reinterpret_cast<int*>(ws + L.topk_ids),
+                       reinterpret_cast<float*>(ws + L.topk_w),
+                       reinterpret_cast<float*>(ws + L.gate_logit),
+                       reinterpret_cast<int*>(ws + L.blockhist),
+                       reinterpret_cast<int*>(ws + L.counts),
+                       reinterpret_cast<int*>(ws + L.offsets),
+                       reinterpret_cast<int*>(ws + L.perm),
+                       reinterpret_cast<int*>(ws + L.inv),
+                       reinterpret_cast<int4*>(ws + L.rt_gu),
+                       reinterpret_cast<int4*>(ws + L.rt_dn),
+                       meta};
+    Layout base{};
+    base.meta = L.meta;
+    base.blockhist = L.blockhist;
+    if (cudaMemsetAsync(meta, 0, routing_zero_bytes(base, T, E, k), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    // The routing's own row tiles are not used here; any supported width will do.
+    const LogitSrc lsrc{router_logits, 1, 0, nullptr};
+    if (enqueue_routing(T, H, E, k, d->score_fn, 16, 16, lsrc, false, hidden, w_g, rb,
+                        topk_ids_out, topk_w_out, send_counts, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_gather_rows(T * k, H, k, rb.perm, static_cast<const __nv_bfloat16*>(hidden),
+                           static_cast<__nv_bfloat16*>(x_send), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_ep_experts(const moe_ep_dims* d, int32_t R, const void* x_recv,
+                                  const int32_t* recv_counts, const void* hidden,
+                                  const void* w_gate_up, const void* w_down,
+                                  const void* ws_gate_up, const void* ws_down, void* workspace,
+                                  size_t workspace_bytes, void* cuda_stream) {
+    if (!ep_dims_valid(d)) return MOE_ERR_INVALID_ARG;
+    if (!ep_dims_supported(d)) return MOE_ERR_UNSUPPORTED;
+    if (R < 0 || R > d->R_max) return MOE_ERR_INVALID_ARG;
+    const void* required[] = {recv_counts, w_gate_up, w_down, ws_gate_up, ws_down};
+    for (const void* p : required)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!x_recv || !aligned16(x_recv))) return MOE_ERR_INVALID_ARG;
+    if (d->T > 0 && (!hidden || !aligned16(hidden))) return MOE_ERR_INVALID_ARG;
+    if (!ep_workspace_ok(*d, workspace, workspace_bytes)) return MOE_ERR_WORKSPACE;
+    if (R == 0 && d->T == 0) return MOE_OK;
+    const int T = d->T, H = d->H, G = d->G, I = d->I, Is = d->I_s;
+    const int E_loc = d->E / G;
+    const EpLayout L = ep_layout_of(*d);
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    char* ws = static_cast<char*>(workspace);
+    int* meta = reinterpret_cast<int*>(ws + L.meta);
+    int4* rt_gu = reinterpret_cast<int4*>(ws + L.rt_gu);
+    int4* rt_dn = reinterpret_cast<int4*>(ws + L.rt_dn);
+    auto* h_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.h_hi);
+    auto* hs_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_hi);
+    float* y = reinterpret_cast<float*>(ws + L.y);
+    const int num_sms = sm_count();
+    if (num_sms <= 0) return MOE_ERR_CUDA;
+
+    // Tile widths from the mean rows per (source, local expert) segment; the
+    // down GEMM keeps the weights on M (at most 64 tokens per tile) so that y
+    // is fp32 on every rank.
+    const size_t segs = static_cast<size_t>(G) * E_loc;
+    const int bn_gu = pick_bn(static_cast<size_t>(R), static_cast<int>(segs), 256, true);
+    const int bn_dn = pick_bn(static_cast<size_t>(R), static_cast<int>(segs), 64, false);
+
+    GemmMaps gu{}, dn{};
+    const uint64_t Rm = R > 0 ? R : 1, Tm = T > 0 ? T : 1;  // maps need non-empty dimensions
+    bool ok = make_pair_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E_loc) * 2 * I - I,
+                            static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
+              make_pair_map(&gu.ws, ws_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2, kGemmBM) &&
+              make_map(&dn.w, w_down, I, static_cast<uint64_t>(E_loc) * H, kGemmBM) &&
+              make_map(&dn.ws, ws_down, Is, H, kGemmBM) &&
+              make_pair_map(&dn.h, h_hi, I, Rm, L.h_lo - L.h_hi, bn_dn) &&
+              make_pair_map(&dn.hs, hs_hi, Is, Tm, L.hs_lo - L.hs_hi, bn_dn) &&
+              make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H,
+                             static_cast<uint64_t>(R) + T);
+    if (!ok) return MOE_ERR_CUDA;
+
+    GemmArgs ga{};
+    ga.T = T;
+    ga.H = H;
+    ga.E = E_loc;
+    ga.k = 1;
+    ga.I = I;
+    ga.I_s = Is;
+    ga.P = R;
+    ga.hidden = static_cast<const __nv_bfloat16*>(hidden);
+    ga.xrows = static_cast<const __nv_bfloat16*>(x_recv);
+    ga.meta = meta;
+    ga.gate_logit = reinterpret_cast<const float*>(ws + L.gate_logit);
+    ga.h_hi = h_hi;
+    ga.h_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.h_lo);
+    ga.hs_hi = hs_hi;
+    ga.hs_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.hs_lo);
+    ga.y = y;
+    ga.err = reinterpret_cast<unsigned*>(meta + META_ERR);
+    GemmArgs gd = ga;
+    ga.rowtiles = rt_gu;
+    gd.rowtiles = rt_dn;
+    ga.sched = meta + META_SCHED_GU;
+    gd.sched = meta + META_SCHED_DN;
+
+    const size_t routed_min = static_cast<size_t>(R) < segs ? static_cast<size_t>(R) : segs;
+    const int F_gu = (I + kGemmBM - 1) / kGemmBM, F_s = (Is + kGemmBM - 1) / kGemmBM;
+    const int F_dn = (H + kGemmBM - 1) / kGemmBM;
+    const size_t max_gu = (R / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
+    const size_t max_dn = (R / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
+    const size_t cap = 1u << 30;
+    const int tiles_gu = static_cast<int>(max_gu < cap ? max_gu : cap);
+    const int tiles_dn = static_cast<int>(max_dn < cap ? max_dn : cap);
+
+    if (cudaMemsetAsync(meta, 0, META_WORDS * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_ep_tiles(G, E_loc, R, recv_counts, bn_gu, bn_dn, rt_gu, rt_dn, meta, st) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_gate_up(bn_gu, gu, ga, tiles_gu, num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_down(bn_dn, dn, gd, tiles_dn, num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_ep_combine(const moe_ep_dims* d, int32_t R, const float* y_back,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  void* cuda_stream) {
+    if (!ep_dims_valid(d)) return MOE_ERR_INVALID_ARG;
+    if (!ep_dims_supported(d)) return MOE_ERR_UNSUPPORTED;
+    if (R < 0 || R > d->R_max) return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) return MOE_OK;
+    if (!y_back || !aligned16(y_back) || !out || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (!ep_workspace_ok(*d, workspace, workspace_bytes)) return MOE_ERR_WORKSPACE;
+    const EpLayout L = ep_layout_of(*d);
+    char* ws = static_cast<char*>(workspace);
+    const float* y_shared = reinterpret_cast<const float*>(ws + L.y) + static_cast<size_t>(R) * d->H;
+    if (launch_combine_split(d->T, d->H, d->k, y_back, y_shared,
+                             reinterpret_cast<const float*>(ws + L.topk_w),
+                             reinterpret_cast<const int*>(ws + L.inv),
+                             static_cast<__nv_bfloat16*>(out),
+                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }

@@ -226,15 +226,19 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         uint32_t qph = 0;
         Tile ti;
         while (ok && tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
-            uint32_t trow[RPT];  // token (hidden row) of each row this thread copies
+            // source row of each row this thread copies: a token's hidden row, or a
+            // pre-gathered row (expert parallelism)
+            const bool pre = !ti.shared && a.xrows != nullptr;
+            uint32_t trow[RPT];
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
                 const int r = r_first + 8 * j;
                 uint32_t t = 0;
-                if (r < ti.n_rows) t = ti.shared ? ti.m0 + r : a.perm[ti.p0 + r] / a.k;
+                if (r < ti.n_rows)
+                    t = ti.shared ? ti.m0 + r : (pre ? ti.p0 + r : a.perm[ti.p0 + r] / a.k);
                 trow[j] = t;
             }
-            const __nv_bfloat16* col = a.hidden + c * 8;
+            const __nv_bfloat16* col = (pre ? a.xrows : a.hidden) + c * 8;
             // Each hidden row is gathered by the k experts of its token: keep it
             // in L2. The 256-byte L2 prefetch also brings in the row's next K step.
             const uint64_t pol_x = ptx::policy_evict_last();
@@ -646,7 +650,7 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         const uint32_t stg_u32 = ptx::smem_u32(stg);
         int as = 0;
         uint32_t aph = 0;
-        const int shared_row0 = a.T * a.k;
+        const int shared_row0 = a.P;
         int qs = 0;
         uint32_t qph = 0;
         Tile ti;

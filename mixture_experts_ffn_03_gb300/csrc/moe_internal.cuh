@@ -34,6 +34,7 @@ enum : unsigned {
     ERR_GATE_UP_TIMEOUT = 1u << 0,
     ERR_DOWN_TIMEOUT = 1u << 1,
     ERR_ROUTER_TIMEOUT = 1u << 2,
+    ERR_EP_COUNTS = 1u << 3,      // received-row counts inconsistent (expert parallelism)
 };
 
 // Status block layout (int32 words at the start of the workspace).
@@ -90,11 +91,27 @@ cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* 
                            const int* offsets, int* perm, int* inv, cudaStream_t st);
 cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st);
+// Expert parallelism: the fp32 combine with the routed rows y_routed [T*k, H]
+// (sorted order) and the gated shared rows y_shared [T, H] in separate arrays;
+// the hidden rows of the (token, slot) pairs in sorted order; the row tiles of
+// the received rows (G source segments of E_loc local experts).
+constexpr int kEpTileThreads = 1024;
+cudaError_t launch_combine_split(int T, int H, int k, const float* y_routed, const float* y_shared,
+                                 const float* topk_w, const int* inv, __nv_bfloat16* out,
+                                 cudaStream_t st);
+cudaError_t launch_gather_rows(int P, int H, int k, const int* perm,
+                               const __nv_bfloat16* hidden, __nv_bfloat16* rows, cudaStream_t st);
+cudaError_t launch_ep_tiles(int G, int E_loc, int R, const int* recv_counts, int bn_gu,
+                            int bn_dn, int4* rt_gu, int4* rt_dn, int* meta, cudaStream_t st);
 
 // Grouped GEMMs (moe_gemm.cu).
 struct GemmArgs {
     int T, H, E, k, I, I_s;
+    int P;                  // routed rows (T*k; the received rows with expert parallelism)
     const __nv_bfloat16* hidden;
+    // Routed rows already gathered in sorted order (row p = xrows[p]), or null:
+    // row p is hidden[perm[p] / k]. Shared-expert rows always come from hidden.
+    const __nv_bfloat16* xrows;
     const int* perm;
     const int* counts;
     const int* offsets;

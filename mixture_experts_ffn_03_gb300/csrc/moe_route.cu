@@ -542,8 +542,9 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
 }
 
 __global__ void __launch_bounds__(256)
-combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __restrict__ topk_w,
-               const int* __restrict__ inv, __nv_bfloat16* __restrict__ out) {
+combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __restrict__ y_shared,
+               const float* __restrict__ topk_w, const int* __restrict__ inv,
+               __nv_bfloat16* __restrict__ out) {
     const int t = blockIdx.x;
     const int h = (blockIdx.y * 256 + threadIdx.x) * 4;
     ptx::griddep_launch_dependents();
@@ -561,8 +562,7 @@ combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __
         acc.z = fmaf(w, v.z, acc.z);
         acc.w = fmaf(w, v.w, acc.w);
     }
-    const size_t srow = static_cast<size_t>(T) * k + t;
-    const float4 s = __ldcs(reinterpret_cast<const float4*>(y + srow * H + h));
+    const float4 s = __ldcs(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * H + h));
     acc.x += s.x;
     acc.y += s.y;
     acc.z += s.z;
@@ -663,6 +663,86 @@ combine_y24_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// ---------------------------------------------------- expert parallelism
+// Rows of the (token, slot) pairs in expert-sorted order: rows[p] =
+// hidden[perm[p] / k]. The rows bound for one rank's block of experts are
+// then one contiguous range (the send buffer of the dispatch exchange).
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(int H, int k, const int* __restrict__ perm,
+                   const __nv_bfloat16* __restrict__ hidden, __nv_bfloat16* __restrict__ rows) {
+    const int p = blockIdx.x;
+    const int c = blockIdx.y * 256 + threadIdx.x;  // 16-byte chunk of the row
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    if (c >= H / 8) return;
+    const int t = perm[p] / k;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H) + c);
+    reinterpret_cast<uint4*>(rows + static_cast<size_t>(p) * H)[c] = v;
+}
+
+// Row tiles of the rows one rank received in the dispatch exchange: G source
+// segments in source order, each holding its rows sorted by local expert, with
+// recv_counts[s * E_loc + e] rows of expert e from source s. Thread i owns
+// segment i (i = s * E_loc + e); the segments' rows and tiles are exclusive
+// scans in that order. Tiles are {local expert, first row in the segment,
+// rows, first row in the received buffer}. If the counts are negative or do
+// not add up to R, no routed tile is written and the status word records
+// ERR_EP_COUNTS (the shared expert's tiles still run).
+__global__ void __launch_bounds__(kEpTileThreads)
+ep_tiles_kernel(int G, int E_loc, int R, const int* __restrict__ recv_counts, int bn_gu,
+                int bn_dn, int4* __restrict__ rt_gu, int4* __restrict__ rt_dn,
+                int* __restrict__ meta) {
+    constexpr int NW = kEpTileThreads / 32;
+    __shared__ int s_warp[NW];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_tstart[kMaxExperts + 1];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    const int nseg = G * E_loc;  // <= kMaxExperts
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    const int c = tid < nseg ? recv_counts[tid] : 0;
+    if (c < 0) atomicOr(&s_bad, 1);
+    int total;
+    const int off = block_excl_scan<NW>(c < 0 ? 0 : c, s_warp, &total);
+    if (tid < nseg) s_off[tid] = off;
+    if (tid == 0) s_off[nseg] = total;
+    __syncthreads();
+    const bool bad = s_bad != 0 || total != R;
+    if (bad) {
+        if (tid == 0) {
+            meta[META_RT_GU] = 0;
+            meta[META_RT_DN] = 0;
+            atomicOr(reinterpret_cast<unsigned*>(meta + META_ERR), ERR_EP_COUNTS);
+        }
+        return;
+    }
+    for (int g = 0; g < 2; ++g) {
+        const int bn = g == 0 ? bn_gu : bn_dn;
+        int tot_tiles;
+        const int pos = block_excl_scan<NW>((c + bn - 1) / bn, s_warp, &tot_tiles);
+        if (tid < nseg) s_tstart[tid] = pos;
+        if (tid == 0) s_tstart[nseg] = tot_tiles;
+        __syncthreads();
+        int4* rt = g == 0 ? rt_gu : rt_dn;
+        for (int i = tid; i < tot_tiles; i += kEpTileThreads) {
+            int lo = 0, hi = nseg - 1;  // the largest segment with s_tstart <= i
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_tstart[mid] <= i) lo = mid;
+                else hi = mid - 1;
+            }
+            const int m0 = (i - s_tstart[lo]) * bn;
+            const int n = s_off[lo + 1] - s_off[lo];
+            rt[i] = make_int4(lo % E_loc, m0, min(bn, n - m0), s_off[lo] + m0);
+        }
+        if (tid == 0) meta[g == 0 ? META_RT_GU : META_RT_DN] = tot_tiles;
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 bool route_small_fits(int T, int E, int k) {
@@ -742,7 +822,30 @@ cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const 
                              reinterpret_cast<const uint8_t*>(y), topk_w, inv, out);
     }
     dim3 grid(T, (H / 4 + 255) / 256);
-    return launch_kernel(combine_kernel, grid, dim3(256), 0, st, true, T, H, k, y, topk_w, inv, out);
+    return launch_kernel(combine_kernel, grid, dim3(256), 0, st, true, T, H, k, y,
+                         y + static_cast<size_t>(T) * k * H, topk_w, inv, out);
+}
+
+cudaError_t launch_combine_split(int T, int H, int k, const float* y_routed, const float* y_shared,
+                                 const float* topk_w, const int* inv, __nv_bfloat16* out,
+                                 cudaStream_t st) {
+    dim3 grid(T, (H / 4 + 255) / 256);
+    return launch_kernel(combine_kernel, grid, dim3(256), 0, st, true, T, H, k, y_routed, y_shared,
+                         topk_w, inv, out);
+}
+
+cudaError_t launch_gather_rows(int P, int H, int k, const int* perm,
+                               const __nv_bfloat16* hidden, __nv_bfloat16* rows, cudaStream_t st) {
+    if (P == 0) return cudaSuccess;
+    dim3 grid(P, (H / 8 + 255) / 256);
+    return launch_kernel(gather_rows_kernel, grid, dim3(256), 0, st, true, H, k, perm, hidden,
+                         rows);
+}
+
+cudaError_t launch_ep_tiles(int G, int E_loc, int R, const int* recv_counts, int bn_gu,
+                            int bn_dn, int4* rt_gu, int4* rt_dn, int* meta, cudaStream_t st) {
+    return launch_kernel(ep_tiles_kernel, dim3(1), dim3(kEpTileThreads), 0, st, true, G, E_loc, R,
+                         recv_counts, bn_gu, bn_dn, rt_gu, rt_dn, meta);
 }
 
 }  // namespace moe
