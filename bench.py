@@ -16,7 +16,9 @@ reported under per_config. Prints one JSON line (rank 0).
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a
 bounded token sample per step), with the same metric and workload.
-Multi-GPU runs (torchrun) are independent replicas: the layer does not shard.
+Multi-GPU runs (torchrun) are independent replicas by default; --ep spreads
+the experts over the ranks instead (expert parallelism, two all-to-alls per
+step), and --ep --ep-ranks G runs G such ranks one after another on one GPU.
 """
 from __future__ import annotations
 
@@ -457,6 +459,91 @@ def measure_per_config(args, dev, stream, flush, peaks, names):
     return res
 
 
+def run_expert_parallel(args, cfg):
+    """--ep: the layer spread over the ranks by expert parallelism (rank g holds
+    experts [g E/N, (g+1) E/N) and the shared expert; every rank routes the
+    workload's T tokens; two all-to-all exchanges per step over NCCL). At one
+    GPU, --ep-ranks G runs G ranks one after another on that GPU (in-process
+    exchange). Whole-job tokens/s over the slowest rank's time."""
+    import torch
+    import mixture_experts_ffn_03_gb300 as moe
+    from mixture_experts_ffn_03_gb300 import expert_parallel as ep
+    from mixture_experts_ffn_03_gb300 import workloads as wl
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    moe.load_library()
+    G = world if world > 1 else max(1, args.ep_ranks)
+    if cfg.E % G:
+        raise SystemExit(f"E={cfg.E} is not a multiple of {G} ranks")
+    e_loc = cfg.E // G
+    full = wl.make_inputs(cfg, seed=0, device=str(dev))
+    mine = [rank] if world > 1 else list(range(G))
+    layers = []
+    for g in mine:
+        layers.append(ep.ExpertParallelMoE(
+            g, G, full["w_gate_up"][g * e_loc:(g + 1) * e_loc].clone(),
+            full["w_down"][g * e_loc:(g + 1) * e_loc].clone(), full["ws_gate_up"],
+            full["ws_down"], full["w_g"], cfg.E, cfg.k, cfg.score_fn, cfg.T))
+    hidden, logits = full["hidden"], full["logits"]
+    del full["w_gate_up"], full["w_down"]
+    torch.cuda.empty_cache()
+    flush = L2Flush(dev)
+
+    def step():
+        if world > 1:
+            return [layers[0].forward(hidden, logits)]
+        return ep.LocalExchange(layers).forward([hidden] * G, [logits] * G)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    for i in range(K):
+        flush(i)
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    if dist is not None:
+        total_ms = max_over_ranks(total_ms, dist, dev)
+    for layer in layers:
+        st = moe.device_status(layer._ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError(moe.status_string(st))
+    if rank == 0:
+        tokens = G * cfg.T   # every rank routes T tokens per step
+        line = dict(
+            metric="MoE-layer tokens/s", value=tokens * K / (total_ms / 1e3), unit="tokens/s",
+            n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=total_ms / K,
+            higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+            data="synthetic",
+            config=dict(workload=workload_name(cfg), seed=0, weights="bf16",
+                        parallelism=f"ep{G}" + (" (ranks emulated on one GPU)" if world == 1 else ""),
+                        experts_per_rank=e_loc, tokens_per_rank=cfg.T,
+                        l2="flushed between timed steps: 256 MB write, then 256 MB read",
+                        launch="stream; host synchronises once per exchange for the row counts"),
+            gpu_launches=None, clocks=clocks)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,6 +559,10 @@ def main():
                          "(moe_forward_nvfp4)")
     ap.add_argument("--router", action="store_true",
                     help="compute the router logits in the layer from W_router (moe_forward_router)")
+    ap.add_argument("--ep", action="store_true",
+                    help="expert parallelism over the ranks (NCCL all-to-all exchanges)")
+    ap.add_argument("--ep-ranks", type=int, default=1,
+                    help="with --ep on one GPU: ranks to run one after another on it")
     ap.add_argument("--fusion", action="store_true",
                     help="allow the fused gate_up + down launch (bf16 weights, decode-sized "
                          "batches; off by default)")
@@ -482,6 +573,8 @@ def main():
     cfg = wl.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.ep:
+        return run_expert_parallel(args, cfg)
 
     import numpy as np
     import torch

@@ -220,9 +220,9 @@ __device__ __forceinline__ void ordered_scatter(const int* ids, long a0, long a1
     }
 }
 
-// Routing of one token per warp; writes ids, weights and the gate logit.
-// Lane j < k returns the token's j-th selected expert.
-template <int EPL>
+// Routing of one token per warp; writes ids, weights and (with GATE) the gate
+// logit. Lane j < k returns the token's j-th selected expert.
+template <int EPL, bool GATE = true>
 __device__ __forceinline__ int route_and_store(int t, int H, int E, int k, int score_fn,
                                                 const LogitSrc& logits,
                                                 const __nv_bfloat16* __restrict__ hidden,
@@ -259,12 +259,14 @@ __device__ __forceinline__ int route_and_store(int t, int H, int E, int k, int s
         }
     }
     GateLogit gl;
-    gl.load(t, H, hidden, w_g, lane, 0);
+    if (GATE) gl.load(t, H, hidden, w_g, lane, 0);
     int my_e;
     float my_w;
     route_token<EPL>(v, E, k, score_fn, lane, my_e, my_w);
-    const float z = gl.finish(t, H, hidden, w_g, lane);
-    if (lane == 0) gate_logit[t] = z;
+    if (GATE) {
+        const float z = gl.finish(t, H, hidden, w_g, lane);
+        if (lane == 0) gate_logit[t] = z;
+    }
     if (lane < k) {
         const size_t o = static_cast<size_t>(t) * k + lane;
         topk_ids[o] = my_e;
@@ -276,8 +278,10 @@ __device__ __forceinline__ int route_and_store(int t, int H, int E, int k, int s
 }
 
 // ------------------------------------------------------------ small batches
-// Routing (a warp per token) plus, in the last CTA to finish, the complete
-// permute of all T*k <= kSmallSlots slots.
+// Routing of one token per CTA (warp 0 selects the experts; all eight warps
+// share the gate logit's dot product, so the hidden row arrives in one round
+// trip) plus, in the last CTA to finish, the complete permute of all
+// T*k <= kSmallSlots slots.
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
@@ -290,14 +294,59 @@ route_permute_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn
                      int* __restrict__ counts_out) {
     extern __shared__ int s_dyn[];
     __shared__ int s_warp[kRouteWarps];
+    __shared__ float s_gate[kRouteWarps];
     __shared__ int s_is_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // no-op unless launched behind the router GEMM
-    const int t = blockIdx.x * kRouteWarps + warp;
-    if (t < T)
-        route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids, topk_w,
-                             gate_logit, ids_out, w_out, lane);
+    const int t = blockIdx.x;
+    // Gate logit z_t = x_t . w_g: thread i takes the 16-byte chunks i, i + 256,
+    // ... of the row, loaded before warp 0's top-k so that their latency
+    // overlaps it; the threads' sums are added per warp, then in warp order.
+    {
+        const uint4* xr = reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H);
+        const uint4* gr = reinterpret_cast<const uint4*>(w_g);
+        const int nch = H / 8, nthr = kRouteWarps * 32;
+        uint4 xa[kGateBatch], ga[kGateBatch];
+        auto load = [&](int c0) {
+#pragma unroll
+            for (int i = 0; i < kGateBatch; ++i) {
+                const int c = c0 + tid + nthr * i;
+                xa[i] = c < nch ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+                ga[i] = c < nch ? __ldg(gr + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        load(0);
+        if (warp == 0)
+            route_and_store<EPL, false>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids,
+                                        topk_w, gate_logit, ids_out, w_out, lane);
+        float acc = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += nthr * kGateBatch) {
+            if (c0 > 0) load(c0);
+#pragma unroll
+            for (int i = 0; i < kGateBatch; ++i) {
+                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&xa[i]);
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&ga[i]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 fa = __bfloat1622float2(a2[q]);
+                    const float2 fb = __bfloat1622float2(b2[q]);
+                    acc = fmaf(fa.x, fb.x, acc);
+                    acc = fmaf(fa.y, fb.y, acc);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) s_gate[warp] = acc;
+        __syncthreads();
+        if (tid == 0) {
+            float z = 0.f;
+#pragma unroll
+            for (int w = 0; w < kRouteWarps; ++w) z += s_gate[w];
+            gate_logit[t] = z;
+        }
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) s_is_last = (atomicAdd(&meta[META_TICKET], 1) == static_cast<int>(gridDim.x) - 1);
@@ -541,28 +590,47 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
     ordered_scatter(ids, wa0, wa1, running, perm, inv, lane);
 }
 
+// Every thread of a token's CTA needs the same k slot positions and weights:
+// they are read once into shared memory, then each thread issues the loads of
+// up to eight y rows together. The sum runs in slot order, then the shared row.
+constexpr int kCombineBatch = 8;
+
 __global__ void __launch_bounds__(256)
 combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __restrict__ y_shared,
                const float* __restrict__ topk_w, const int* __restrict__ inv,
                __nv_bfloat16* __restrict__ out) {
+    __shared__ int s_inv[32];
+    __shared__ float s_w[32];
     const int t = blockIdx.x;
     const int h = (blockIdx.y * 256 + threadIdx.x) * 4;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    if (h >= H) return;
     const size_t tk = static_cast<size_t>(t) * k;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-        const float w = topk_w[tk + j];
-        const int p = inv[tk + j];
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(y + static_cast<size_t>(p) * H + h));
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    if (threadIdx.x < k) {
+        s_inv[threadIdx.x] = inv[tk + threadIdx.x];
+        s_w[threadIdx.x] = topk_w[tk + threadIdx.x];
     }
+    __syncthreads();
+    if (h >= H) return;
     const float4 s = __ldcs(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * H + h));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+        float4 v[kCombineBatch];
+#pragma unroll
+        for (int j = 0; j < kCombineBatch; ++j)
+            if (j0 + j < k)
+                v[j] = __ldcs(reinterpret_cast<const float4*>(y + static_cast<size_t>(s_inv[j0 + j]) * H + h));
+#pragma unroll
+        for (int j = 0; j < kCombineBatch; ++j) {
+            if (j0 + j < k) {
+                const float w = s_w[j0 + j];
+                acc.x = fmaf(w, v[j].x, acc.x);
+                acc.y = fmaf(w, v[j].y, acc.y);
+                acc.z = fmaf(w, v[j].z, acc.z);
+                acc.w = fmaf(w, v[j].w, acc.w);
+            }
+        }
+    }
     acc.x += s.x;
     acc.y += s.y;
     acc.z += s.z;
@@ -624,22 +692,28 @@ __global__ void __launch_bounds__(128)
 combine_y24_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
                    const float* __restrict__ topk_w, const int* __restrict__ inv,
                    __nv_bfloat16* __restrict__ out) {
+    __shared__ int s_inv[32];
+    __shared__ float s_w[32];
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31;
     const int hw = (blockIdx.y * 128 + (threadIdx.x & ~31)) * 16;  // warp's first output
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+    if (threadIdx.x < k) {
+        s_inv[threadIdx.x] = inv[static_cast<size_t>(t) * k + threadIdx.x];
+        s_w[threadIdx.x] = topk_w[static_cast<size_t>(t) * k + threadIdx.x];
+    }
+    __syncthreads();
     if (hw >= H) return;  // whole warp past the row end
     const int lanes_valid = min(32, (H - hw) / 16);  // H is a multiple of 64
     const size_t row_bytes = static_cast<size_t>(3) * H;
-    const size_t tk = static_cast<size_t>(t) * k;
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll 4
     for (int j = 0; j < k; ++j) {
-        const float w = topk_w[tk + j];
-        const int p = inv[tk + j];
+        const float w = s_w[j];
+        const int p = s_inv[j];
         float f[16];
         y24_row(y + static_cast<size_t>(p) * row_bytes + 3 * hw, lane, lanes_valid, f);
 #pragma unroll
@@ -773,7 +847,7 @@ cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int b
                                  float* gate_logit, int* counts, int* offsets, int* perm,
                                  int* inv, int4* rt_gu, int4* rt_dn, int* meta, int* ids_out,
                                  float* w_out, int* counts_out, cudaStream_t st) {
-    const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
+    const int blocks = T;  // one token per CTA
     const size_t smem = (static_cast<size_t>(T) * k + static_cast<size_t>(kRouteWarps) * E) *
                         sizeof(int);
 #define MOE_LAUNCH_RP(N)                                                                        \
