@@ -590,47 +590,28 @@ scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
     ordered_scatter(ids, wa0, wa1, running, perm, inv, lane);
 }
 
-// Every thread of a token's CTA needs the same k slot positions and weights:
-// they are read once into shared memory, then each thread issues the loads of
-// up to eight y rows together. The sum runs in slot order, then the shared row.
-constexpr int kCombineBatch = 8;
-
 __global__ void __launch_bounds__(256)
 combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __restrict__ y_shared,
                const float* __restrict__ topk_w, const int* __restrict__ inv,
                __nv_bfloat16* __restrict__ out) {
-    __shared__ int s_inv[32];
-    __shared__ float s_w[32];
     const int t = blockIdx.x;
     const int h = (blockIdx.y * 256 + threadIdx.x) * 4;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    const size_t tk = static_cast<size_t>(t) * k;
-    if (threadIdx.x < k) {
-        s_inv[threadIdx.x] = inv[tk + threadIdx.x];
-        s_w[threadIdx.x] = topk_w[tk + threadIdx.x];
-    }
-    __syncthreads();
     if (h >= H) return;
-    const float4 s = __ldcs(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * H + h));
+    const size_t tk = static_cast<size_t>(t) * k;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
-        float4 v[kCombineBatch];
-#pragma unroll
-        for (int j = 0; j < kCombineBatch; ++j)
-            if (j0 + j < k)
-                v[j] = __ldcs(reinterpret_cast<const float4*>(y + static_cast<size_t>(s_inv[j0 + j]) * H + h));
-#pragma unroll
-        for (int j = 0; j < kCombineBatch; ++j) {
-            if (j0 + j < k) {
-                const float w = s_w[j0 + j];
-                acc.x = fmaf(w, v[j].x, acc.x);
-                acc.y = fmaf(w, v[j].y, acc.y);
-                acc.z = fmaf(w, v[j].z, acc.z);
-                acc.w = fmaf(w, v[j].w, acc.w);
-            }
-        }
+#pragma unroll 4
+    for (int j = 0; j < k; ++j) {
+        const float w = topk_w[tk + j];
+        const int p = inv[tk + j];
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(y + static_cast<size_t>(p) * H + h));
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
     }
+    const float4 s = __ldcs(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * H + h));
     acc.x += s.x;
     acc.y += s.y;
     acc.z += s.z;
@@ -692,28 +673,22 @@ __global__ void __launch_bounds__(128)
 combine_y24_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
                    const float* __restrict__ topk_w, const int* __restrict__ inv,
                    __nv_bfloat16* __restrict__ out) {
-    __shared__ int s_inv[32];
-    __shared__ float s_w[32];
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31;
     const int hw = (blockIdx.y * 128 + (threadIdx.x & ~31)) * 16;  // warp's first output
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    if (threadIdx.x < k) {
-        s_inv[threadIdx.x] = inv[static_cast<size_t>(t) * k + threadIdx.x];
-        s_w[threadIdx.x] = topk_w[static_cast<size_t>(t) * k + threadIdx.x];
-    }
-    __syncthreads();
     if (hw >= H) return;  // whole warp past the row end
     const int lanes_valid = min(32, (H - hw) / 16);  // H is a multiple of 64
     const size_t row_bytes = static_cast<size_t>(3) * H;
+    const size_t tk = static_cast<size_t>(t) * k;
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll 4
     for (int j = 0; j < k; ++j) {
-        const float w = s_w[j];
-        const int p = s_inv[j];
+        const float w = topk_w[tk + j];
+        const int p = inv[tk + j];
         float f[16];
         y24_row(y + static_cast<size_t>(p) * row_bytes + 3 * hw, lane, lanes_valid, f);
 #pragma unroll
