@@ -76,7 +76,11 @@ def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, total_ms: flo
 
 def workload_name(cfg):
     sf = "softmax" if cfg.score_fn == 0 else "sigmoid"
-    return (f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} I={cfg.I} I_s={cfg.I_s} "
+    from mixture_experts_ffn_03_gb300 import workloads as wl
+    full = wl.CONFIGS.get(cfg.name)
+    reduced = full is not None and (full.T, full.E) != (cfg.T, cfg.E)
+    return (f"{cfg.name}{' (reduced)' if reduced else ''}: T={cfg.T} H={cfg.H} E={cfg.E} "
+            f"k={cfg.k} I={cfg.I} I_s={cfg.I_s} "
             f"{sf}+renorm{', zipf-skewed logits' if cfg.skew else ''}")
 
 
@@ -563,6 +567,10 @@ def main():
                     help="expert parallelism over the ranks (NCCL all-to-all exchanges)")
     ap.add_argument("--ep-ranks", type=int, default=1,
                     help="with --ep on one GPU: ranks to run one after another on it")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="reduced workload for profiling captures: this many tokens")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="reduced workload for profiling captures: this many experts")
     ap.add_argument("--fusion", action="store_true",
                     help="allow the fused gate_up + down launch (bf16 weights, decode-sized "
                          "batches; off by default)")
@@ -571,6 +579,13 @@ def main():
 
     from mixture_experts_ffn_03_gb300 import workloads as wl
     cfg = wl.CONFIGS[args.config]
+    if args.tokens is not None or args.experts is not None:
+        # same shapes per expert, fewer tokens or experts (a capture that fits the
+        # profiler's memory budget); never the headline line's workload
+        import dataclasses
+        cfg = dataclasses.replace(cfg, T=args.tokens if args.tokens is not None else cfg.T,
+                                  E=args.experts if args.experts is not None else cfg.E)
+        args.no_per_config = True
     if args.impl == "reference":
         return run_reference(args, cfg)
     if args.ep:
