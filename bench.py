@@ -155,8 +155,10 @@ KERNEL_SOURCES = {
                           "moe_internal.cuh"),
     "moe_gate_up_nvfp4": ("moe_gemm_mx.cu", "mxfp8.cuh", "gemm_common.cuh", "ptx.cuh",
                           "moe_internal.cuh"),
-    "moe_expert_fused": ("moe_fused.cu", "moe_fused.cuh", "gemm_common.cuh", "ptx.cuh",
-                         "moe_internal.cuh"),
+    "moe_expert_fused": ("moe_fused.cu", "moe_fused.cuh", "routing.cuh", "gemm_common.cuh",
+                         "ptx.cuh", "moe_internal.cuh"),
+    "moe_layer_fused": ("moe_fused.cu", "moe_fused.cuh", "routing.cuh", "gemm_common.cuh",
+                        "ptx.cuh", "moe_internal.cuh"),
 }
 
 
@@ -383,7 +385,8 @@ def measure(args, cfg, dev, layer, inp, stream, flush, K, sampler=None, dist=Non
     stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev]
                 for j in range(moe.NUM_STAGES)]
     return dict(step_ms=step_ms, stage_ms=stage_ms, counts=counts.cpu().tolist(), out=out,
-                n_launch=n_launch, fused=n_launch < n_separate, wall=wall, clocks=clocks)
+                n_launch=n_launch, fused=n_launch < n_separate, layer=n_launch == 1, wall=wall,
+                clocks=clocks)
 
 
 def work_of(args, cfg, m):
@@ -395,7 +398,12 @@ def work_of(args, cfg, m):
         work["flops"] += 2.0 * cfg.T * cfg.E * cfg.H
         work["bytes"] += 2.0 * cfg.E * cfg.H - 4.0 * cfg.T * cfg.E
     gu_kernel = "moe_gate_up_mxfp8" if mx else ("moe_gate_up_nvfp4" if nv else "moe_gate_up")
-    if m["fused"]:
+    if m["layer"]:
+        # the whole layer is one launch (the routing stage of the per-kernel events)
+        gu_kernel = "moe_layer_fused"
+        work["gate_up_bytes"] = work["bytes"]
+        work["gate_up_flops"] = work["flops"]
+    elif m["fused"]:
         # gate_up and down run as one launch (the gate_up stage of the per-kernel events)
         gu_kernel = "moe_expert_fused"
         work["gate_up_bytes"] += work["down_bytes"]
@@ -407,10 +415,11 @@ def rooflines(cfg, work, m, peaks, gu_kernel):
     """`roofline` of the dominant kernel (gate_up, or the fused expert launch)
     and `layer_roofline` of the whole step."""
     ms_step = sum(m["step_ms"]) / len(m["step_ms"])
-    gu_ms = statistics.mean(m["stage_ms"][2])
+    gu_ms = statistics.mean(m["stage_ms"][0 if m["layer"] else 2])
     hbm_bound = work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (
         peaks["bf16_tflops_sustained"] * 1e12)
-    kname = f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if m["fused"] else "")
+    kname = ("moe_layer_fused (routing, gate_up, down and combine in one launch)" if m["layer"]
+             else f"{gu_kernel} grouped GEMM" + (" (gate_up + down)" if m["fused"] else ""))
     if hbm_bound:
         achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
         roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
@@ -571,9 +580,9 @@ def main():
                     help="reduced workload for profiling captures: this many tokens")
     ap.add_argument("--experts", type=int, default=None,
                     help="reduced workload for profiling captures: this many experts")
-    ap.add_argument("--fusion", action="store_true",
-                    help="allow the fused gate_up + down launch (bf16 weights, decode-sized "
-                         "batches; off by default)")
+    ap.add_argument("--fusion", type=int, nargs="?", const=1, default=0,
+                    help="launch fusion (bf16 weights, decode-sized batches; off by default): "
+                         "1 gate_up + down in one launch, 2 the whole layer in one launch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -715,12 +724,13 @@ def main():
                     parallelism="replicas" if world > 1 else "1gpu",
                     l2="flushed between timed steps: 256 MB write, then 256 MB read of a "
                        "second buffer (no dirty lines left)", launch="stream",
-                    experts=("one fused gate_up + down launch" if m["fused"]
+                    experts=("the whole layer in one launch" if m["layer"] else
+                             "one fused gate_up + down launch" if m["fused"]
                              else "gate_up and down launches"),
                     wall_s=round(m["wall"], 3)),
         roofline=roof, layer_roofline=layer_roof, kernel_us=kernel_us(m),
         kernel_timing="separate pass of K steps with library-recorded events around each kernel",
-        down_gbs=None if m["fused"] else work["down_bytes"] / (dn_ms / 1e3) / 1e9,
+        down_gbs=None if (m["fused"] or m["layer"]) else work["down_bytes"] / (dn_ms / 1e3) / 1e9,
         e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h,
                  mode="serving loop (moe.HostPipeline): transfers overlap neighbouring steps' compute",

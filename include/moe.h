@@ -260,7 +260,9 @@ moe_status moe_workspace_layout(const moe_dims* d, moe_workspace_layout_t* layou
  * when T*k <= 2048), scatter, gate_up GEMM, down GEMM, combine. A stage that
  * a batch merges into the one before is empty: the scatter stage when
  * T*k <= 2048, and the down stage when the fused expert launch
- * (moe_set_expert_fusion, when enabled) runs in the gate_up stage. */
+ * (moe_set_expert_fusion, when enabled) runs in the gate_up stage. The
+ * whole-layer launch (fusion level 2) runs in the routing stage and leaves the
+ * other four empty. */
 #define MOE_NUM_STAGES 5
 
 /* Optional per-kernel timing. `events` points to MOE_NUM_STAGES + 1
@@ -275,7 +277,7 @@ moe_status moe_set_stage_events(void* const* events, int n_events);
 /* Number of kernels one moe_forward with these sizes launches from the
  * calling host thread, or 0 for invalid sizes or T = 0: routing (1 launch
  * when T*k <= 2048, else 2), the expert GEMMs (1 launch when they run fused,
- * else 2) and the combine. */
+ * else 2) and the combine; 1 when the whole layer runs as one launch. */
 int moe_launch_count(const moe_dims* d);
 
 /* The same for moe_forward_mxfp8 and moe_forward_nvfp4 (their expert GEMMs
@@ -298,7 +300,21 @@ int moe_launch_count_quantized(const moe_dims* d);
  * than the wait limit, the layer reports MOE_ERR_DEVICE_TIMEOUT through
  * moe_device_status. Source: "Add Qwen3.5-35B-A3B (support vision and text
  * input)", Description (the routed experts and the shared expert); the
- * fusion is an implementation choice. */
+ * fusion is an implementation choice.
+ *
+ * enable: 0 (default) separate launches; 1 the fused expert phase above;
+ * 2 also, where it applies, the whole layer in one persistent launch of one
+ * CTA per SM: moe_forward (router logits given, not moe_forward_router),
+ * T*k <= 2048, E <= 256 and the fused expert phase applying (decode-sized
+ * batches). In that launch every CTA routes tokens (CTA b takes tokens b,
+ * b + #SMs, ...), the last CTA to finish builds the permute, the others wait
+ * for it; then the fused expert phase; then every CTA waits until all have
+ * finished their expert tiles and combines its tokens. Both waits are bounded
+ * in time like every wait in the library (a timeout is reported by
+ * moe_device_status as MOE_ERR_DEVICE_TIMEOUT, and no token is combined
+ * after one). The arithmetic is that of the separate kernels: results,
+ * routing outputs and counts are bitwise identical. Other values are
+ * clamped to 0..2. moe_get_expert_fusion returns the calling thread's level. */
 void moe_set_expert_fusion(int enable);
 int moe_get_expert_fusion(void);
 

@@ -134,22 +134,24 @@ def launch_count_quantized(dims: MoEDims) -> int:
     return int(load_library().moe_launch_count_quantized(ctypes.byref(dims)))
 
 
-def set_expert_fusion(enable: bool) -> None:
-    """Allow or forbid (the default) the fused gate_up + down launch for bf16
-    weights on decode-sized batches, for calls from this host thread."""
-    load_library().moe_set_expert_fusion(1 if enable else 0)
+def set_expert_fusion(level) -> None:
+    """Launch fusion for bf16 weights, for calls from this host thread: 0 or
+    False (the default) none; 1 or True the fused gate_up + down launch on
+    decode-sized batches; 2 also the whole layer in one launch where it
+    applies (T*k <= 2048, E <= 256, logits given)."""
+    load_library().moe_set_expert_fusion(int(level))
 
 
-def get_expert_fusion() -> bool:
-    return bool(load_library().moe_get_expert_fusion())
+def get_expert_fusion() -> int:
+    return int(load_library().moe_get_expert_fusion())
 
 
 class expert_fusion:  # noqa: N801 (used like a function: `with expert_fusion(True):`)
-    """Context manager: `with expert_fusion(True): ...` runs the block with
-    the fused expert launch allowed (or forbidden), then restores the setting."""
+    """Context manager: `with expert_fusion(level): ...` runs the block with
+    that fusion level (set_expert_fusion), then restores the setting."""
 
-    def __init__(self, enable: bool):
-        self.enable = bool(enable)
+    def __init__(self, enable):
+        self.enable = int(enable)
 
     def __enter__(self):
         self.prev = get_expert_fusion()

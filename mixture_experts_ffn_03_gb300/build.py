@@ -19,7 +19,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["moe_api.cu", "moe_route.cu", "moe_gemm.cu", "moe_gemm_mx.cu", "moe_router.cu", "moe_fused.cu",
            "moe_static.cu"]
-HEADERS = ["ptx.cuh", "moe_internal.cuh", "gemm_common.cuh", "mxfp8.cuh", "moe_fused.cuh"]
+HEADERS = ["ptx.cuh", "moe_internal.cuh", "gemm_common.cuh", "mxfp8.cuh", "moe_fused.cuh",
+           "routing.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

@@ -215,32 +215,40 @@ int pick_bn(size_t tk, int E, int cap, bool gate_up) {
     return bn;
 }
 
-// Per host thread: may moe_forward / moe_forward_router run gate_up and down
-// as one launch (moe_set_expert_fusion)? Off by default: measured on GB300,
-// the fused launch is no faster at decode (the programmatic dependent launch
-// already overlaps the boundary) and slower on wide batches (its down steps
-// share the gate_up-sized ring and keep fewer bytes in flight).
-thread_local bool tl_fusion = false;
+// Per host thread: may moe_forward / moe_forward_router fuse launches
+// (moe_set_expert_fusion)? 0 (default): no; 1: gate_up and down as one
+// launch; 2: also the whole layer in one launch where it applies. Off by
+// default: measured on GB300, the fused launches are no faster at decode (the
+// programmatic dependent launches already overlap the boundaries) and the
+// fused expert launch is slower on wide batches (its down steps share the
+// gate_up-sized ring and keep fewer bytes in flight).
+thread_local int tl_fusion = 0;
 
-// Token-tile widths of the two bf16 GEMMs, and whether they run fused.
+// Token-tile widths of the two bf16 GEMMs, and which launches are fused.
 struct BnPlan {
     int gu, dn;
-    bool fused;
+    bool fused;  // gate_up and down in one launch
+    bool layer;  // routing, both GEMMs and the combine in one launch
 };
 
-BnPlan bn_plan(size_t tk, int E, bool mx) {
+BnPlan bn_plan(size_t tk, int E, bool mx, bool router = false) {
     BnPlan p;
     p.gu = pick_bn(tk, E, mx ? 64 : 256, true);
     p.dn = pick_bn(tk, E, mx ? 64 : 128, false);
-    p.fused = !mx && tl_fusion && p.gu == p.dn && p.gu <= kFusedMaxBN;
+    p.fused = !mx && tl_fusion >= 1 && p.gu == p.dn && p.gu <= kFusedMaxBN;
+    p.layer = p.fused && tl_fusion >= 2 && !router && tk <= static_cast<size_t>(kSmallSlots) &&
+              E <= kLayerMaxExperts;
     return p;
 }
 
 // Kernels one forward launches: routing (one launch, or route with the block
-// histograms + scatter), the expert GEMMs (one fused launch or two), the combine.
-int launches_of(const moe_dims& d, bool mx) {
+// histograms + scatter), the expert GEMMs (one fused launch or two), the
+// combine; or the whole layer as one launch.
+int launches_of(const moe_dims& d, bool mx, bool router = false) {
     const size_t tk = static_cast<size_t>(d.T) * d.k;
-    return (route_small_fits(d.T, d.E, d.k) ? 1 : 2) + (bn_plan(tk, d.E, mx).fused ? 1 : 2) + 1;
+    const BnPlan p = bn_plan(tk, d.E, mx, router);
+    if (p.layer) return 1;
+    return (route_small_fits(d.T, d.E, d.k) ? 1 : 2) + (p.fused ? 1 : 2) + 1;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -492,7 +500,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
 
     // The MXFP8 GEMMs keep the weights on the MMA's M side at every size and
     // take tiles of at most 64 tokens.
-    const BnPlan plan = bn_plan(tk, E, W.mx);
+    const BnPlan plan = bn_plan(tk, E, W.mx, w_router != nullptr);
     const int bn_gu = plan.gu, bn_dn = plan.dn;
     const int num_sms = sm_count();
     if (num_sms <= 0) return MOE_ERR_CUDA;
@@ -584,6 +592,34 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
             return MOE_ERR_CUDA;
         lsrc = LogitSrc{partial, rp.splits, static_cast<size_t>(T) * E, logits_out};
     }
+    if (plan.layer) {
+        // The whole layer in one launch: its time is stage 0's, the others are empty.
+        int* ready = reinterpret_cast<int*>(ws + L.ready);
+        LayerArgs la{};
+        la.score_fn = d->score_fn;
+        la.bn_gu = bn_gu;
+        la.bn_dn = bn_dn;
+        la.logits = lsrc;
+        la.w_g = static_cast<const __nv_bfloat16*>(w_g);
+        la.topk_ids = topk_ids;
+        la.topk_w = topk_w;
+        la.gate_logit = gate_logit;
+        la.counts = counts;
+        la.offsets = offsets;
+        la.perm = perm;
+        la.inv = inv;
+        la.rt_gu = rt_gu;
+        la.rt_dn = rt_dn;
+        la.meta = meta;
+        la.ids_out = topk_ids_out;
+        la.w_out = topk_w_out;
+        la.counts_out = expert_counts_out;
+        la.out = static_cast<__nv_bfloat16*>(out);
+        if (launch_layer_fused(bn_gu, gu, dn, ga, ready, la, num_sms, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        for (int i = 1; i <= MOE_NUM_STAGES; ++i) mark_stage(i, st);
+        return MOE_OK;
+    }
     const RouteBufs rb{topk_ids, topk_w, gate_logit, blockhist, counts, offsets,
                        perm,     inv,    rt_gu,      rt_dn,     meta};
     if (enqueue_routing(T, H, E, k, d->score_fn, bn_gu, bn_dn, lsrc, w_router != nullptr, hidden,
@@ -659,7 +695,7 @@ MOE_API size_t moe_workspace_size_router(const moe_dims* d) {
 
 MOE_API int moe_launch_count_router(const moe_dims* d) {
     if (!dims_valid(d) || !dims_supported(d) || d->T == 0) return 0;
-    return launches_of(*d, false) + 1;
+    return launches_of(*d, false, true) + 1;
 }
 
 MOE_API moe_status moe_forward_mxfp8(const moe_dims* d, const void* hidden,
@@ -749,9 +785,11 @@ MOE_API int moe_launch_count_quantized(const moe_dims* d) {
     return launches_of(*d, true);
 }
 
-MOE_API void moe_set_expert_fusion(int enable) { tl_fusion = enable != 0; }
+MOE_API void moe_set_expert_fusion(int enable) {
+    tl_fusion = enable <= 0 ? 0 : (enable >= 2 ? 2 : 1);
+}
 
-MOE_API int moe_get_expert_fusion(void) { return tl_fusion ? 1 : 0; }
+MOE_API int moe_get_expert_fusion(void) { return tl_fusion; }
 
 MOE_API moe_status moe_set_stage_events(void* const* events, int n_events) {
     if (n_events == 0 || events == nullptr) {

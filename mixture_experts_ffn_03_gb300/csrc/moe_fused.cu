@@ -36,6 +36,7 @@
 // (stacked 3D expert weights; per-token sigmoid-gated shared expert).
 #include "gemm_common.cuh"
 #include "moe_fused.cuh"
+#include "routing.cuh"
 
 namespace moe {
 namespace {
@@ -147,10 +148,70 @@ struct FusedSched {
     }
 };
 
-template <int BN>
+// Whole-layer launch, before the expert phase: routing of every token (CTA b
+// takes tokens b, b + grid, ...) by the CTA's first 256 threads, with the
+// routing kernel's arithmetic; the permute by the last CTA to finish
+// (completion ticket), in the pipeline's shared memory, which no stage uses
+// yet; then every CTA waits (bounded in time) for the permute's flag. Called
+// by all threads; false if the wait gave up (the status word then says so).
+__device__ __noinline__ bool layer_prologue(uint8_t* smem, const GemmArgs& a, const LayerArgs& l,
+                                            volatile int* abort_flag, unsigned code) {
+    __shared__ float s_gate[kRouteWarps];
+    __shared__ int s_warp[kRouteWarps];
+    __shared__ int s_flag;
+    const int tid = threadIdx.x;
+    if (tid < kSmallThreads)
+        for (int t = blockIdx.x; t < a.T; t += gridDim.x)
+            route_token_cta<kLayerMaxExperts / 32>(t, a.H, a.E, a.k, l.score_fn, l.logits,
+                                                   a.hidden, l.w_g, l.topk_ids, l.topk_w,
+                                                   l.gate_logit, l.ids_out, l.w_out, s_gate);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+        s_flag = atomicAdd(&l.meta[META_TICKET], 1) == static_cast<int>(gridDim.x) - 1;
+    __syncthreads();
+    if (s_flag) {
+        __threadfence();
+        if (tid < kSmallThreads)
+            permute_small(a.T, a.E, a.k, l.bn_gu, l.bn_dn, l.topk_ids, l.counts, l.offsets, l.perm,
+                          l.inv, l.rt_gu, l.rt_dn, l.meta, l.counts_out,
+                          reinterpret_cast<int*>(smem), s_warp);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) red_release_gpu_add(&l.meta[META_PERMUTED], 1);
+    }
+    if (tid == 0) s_flag = wait_ready(&l.meta[META_PERMUTED], 1, abort_flag, a.err, code) ? 1 : 0;
+    __syncthreads();
+    return s_flag != 0;
+}
+
+// Whole-layer launch, after the expert phase (and after TMEM is released):
+// the CTA counts itself done (its epilogue warps have waited for their y
+// stores), waits (bounded) until every CTA is, then combines tokens b, b +
+// grid, ... with the combine kernel's arithmetic. No combine after an abort.
+__device__ __noinline__ void layer_epilogue(const GemmArgs& a, const LayerArgs& l,
+                                            volatile int* abort_flag, unsigned code) {
+    __shared__ int s_ok;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        fence_proxy_async_global();
+        __threadfence();
+        red_release_gpu_add(&l.meta[META_DONE], 1);
+        s_ok = wait_ready(&l.meta[META_DONE], static_cast<int>(gridDim.x), abort_flag, a.err, code)
+                   ? 1
+                   : 0;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    for (int t = blockIdx.x; t < a.T; t += gridDim.x)
+        combine_token(t, a.H, a.k, a.y, a.y + static_cast<size_t>(a.P) * a.H, l.topk_w, l.inv,
+                      l.out, tid, blockDim.x);
+}
+
+template <int BN, bool LAYER>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 expert_fused_kernel(const __grid_constant__ GemmMaps gu, const __grid_constant__ GemmMaps dn,
-                    const GemmArgs a, int* __restrict__ ready) {
+                    const GemmArgs a, int* __restrict__ ready, const LayerArgs l) {
     using C = FusedCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -168,17 +229,21 @@ expert_fused_kernel(const __grid_constant__ GemmMaps gu, const __grid_constant__
     }
     const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + 2 + kEpiWarps);
     ptx::griddep_wait();  // routing, row tiles and the slot order come from earlier kernels
+    volatile int* abort_flag = &ctl->abort;
+    const unsigned code = ERR_GATE_UP_TIMEOUT | ERR_DOWN_TIMEOUT;
+    bool permuted = true;
+    if constexpr (LAYER) permuted = layer_prologue(smem, a, l, abort_flag, code);
 
-    const int R = a.meta[META_RT_GU];
+    const int R = permuted ? a.meta[META_RT_GU] : 0;
     const int F_gu = (a.I + kGemmBM - 1) / kGemmBM, F_s = (a.I_s + kGemmBM - 1) / kGemmBM;
     const int F_h = (a.H + kGemmBM - 1) / kGemmBM;
     const int RT_s = (a.T + BN - 1) / BN;
     const int tk = a.T * a.k;
-    volatile int* abort_flag = &ctl->abort;
     unsigned* err = a.err;
-    const unsigned code = ERR_GATE_UP_TIMEOUT | ERR_DOWN_TIMEOUT;
 
-    if (warp == 0) {
+    if (!permuted) {
+        // no tile lists: no role runs
+    } else if (warp == 0) {
         if (lane == 0) {  // ---------------------------------- tiles + TMA producer
             const uint64_t pol_w = ptx::policy_evict_normal();
             const uint64_t pol_h = ptx::policy_evict_last();  // h rows are re-read per feature block
@@ -416,22 +481,39 @@ expert_fused_kernel(const __grid_constant__ GemmMaps gu, const __grid_constant__
                 aph ^= 1u;
             }
         }
-        if (lane == 0) ptx::bulk_wait_all();
+        if (lane == 0) {
+            ptx::bulk_wait_all();
+            if constexpr (LAYER) fence_proxy_async_global();  // y is read by other CTAs next
+        }
     }
     gemm_teardown<C>(tmem_base, warp);
+    if constexpr (LAYER) layer_epilogue(a, l, abort_flag, code);
 }
 
 template <int BN>
 cudaError_t launch_fused_bn(const GemmMaps& gu, const GemmMaps& dn, const GemmArgs& a, int* ready,
                             int max_tiles, int num_sms, cudaStream_t st) {
     using C = FusedCfg<BN>;
-    cudaError_t e = cudaFuncSetAttribute(expert_fused_kernel<BN>,
+    cudaError_t e = cudaFuncSetAttribute(expert_fused_kernel<BN, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
-    return launch_kernel(expert_fused_kernel<BN>, dim3(grid), dim3(kFusedThreads), C::SMEM, st,
-                         true, gu, dn, a, ready);
+    return launch_kernel(expert_fused_kernel<BN, false>, dim3(grid), dim3(kFusedThreads), C::SMEM,
+                         st, true, gu, dn, a, ready, LayerArgs{});
+}
+
+// One CTA per SM: every CTA routes, waits for the permute, takes expert
+// tiles (or none) and combines, so the grid never exceeds what is resident.
+template <int BN>
+cudaError_t launch_layer_bn(const GemmMaps& gu, const GemmMaps& dn, const GemmArgs& a, int* ready,
+                            const LayerArgs& l, int num_sms, cudaStream_t st) {
+    using C = FusedCfg<BN>;
+    cudaError_t e = cudaFuncSetAttribute(expert_fused_kernel<BN, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(expert_fused_kernel<BN, true>, dim3(num_sms), dim3(kFusedThreads), C::SMEM,
+                         st, false, gu, dn, a, ready, l);
 }
 
 }  // namespace
@@ -442,6 +524,16 @@ cudaError_t launch_expert_fused(int bn, const GemmMaps& gu, const GemmMaps& dn, 
         case 16: return launch_fused_bn<16>(gu, dn, a, ready, max_tiles, num_sms, st);
         case 32: return launch_fused_bn<32>(gu, dn, a, ready, max_tiles, num_sms, st);
         case 64: return launch_fused_bn<64>(gu, dn, a, ready, max_tiles, num_sms, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_layer_fused(int bn, const GemmMaps& gu, const GemmMaps& dn, const GemmArgs& a,
+                               int* ready, const LayerArgs& l, int num_sms, cudaStream_t st) {
+    switch (bn) {
+        case 16: return launch_layer_bn<16>(gu, dn, a, ready, l, num_sms, st);
+        case 32: return launch_layer_bn<32>(gu, dn, a, ready, l, num_sms, st);
+        case 64: return launch_layer_bn<64>(gu, dn, a, ready, l, num_sms, st);
         default: return cudaErrorInvalidValue;
     }
 }

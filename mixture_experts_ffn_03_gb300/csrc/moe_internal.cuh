@@ -45,6 +45,8 @@ enum : int {
     META_TICKET = 3,       // block-completion counter of the routing launch
     META_SCHED_GU = 4,     // tiles claimed by the gate_up GEMM's CTAs (past their first)
     META_SCHED_DN = 5,     // tiles claimed by the down GEMM's CTAs
+    META_PERMUTED = 6,     // whole-layer launch: the permute is written
+    META_DONE = 7,         // whole-layer launch: CTAs whose expert tiles are all done
     META_WORDS = 64,
 };
 

@@ -99,6 +99,11 @@ def test_host_validation(lib):
         assert moe.launch_count_quantized(decode) == 4                      # never fused
         assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 5  # BN 160/128
         assert moe.launch_count(moe.make_dims(512, 2048, 256, 8, 512, 512, 0)) == 4   # BN 32/32
+    with moe.expert_fusion(2):
+        assert moe.get_expert_fusion() == 2
+        assert moe.launch_count(decode) == 1               # the whole layer in one launch
+        assert moe.launch_count_router(decode) == 4        # the router variant is not folded
+        assert moe.launch_count(moe.make_dims(64, 2048, 512, 8, 512, 512, 1)) == 3  # E > 256
     assert not moe.get_expert_fusion()
     assert moe.launch_count(moe.make_dims(4096, 2048, 256, 8, 512, 512, 0)) == 5
     assert moe.launch_count(moe.make_dims(0, 2048, 256, 8, 512, 512, 0)) == 0

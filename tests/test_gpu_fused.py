@@ -122,3 +122,78 @@ def test_fusion_launch_counts(moe):
     p = moe.make_dims(**wl.CONFIGS["prefill"].dims())
     with moe.expert_fusion(True):
         assert moe.launch_count(p) == 5
+
+
+# ---------------------------------------------------------------- whole layer
+# Level 2: routing, the permute, both expert GEMMs and the combine in one
+# persistent launch (decode-sized batches, E <= 256). Same arithmetic as the
+# separate launches, so the outputs, ids, weights and counts are bitwise
+# theirs; the routing-to-experts and experts-to-combine hand-offs are the
+# launch's bounded grid-wide waits.
+LAYER_CASES = [c for c in CASES if c.E <= 256] + [
+    # 256 tokens: more tokens than CTAs, so CTAs route and combine several each
+    wl.MoEConfig("l_many_tokens", T=256, H=256, E=256, k=8, I=128, I_s=128, score_fn=wl.SOFTMAX),
+]
+
+
+def layer_applies(moe, cfg):
+    d = moe.make_dims(**cfg.dims())
+    with moe.expert_fusion(2):
+        return moe.launch_count(d) == 1
+
+
+def run_layer(moe, cfg, x, level):
+    layer = moe.MoELayer(x["w_gate_up"], x["w_down"], x["ws_gate_up"], x["ws_down"], x["w_g"],
+                         cfg.k, cfg.score_fn)
+    ids = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
+    counts = torch.full((cfg.E,), -1, dtype=torch.int32, device="cuda")
+    with moe.expert_fusion(level):
+        out = layer.forward(x["hidden"], x["logits"], topk_ids=ids, topk_w=w, counts=counts)
+        st = moe.device_status(layer.workspace(cfg.T))
+    assert st == moe.MOE_OK, moe.status_string(st)
+    torch.cuda.synchronize()
+    return layer, out, ids, w, counts
+
+
+@pytest.mark.parametrize("cfg", LAYER_CASES, ids=lambda c: c.name)
+def test_layer_launch_bitwise_equals_separate(moe, cfg):
+    assert layer_applies(moe, cfg)
+    inp = wl.make_inputs(cfg, seed=7)
+    x = {n: t.cuda() for n, t in inp.items()}
+    _, out_l, ids_l, w_l, c_l = run_layer(moe, cfg, x, 2)
+    _, out_s, ids_s, w_s, c_s = run_layer(moe, cfg, x, 0)
+    assert torch.equal(ids_l, ids_s) and torch.equal(c_l, c_s)
+    assert torch.equal(w_l.view(torch.int32), w_s.view(torch.int32))
+    assert torch.equal(out_l.view(torch.int16), out_s.view(torch.int16)), \
+        f"{(out_l != out_s).sum().item()} elements differ"
+    check_output(out_l, oracle.moe_forward(inp, cfg.k, cfg.score_fn)["out"], cfg.name)
+
+
+def test_layer_launch_decode_full_size_and_repeats(moe):
+    cfg = wl.CONFIGS["decode"]
+    assert layer_applies(moe, cfg)
+    x = wl.make_inputs(cfg, seed=0, device="cuda")
+    layer, out0, *_ = run_layer(moe, cfg, x, 2)
+    out0 = out0.clone()
+    _, out_s, *_ = run_layer(moe, cfg, x, 0)
+    assert torch.equal(out0.view(torch.int16), out_s.view(torch.int16))
+    out = torch.empty_like(out0)
+    differ = torch.zeros((), dtype=torch.int64, device=out.device)
+    with moe.expert_fusion(2):
+        for _ in range(100):
+            layer.forward(x["hidden"], x["logits"], out=out)
+            differ += (out.view(torch.int16) != out0.view(torch.int16)).any().to(torch.int64)
+        st = moe.device_status(layer.workspace(cfg.T))
+    assert st == moe.MOE_OK, moe.status_string(st)
+    assert int(differ) == 0
+
+
+def test_layer_launch_applies_only_to_decode_sized_batches(moe):
+    with moe.expert_fusion(2):
+        assert moe.launch_count(moe.make_dims(**wl.CONFIGS["decode"].dims())) == 1
+        # more than 256 experts, or more than 2048 (token, slot) pairs: separate launches
+        assert moe.launch_count(moe.make_dims(**wl.CONFIGS["wide"].dims())) == 4
+        assert moe.launch_count(moe.make_dims(**wl.CONFIGS["prefill"].dims())) == 5
+        # the router variant keeps its own launches
+        assert moe.launch_count_router(moe.make_dims(**wl.CONFIGS["decode"].dims())) == 4
