@@ -444,392 +444,6 @@ gate_up_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
     gemm_teardown<C>(tmem_base, warp);
 }
 
-// ====================================================== gate_up, tokens on M
-// The gate_up GEMM with the token rows on the MMA's M side (M = 128, the
-// tile's BN rows used) and the 128 gate + 128 up weight rows on N = 256. One
-// MMA then covers 256 x 16 weights, twice as many as with the weights on M,
-// which halves the MMA instructions per weight byte. The converter warps
-// dequantise each half stage (64 K values) of the 256 weight rows into a
-// 128-byte-swizzled bf16 tile in shared memory (the MMA's B operand: 32 KB,
-// gate rows then up rows), in a ring of A_STAGES such tiles after the code
-// stages. The code stages (codes, token rows, scales) and their TMA
-// producer and row gather are those of gate_up_mx_kernel. Accumulators: two
-// stages of 128 gate + 128 up columns, tokens on the TMEM lanes; the
-// epilogue is the tokens-on-M one of the bf16 GEMM, writing h into the
-// 64-column panels that the down GEMM reads, with the NVFP4 matrix scale.
-template <int BN, bool NV>
-struct MxTsCfg {
-    using Base = MxCfg<BN, true, NV>;
-    static constexpr int KS = Base::KS;                  // 128 K values per code stage
-    static constexpr int CODE_ROW = Base::CODE_ROW;
-    static constexpr int CODE_BYTES = Base::CODE_BYTES;
-    static constexpr int SCALE_BLOCK = Base::SCALE_BLOCK;
-    static constexpr int TOK_OFF = Base::TOK_OFF;
-    static constexpr int SC_OFF = Base::SC_OFF;
-    static constexpr int STAGE_BYTES = Base::STAGE_BYTES;
-    static constexpr int W_BYTES = 2 * kGemmBM * kGemmBK * 2;  // 256 rows x 64 K bf16
-    static constexpr int A_STAGES = 2;                          // converted half-stage tiles
-    static constexpr int CONVERTER_WARPS = kCvtWarps;
-    static constexpr int CTL_BYTES = 1024;
-    static constexpr int STAGES_FIT =
-        (kSmemLimit - 1024 - CTL_BYTES - A_STAGES * W_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
-    static constexpr int W_OFF = STAGES * STAGE_BYTES;
-    static constexpr int CTL_OFF = W_OFF + A_STAGES * W_BYTES;
-    static constexpr int SMEM = 1024 + CTL_OFF + CTL_BYTES;
-    static constexpr int ACC_COLS = 2 * kGemmBM;  // 128 gate + 128 up columns
-    static constexpr int ACC_STAGES = 2;
-    static constexpr int TMEM_COLS = 512;
-    static_assert(STAGES >= 3, "pipeline depth");
-    static_assert(SMEM <= kSmemLimit, "shared memory budget");
-    static_assert(W_OFF % 1024 == 0 && W_BYTES % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
-    // The MMA reads 128 token rows from each token sub-tile although BN are
-    // loaded; the rows past BN (never used) must lie inside shared memory.
-    static_assert((STAGES - 1) * STAGE_BYTES + TOK_OFF + BN * 128 + 128 * 128 <= CTL_OFF,
-                  "token tile slack");
-    static_assert(KS == 2 * kGemmBK, "two converted halves per code stage");
-};
-
-// One converter thread's share of a half stage: weight row R (gate rows
-// 0..127, up rows 128..255) for the K values [64 h, 64 h + 64) of the code
-// stage at `codes`, dequantised into the 128-byte-swizzled bf16 tile `wt`
-// (row R at R * 128, 16-byte chunk c at c ^ (R & 7)).
-template <bool NV>
-__device__ __forceinline__ void convert_half(uint32_t codes, uint32_t sc_off, int R, int h,
-                                             uint32_t wt) {
-    const int p = R >> 7, r = R & 127;
-    const uint32_t sc = codes + sc_off + static_cast<uint32_t>(p * 128 + r);  // scales [block][plane][row]
-    const uint32_t dst = wt + static_cast<uint32_t>(R) * 128u;
-    const uint32_t dswz = static_cast<uint32_t>(R & 7);
-    if constexpr (NV) {
-        // 64-byte code rows (64-byte swizzle: chunk c of row R at c ^ ((R >> 1) & 3));
-        // this half is chunks 2h, 2h + 1 (32 values each), scale blocks 4h .. 4h + 3
-        const uint32_t row = codes + static_cast<uint32_t>(R) * 64u;
-        const uint32_t swz = static_cast<uint32_t>((R >> 1) & 3);
-        uint4 v[2];
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-            v[c] = ptx::ld_shared_v4u(row + ((static_cast<uint32_t>(2 * h + c) ^ swz) << 4));
-        uint32_t s[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) s[j] = ptx::ld_shared_u8(sc + (4 * h + j) * 256);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            uint32_t o[16];
-            nv_dequant32(v[c], e4m3_to_bf16x2(s[2 * c]), e4m3_to_bf16x2(s[2 * c + 1]), o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                ptx::st_shared_v4u(dst + ((static_cast<uint32_t>(4 * c + q) ^ dswz) << 4),
-                                   o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
-    } else {
-        // 128-byte code rows (128-byte swizzle); this half is chunks 4h .. 4h + 3
-        // (16 values each), scale blocks 2h, 2h + 1
-        const uint32_t row = codes + static_cast<uint32_t>(R) * 128u;
-        const uint32_t swz = static_cast<uint32_t>(R & 7);
-        uint4 v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            v[c] = ptx::ld_shared_v4u(row + ((static_cast<uint32_t>(4 * h + c) ^ swz) << 4));
-        uint32_t s[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) s[j] = ptx::ld_shared_u8(sc + (2 * h + j) * 256);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o[8];
-            mx_dequant16(v[c], s[c >> 1], o);
-            ptx::st_shared_v4u(dst + ((static_cast<uint32_t>(2 * c) ^ dswz) << 4), o[0], o[1], o[2],
-                               o[3]);
-            ptx::st_shared_v4u(dst + ((static_cast<uint32_t>(2 * c + 1) ^ dswz) << 4), o[4], o[5],
-                               o[6], o[7]);
-        }
-    }
-}
-
-template <int BN, bool NV>
-__global__ void __launch_bounds__(kMxThreads, 1)
-gate_up_mx_ts_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
-    using C = MxTsCfg<BN, NV>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::CTL_OFF);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ptx::griddep_launch_dependents();
-    if (warp == 0 && lane == 0) {
-        ptx::prefetch_tmap(&maps.w);
-        ptx::prefetch_tmap(&maps.ws);
-        ptx::prefetch_tmap(&maps.sc);
-        ptx::prefetch_tmap(&maps.scs);
-    }
-    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + 2 + kEpiWarps + kCvtWarps);
-    ptx::griddep_wait();  // routing, tile lists and the slot order come from earlier kernels
-
-    const int R = a.meta[META_RT_GU];
-    const int F = a.I / kGemmBM, F_s = a.I_s / kGemmBM;
-    const int shared_tiles = ((a.T + BN - 1) / BN) * F_s;
-    const int num_tiles = R * F + shared_tiles;
-    const int ksteps = a.H / C::KS;
-    volatile int* abort_flag = &ctl->abort;
-    unsigned* err = a.err;
-    const unsigned code = ERR_GATE_UP_TIMEOUT;
-
-    if (warp == 0) {
-        if (lane == 0) {  // ---------------------------------- TMA producer
-            const uint64_t pol = ptx::policy_evict_normal();
-            int s = 0;
-            uint32_t ph = 0, armed = 0, parity_bits = 0;
-            bool ok = true;
-            TileSched<BN> sch;
-            Tile ti = sch.start(num_tiles, shared_tiles, F, F_s, a);
-            int qs = 0;
-            uint32_t qph = 0;
-            ok = tq_publish(ctl, qs, qph, ti, abort_flag, err, code);
-            for (; ok && ti.n_rows >= 0;
-                 ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
-                sch.prefetch(a);
-                const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
-                const CUtensorMap* tsc = ti.shared ? &maps.scs : &maps.sc;
-                const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
-                const int blk0 = ti.shared ? 0 : ti.e * (a.H / C::SCALE_BLOCK);
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* st = smem + s * C::STAGE_BYTES;
-                    const uint32_t fb = bar_addr(&ctl->full_a[s]);
-                    ptx::mbar_arrive_expect_tx(fb, C::CODE_BYTES + C::Base::SCALE_BYTES);
-                    ptx::tma_load_3d(ptx::smem_u32(st), tw, fb, ks * C::CODE_ROW, row_g, 0, pol);
-                    ptx::tma_load_3d(ptx::smem_u32(st + C::SC_OFF), tsc, fb, ti.f * kGemmBM, 0,
-                                     blk0 + ks * (C::KS / C::SCALE_BLOCK), pol);
-                    armed |= 1u << s;
-                    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
-                    if (++s == C::STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (!ok) drain_tma<C::STAGES>(ctl, armed, parity_bits);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {  // ---------------------------------- MMA issuer
-            int s = 0, as = 0, t = 0;
-            uint32_t ph = 0, aph = 0, tph = 0;
-            bool ok = true;
-            int qs = 0;
-            uint32_t qph = 0;
-            Tile ti;
-            // D[token, 0:128] = gate, D[token, 128:256] = up
-            const uint32_t idesc = ptx::idesc_bf16_f32(kGemmBM, 2 * kGemmBM);
-            while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
-                if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d = tmem_base + as * C::ACC_COLS;
-                for (int ks = 0; ks < ksteps && ok; ++ks) {
-                    if (!wait_bar(bar_addr(&ctl->full_b[s]), ph, abort_flag, err, code)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + C::TOK_OFF);
-                    for (int h = 0; h < 2; ++h) {
-                        if (!wait_bar(bar_addr(&ctl->a_full[t]), tph, abort_flag, err, code)) {
-                            ok = false;
-                            break;
-                        }
-                        // gathered rows (cp.async) and converted weights (generic stores)
-                        ptx::fence_proxy_async_smem();
-                        ptx::tc_fence_after();
-                        const uint64_t da = ptx::smem_desc_sw128(sb + h * (BN * 128));
-                        const uint64_t dw =
-                            ptx::smem_desc_sw128(ptx::smem_u32(smem + C::W_OFF + t * C::W_BYTES));
-#pragma unroll
-                        for (int kk = 0; kk < kGemmBK / 16; ++kk)
-                            ptx::mma_bf16_ss(d, da + 2 * kk, dw + 2 * kk, idesc,
-                                             (ks | h | kk) != 0 ? 1u : 0u);
-                        ptx::mma_commit(bar_addr(&ctl->a_empty[t]));
-                        if (++t == C::A_STAGES) {
-                            t = 0;
-                            tph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                    ptx::mma_commit(bar_addr(&ctl->empty[s]));  // codes and token rows consumed
-                    if (++s == C::STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                ptx::mma_commit(bar_addr(&ctl->tfull[as]));
-                if (++as == C::ACC_STAGES) {
-                    as = 0;
-                    aph ^= 1u;
-                }
-            }
-            if (!ok) {
-                ptx::mma_commit(bar_addr(&ctl->drain));
-                wait_bounded(bar_addr(&ctl->drain), 0);
-            }
-        }
-    } else if (warp < 4) {  // ------------------------------ row gather (64 threads)
-        // As in gate_up_mx_kernel: the two 64-column sub-tiles of a stage.
-        constexpr int RPT = BN / 8;
-        const int gl = (warp - 2) * 32 + lane;
-        const int c = gl & 7;
-        const int r_first = gl >> 3;
-        const uint32_t swz = static_cast<uint32_t>((c ^ r_first) << 4);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        int qs = 0;
-        uint32_t qph = 0;
-        Tile ti;
-        while (ok && tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
-            uint32_t trow[RPT];
-#pragma unroll
-            for (int j = 0; j < RPT; ++j) {
-                const int r = r_first + 8 * j;
-                uint32_t tok = 0;
-                if (r < ti.n_rows) tok = ti.shared ? ti.m0 + r : a.perm[ti.p0 + r] / a.k;
-                trow[j] = tok;
-            }
-            const __nv_bfloat16* col = a.hidden + c * 8;
-            for (int ks = 0; ks < ksteps; ++ks) {
-                if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + C::TOK_OFF);
-#pragma unroll
-                for (int sub = 0; sub < 2; ++sub) {
-                    const __nv_bfloat16* src = col + ks * C::KS + sub * 64;
-#pragma unroll
-                    for (int j = 0; j < RPT; ++j) {
-                        const int r = r_first + 8 * j;
-                        if (r < ti.n_rows)
-                            ptx::cp_async_16(sb + sub * (BN * 128) + r * 128 + swz,
-                                             src + static_cast<size_t>(trow[j]) * a.H);
-                    }
-                }
-                ptx::cp_async_arrive_noinc(bar_addr(&ctl->full_b[s]));
-                if (++s == C::STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-        ptx::cp_async_wait_all();
-    } else if (warp < kFirstCvtWarp) {  // -------------------- epilogue (warps 4-11)
-        // Tokens on TMEM lanes: warp (q, half) owns token rows 32q .. and the
-        // features [64 half, +64) of the tile; each thread writes its token's
-        // h as 32-feature runs (64 bytes) of a 64-column panel, hi and lo.
-        const int we = warp - 4, q = warp & 3, half = we >> 2;
-        int as = 0;
-        uint32_t aph = 0;
-        int qs = 0;
-        uint32_t qph = 0;
-        Tile ti;
-        while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
-            if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
-            ptx::tc_fence_after();
-            const int r0 = q * 32;
-            if (r0 < ti.n_rows) {
-                const bool sh = ti.shared != 0;
-                const int n_feat = sh ? a.I_s : a.I;
-                const size_t P = sh ? static_cast<size_t>(a.T) : static_cast<size_t>(a.P);
-                __nv_bfloat16* hbase = sh ? a.hs_hi : a.h_hi;
-                const bool row_ok = r0 + lane < ti.n_rows;
-                const size_t prow = static_cast<size_t>(ti.p0 + r0 + lane) * 64;
-                const float msc = matrix_scale(a, ti);  // NVFP4 matrix scale (1 for MXFP8)
-                const uint32_t tb = tmem_base + as * C::ACC_COLS + (static_cast<uint32_t>(r0) << 16);
-                for (int c = half * 64; c < half * 64 + 64; c += 32) {
-                    const int fb = ti.f * kGemmBM + c;
-                    if (fb >= n_feat) break;  // I, I_s are multiples of 128
-                    uint32_t g[32], u[32];
-                    ptx::tmem_ld_32x32b_x32(tb + c, g);
-                    ptx::tmem_ld_32x32b_x32(tb + kGemmBM + c, u);
-                    ptx::tmem_ld_wait();
-                    if (row_ok) {
-                        uint32_t hi2[16], lo2[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float g0 = msc * __uint_as_float(g[2 * j]);
-                            const float g1 = msc * __uint_as_float(g[2 * j + 1]);
-                            const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * (msc * __uint_as_float(u[2 * j]));
-                            const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * (msc * __uint_as_float(u[2 * j + 1]));
-                            const __nv_bfloat162 hp = __floats2bfloat162_rn(h0, h1);
-                            const __nv_bfloat162 lp =
-                                __floats2bfloat162_rn(h0 - __low2float(hp), h1 - __high2float(hp));
-                            hi2[j] = *reinterpret_cast<const uint32_t*>(&hp);
-                            lo2[j] = *reinterpret_cast<const uint32_t*>(&lp);
-                        }
-                        __nv_bfloat16* panel = hbase + static_cast<size_t>(fb >> 6) * 2 * P * 64 +
-                                               prow + (fb & 63);
-                        uint4* phi = reinterpret_cast<uint4*>(panel);
-                        uint4* plo = reinterpret_cast<uint4*>(panel + P * 64);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            phi[v] = make_uint4(hi2[4 * v], hi2[4 * v + 1], hi2[4 * v + 2], hi2[4 * v + 3]);
-                            plo[v] = make_uint4(lo2[4 * v], lo2[4 * v + 1], lo2[4 * v + 2], lo2[4 * v + 3]);
-                        }
-                    }
-                }
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
-            if (++as == C::ACC_STAGES) {
-                as = 0;
-                aph ^= 1u;
-            }
-        }
-    } else {  // --------------------------------------------- converters (warps 12-19)
-        // Thread ct converts weight row ct (gate rows 0..127, up rows 128..255)
-        // of both halves of every code stage.
-        const int ct = (warp - kFirstCvtWarp) * 32 + lane;
-        int s = 0, t = 0;
-        uint32_t ph = 0, tph = 0;
-        int qs = 0;
-        uint32_t qph = 0;
-        Tile ti;
-        bool ok = true;
-        while (ok && tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
-            for (int ks = 0; ks < ksteps && ok; ++ks) {
-                if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t codes = ptx::smem_u32(smem + s * C::STAGE_BYTES);
-                for (int h = 0; h < 2; ++h) {
-                    if (!wait_bar(bar_addr(&ctl->a_empty[t]), tph ^ 1u, abort_flag, err, code)) {
-                        ok = false;
-                        break;
-                    }
-                    convert_half<NV>(codes, C::SC_OFF, ct, h,
-                                     ptx::smem_u32(smem + C::W_OFF + t * C::W_BYTES));
-                    ptx::fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->a_full[t]));
-                    if (++t == C::A_STAGES) {
-                        t = 0;
-                        tph ^= 1u;
-                    }
-                }
-                if (++s == C::STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-    }
-    gemm_teardown<C>(tmem_base, warp);
-}
-
 // =================================================================== down
 template <int BN, bool NV>
 __global__ void __launch_bounds__(kMxThreads, 1)
@@ -984,11 +598,10 @@ down_mx_kernel(const __grid_constant__ MxMaps maps, const GemmArgs a) {
 template <int BN, bool GU, bool NV>
 cudaError_t launch_mx_bn(const MxMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
                          cudaStream_t st) {
-    // gate_up: tokens on M (gate_up_mx_ts_kernel); down: weights on M.
-    using C = std::conditional_t<GU, MxTsCfg<BN, NV>, MxCfg<BN, GU, NV>>;
+    using C = MxCfg<BN, GU, NV>;
     void (*kern)(MxMaps, GemmArgs);
     if constexpr (GU)
-        kern = gate_up_mx_ts_kernel<BN, NV>;
+        kern = gate_up_mx_kernel<BN, NV>;
     else
         kern = down_mx_kernel<BN, NV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
