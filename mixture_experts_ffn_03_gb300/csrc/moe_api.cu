@@ -137,6 +137,61 @@ bool make_pair_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major bf16 matrix [rows, inner] (inner a multiple of 64) viewed as
+// {64, rows, inner / 64}: a box of 64 x box_rows x kc lands as kc consecutive
+// 64-column chunks of box_rows rows each (128-byte swizzle), the layout of kc
+// separate 2D boxes in one request; chunks past `inner` read as zero.
+bool make_chunk_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint32_t box_rows, uint32_t kc) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kGemmBK), rows, inner / kGemmBK};
+    cuuint64_t strides[2] = {inner * 2, static_cast<cuuint64_t>(kGemmBK) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kGemmBK), box_rows, kc};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The pair map above (two matrices [rows, inner], `plane_bytes` apart) viewed
+// as {64, rows, 2, inner / 64}: a box of 64 x box_rows x 2 x kc lands as kc
+// chunks, each the first matrix's rows then the second's.
+bool make_pair_chunk_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                         uint64_t plane_bytes, uint32_t box_rows, uint32_t kc) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kGemmBK), rows, 2, inner / kGemmBK};
+    cuuint64_t strides[3] = {inner * 2, plane_bytes, static_cast<cuuint64_t>(kGemmBK) * 2};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(kGemmBK), box_rows, 2, kc};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand maps of the bf16 down GEMM (GemmMaps w, ws, h, hs): W_down [E*H, I],
+// Ws_down [H, I_s] and the h_hi / h_lo planes of [P, I] and [T, I_s]. The
+// 128-token tokens-on-M kernel reads 256 weight rows per request; the fused
+// expert launch 64-K steps; down_kernel kDownChunks 64-K chunks per request.
+bool make_down_maps(GemmMaps* dn, const void* w_down, const void* ws_down, const void* h_hi,
+                    const void* hs_hi, uint64_t h_plane, uint64_t hs_plane, uint64_t E, uint64_t H,
+                    uint64_t I, uint64_t Is, uint64_t T, uint64_t P, int bn_dn, bool fused) {
+    const uint32_t bn = static_cast<uint32_t>(bn_dn);
+    if (bn_dn == 128 || fused) {
+        const uint32_t w_rows = bn_dn == 128 ? 256u : static_cast<uint32_t>(kGemmBM);
+        return make_map(&dn->w, w_down, I, E * H, w_rows) &&
+               make_map(&dn->ws, ws_down, Is, H, w_rows) &&
+               make_pair_map(&dn->h, h_hi, I, P, h_plane, bn) &&
+               make_pair_map(&dn->hs, hs_hi, Is, T, hs_plane, bn);
+    }
+    const uint32_t kc = kDownChunks;
+    return make_chunk_map(&dn->w, w_down, I, E * H, kGemmBM, kc) &&
+           make_chunk_map(&dn->ws, ws_down, Is, H, kGemmBM, kc) &&
+           make_pair_chunk_map(&dn->h, h_hi, I, P, h_plane, bn, kc) &&
+           make_pair_chunk_map(&dn->hs, hs_hi, Is, T, hs_plane, bn, kc);
+}
+
 // Tiled map of `rank` dimensions over bytes (dt UINT8) or bf16; dims and box
 // innermost first, strides[i] = byte stride of dimension i + 1.
 bool make_map_nd(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
@@ -404,8 +459,8 @@ struct RouteBufs {
 };
 
 // Routing and the permute (stage 0, and the scatter as stage 1): one launch
-// when T*k <= 2048, else routing with the block histograms, then the scatter.
-// The status words (and, for large batches, the block histograms) must be
+// when T*k <= 2048, else routing with the block histograms, then the scatter
+// (whose launch also computes the gate logits). The status words (and, for large batches, the block histograms) must be
 // zero.
 cudaError_t enqueue_routing(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
                             const LogitSrc& lsrc, bool pdl, const void* hidden, const void* w_g,
@@ -421,12 +476,13 @@ cudaError_t enqueue_routing(int T, int H, int E, int k, int score_fn, int bn_gu,
         mark_stage(1, st);
         return e;
     }
-    e = launch_route_count(T, H, E, k, score_fn, bn_gu, bn_dn, lsrc, pdl, x, g, b.topk_ids,
-                           b.topk_w, b.gate_logit, b.blockhist, b.counts, b.offsets, b.rt_gu,
-                           b.rt_dn, b.meta, ids_out, w_out, counts_out, st);
+    e = launch_route_count(T, E, k, score_fn, bn_gu, bn_dn, lsrc, pdl, b.topk_ids, b.topk_w,
+                           b.blockhist, b.counts, b.offsets, b.rt_gu, b.rt_dn, b.meta, ids_out,
+                           w_out, counts_out, st);
     if (e != cudaSuccess) return e;
     mark_stage(1, st);
-    return launch_scatter(T, E, k, b.topk_ids, b.blockhist, b.offsets, b.perm, b.inv, st);
+    return launch_scatter(T, H, E, k, b.topk_ids, b.blockhist, b.offsets, b.perm, b.inv, x, g,
+                          b.gate_logit, st);
 }
 
 // Bytes of the status block (and the block histograms of large batches) a
@@ -515,15 +571,12 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         // rows follow I rows later, so a map over the first E*2I - I rows with a plane stride
         // of I rows reaches both (and no address past the tensor); likewise I_s for the
         // shared expert. down: 128-token tiles read 256 weight rows per request.
-        const uint32_t dn_w_rows = bn_dn == 128 ? 256u : static_cast<uint32_t>(kGemmBM);
         ok = make_pair_map(&gu.w, W.gate_up, H, static_cast<uint64_t>(E) * 2 * I - I,
                            static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
              make_pair_map(&gu.ws, W.s_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2,
                            kGemmBM) &&
-             make_map(&dn.w, W.down, I, static_cast<uint64_t>(E) * H, dn_w_rows) &&
-             make_map(&dn.ws, W.s_down, Is, H, dn_w_rows) &&
-             make_pair_map(&dn.h, h_hi, I, tk, L.h_lo - L.h_hi, bn_dn) &&
-             make_pair_map(&dn.hs, hs_hi, Is, T, L.hs_lo - L.hs_hi, bn_dn);
+             make_down_maps(&dn, W.down, W.s_down, h_hi, hs_hi, L.h_lo - L.h_hi,
+                            L.hs_lo - L.hs_hi, E, H, I, Is, T, tk, bn_dn, plan.fused);
         ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
              make_y24_store_map(&dn.st[1], y, H, tk + T);
     }
@@ -1007,10 +1060,8 @@ MOE_API moe_status moe_ep_experts(const moe_ep_dims* d, int32_t R, const void* x
     bool ok = make_pair_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E_loc) * 2 * I - I,
                             static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
               make_pair_map(&gu.ws, ws_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2, kGemmBM) &&
-              make_map(&dn.w, w_down, I, static_cast<uint64_t>(E_loc) * H, kGemmBM) &&
-              make_map(&dn.ws, ws_down, Is, H, kGemmBM) &&
-              make_pair_map(&dn.h, h_hi, I, Rm, L.h_lo - L.h_hi, bn_dn) &&
-              make_pair_map(&dn.hs, hs_hi, Is, Tm, L.hs_lo - L.hs_hi, bn_dn) &&
+              make_down_maps(&dn, w_down, ws_down, h_hi, hs_hi, L.h_lo - L.h_hi, L.hs_lo - L.hs_hi,
+                             E_loc, H, I, Is, Tm, Rm, bn_dn, false) &&
               make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H,
                              static_cast<uint64_t>(R) + T);
     if (!ok) return MOE_ERR_CUDA;

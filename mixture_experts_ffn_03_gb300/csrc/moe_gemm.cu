@@ -44,16 +44,22 @@ struct Cfg {
     static constexpr bool TS = GU && BN <= 128;
     static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;  // 16 KB weight tile
     static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
-    static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : (A_BYTES + 2 * B_BYTES);
+    // down: a stage holds KC consecutive 64-K chunks, loaded as one weight
+    // request ([chunk][128 rows]) and one h request ([chunk][h_hi, h_lo][BN
+    // rows]): at decode widths the h tile is small, and two requests per 20 KB
+    // left the TMA request rate, not HBM, setting the pace.
+    static constexpr int KC = GU ? 1 : kDownChunks;
+    static constexpr int STAGE_BYTES = GU ? (2 * A_BYTES + B_BYTES) : KC * (A_BYTES + 2 * B_BYTES);
     static constexpr int CTL_BYTES = 1024;
     // Store staging: gate_up stages each chunk in one buffer per epilogue warp
     // and writes it with plain stores; down uses TMA stores from two buffers
-    // per warp, or one when that buys the pipeline a fourth stage.
+    // per warp, or one when that buys the pipeline another stage.
     static constexpr int STAGES_2BUF =
         (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * 2 * kStgBytes) / STAGE_BYTES;
     static constexpr int STAGES_1BUF =
         (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * kStgBytes) / STAGE_BYTES;
-    static constexpr int EPI_BUFS = (GU || (STAGES_2BUF < 4 && STAGES_1BUF >= 4)) ? 1 : 2;
+    static constexpr int EPI_BUFS =
+        (GU || (STAGES_1BUF > STAGES_2BUF && STAGES_2BUF < kMaxStages)) ? 1 : 2;
     static constexpr int EPI_BYTES = TS ? 0 : kEpiWarps * EPI_BUFS * kStgBytes;
     // TS: the MMA reads the token tile as 128 rows although only BN are loaded
     // (results of the extra rows are never used), so 16 KB - B_BYTES of
@@ -81,6 +87,7 @@ struct Cfg {
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
     static_assert(BN % 8 == 0, "row gather: 8 rows per pass");
     static_assert(GU || BN <= 128, "down: h_hi and h_lo rows share one MMA of N <= 256");
+    static_assert(A_BYTES % 1024 == 0 && (2 * B_BYTES) % 1024 == 0, "chunks keep the swizzle phase");
 };
 
 // ================================================================ gate_up
@@ -392,7 +399,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             for (; ok && ti.n_rows >= 0;
                  ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
                 sch.prefetch(a);
-                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const int ksteps = ((ti.shared ? a.I_s : a.I) / kGemmBK + C::KC - 1) / C::KC;
                 const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
                 const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
                 const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * kGemmBM;
@@ -403,10 +410,11 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     }
                     const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
                     const uint32_t fb = bar_addr(&ctl->full_a[s]);
-                    ptx::mbar_arrive_expect_tx(fb, C::A_BYTES + 2 * C::B_BYTES);
-                    ptx::tma_load_2d(sa, tw, fb, ks * kGemmBK, row_w, pol_w);
-                    // the tile's h_hi rows, then its h_lo rows (two planes, one request)
-                    ptx::tma_load_3d(sa + C::A_BYTES, th, fb, ks * kGemmBK, ti.p0, 0, pol_h);
+                    ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    // KC chunks of 128 weight rows; then per chunk the tile's h_hi
+                    // rows and its h_lo rows (chunks past K read as zeros)
+                    ptx::tma_load_3d(sa, tw, fb, 0, row_w, ks * C::KC, pol_w);
+                    ptx::tma_load_4d(sa + C::KC * C::A_BYTES, th, fb, 0, ti.p0, 0, ks * C::KC, pol_h);
                     armed |= 1u << s;
                     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) {
@@ -426,7 +434,7 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             uint32_t qph = 0;
             Tile ti;
             while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
-                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const int ksteps = ((ti.shared ? a.I_s : a.I) / kGemmBK + C::KC - 1) / C::KC;
                 // h_lo rows sit right after the BN h_hi rows in shared memory, so
                 // one MMA of N = BN + rows covers both halves: accumulator
                 // columns [0, BN) hold W h_hi, columns [BN, BN + rows) W h_lo.
@@ -445,12 +453,16 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
-                    const uint64_t da = ptx::smem_desc_sw128(sa);
-                    const uint64_t dh = ptx::smem_desc_sw128(sa + C::A_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
-                        const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
-                        ptx::mma_bf16_ss(d, da + 2 * kk, dh + 2 * kk, idesc, acc);
+                    for (int c = 0; c < C::KC; ++c) {
+                        const uint64_t da = ptx::smem_desc_sw128(sa + c * C::A_BYTES);
+                        const uint64_t dh =
+                            ptx::smem_desc_sw128(sa + C::KC * C::A_BYTES + c * 2 * C::B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+                            const uint32_t acc = (ks | c | kk) != 0 ? 1u : 0u;
+                            ptx::mma_bf16_ss(d, da + 2 * kk, dh + 2 * kk, idesc, acc);
+                        }
                     }
                     ptx::mma_commit(bar_addr(&ctl->empty[s]));
                     if (++s == C::STAGES) {

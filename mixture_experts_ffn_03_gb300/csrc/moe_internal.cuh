@@ -52,6 +52,9 @@ enum : int {
 
 constexpr int kMaxExperts = 1024;       // routed experts per layer at most
 constexpr int kRouteWarps = 8;          // tokens per route block (one warp each)
+// 64-K chunks per pipeline stage (one TMA request each for weights and h) of
+// the bf16 down GEMM with the weights on M (down_kernel).
+constexpr int kDownChunks = 2;
 constexpr int kSmallSlots = 2048;       // T*k up to which the routing launch also permutes
 constexpr int kCountTokens = 256;       // tokens per histogram block
 constexpr int kGemmBM = 128;            // weight rows (output features) per tile
@@ -82,15 +85,16 @@ cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int b
                                  float* w_out, int* counts_out, cudaStream_t st);
 // Large batches: routing plus per-block expert histograms (blockhist, zero
 // at launch), scanned by the last CTA into counts, offsets, row tiles and
-// per-block bases; then the stable scatter of the slots.
-cudaError_t launch_route_count(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
-                               const LogitSrc& logits, bool pdl, const __nv_bfloat16* hidden,
-                               const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
-                               float* gate_logit, int* blockhist, int* counts, int* offsets,
-                               int4* rt_gu, int4* rt_dn, int* meta, int* ids_out, float* w_out,
-                               int* counts_out, cudaStream_t st);
-cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
-                           const int* offsets, int* perm, int* inv, cudaStream_t st);
+// per-block bases; then the stable scatter of the slots, in the same launch
+// as the shared-expert gate logits.
+cudaError_t launch_route_count(int T, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                               const LogitSrc& logits, bool pdl, int* topk_ids, float* topk_w,
+                               int* blockhist, int* counts, int* offsets, int4* rt_gu, int4* rt_dn,
+                               int* meta, int* ids_out, float* w_out, int* counts_out,
+                               cudaStream_t st);
+cudaError_t launch_scatter(int T, int H, int E, int k, const int* topk_ids, const int* blockhist,
+                           const int* offsets, int* perm, int* inv, const __nv_bfloat16* hidden,
+                           const __nv_bfloat16* w_g, float* gate_logit, cudaStream_t st);
 cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st);
 // Expert parallelism: the fp32 combine with the routed rows y_routed [T*k, H]

@@ -10,7 +10,10 @@
 // permute inside the same launch: the last CTA to finish routing (a completion
 // ticket) builds the whole sorted order (route_permute_kernel). Larger batches
 // take two launches: route_count_kernel (routing plus per-block expert
-// histograms; the last CTA scans them) and scatter_kernel.
+// histograms; the last CTA scans them) and scatter_kernel, whose extra CTAs
+// compute the shared-expert gate logits (they need nothing from routing, so
+// they run beside the histogram scan instead of lengthening every routing
+// warp).
 #include "routing.cuh"
 
 namespace moe {
@@ -150,15 +153,15 @@ __device__ __forceinline__ void scan_block_hist(int nb, int E, int bn_gu, int bn
 // of 256 tokens, accumulated with integer atomics (the sums do not depend on
 // their order) into blockhist, which starts at zero. The last CTA to finish
 // (a completion ticket) scans the histograms: counts, offsets, row tiles and
-// per-block bases for scatter_kernel.
+// per-block bases for scatter_kernel. The gate logits are left to
+// scatter_kernel.
 // At most 64 registers: four CTAs per SM, so a 4096-token batch routes in
 // one wave.
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32, 4)
-route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
-                   const LogitSrc logits, const __nv_bfloat16* __restrict__ hidden,
-                   const __nv_bfloat16* __restrict__ w_g, int* __restrict__ topk_ids,
-                   float* __restrict__ topk_w, float* __restrict__ gate_logit,
+route_count_kernel(int T, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                   const LogitSrc logits, int* __restrict__ topk_ids,
+                   float* __restrict__ topk_w,
                    int* __restrict__ blockhist, int* __restrict__ counts,
                    int* __restrict__ offsets, int4* __restrict__ rt_gu, int4* __restrict__ rt_dn,
                    int* __restrict__ meta, int* __restrict__ ids_out, float* __restrict__ w_out,
@@ -172,8 +175,8 @@ route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_d
     ptx::griddep_wait();  // no-op unless launched behind the router GEMM
     const int t = blockIdx.x * kRouteWarps + warp;
     if (t < T) {
-        const int e = route_and_store<EPL>(t, H, E, k, score_fn, logits, hidden, w_g, topk_ids,
-                                           topk_w, gate_logit, ids_out, w_out, lane);
+        const int e = route_and_store<EPL, false>(t, 0, E, k, score_fn, logits, nullptr, nullptr,
+                                                  topk_ids, topk_w, nullptr, ids_out, w_out, lane);
         if (lane < k) atomicAdd(&blockhist[static_cast<size_t>(t / kCountTokens) * E + e], 1);
     }
     __threadfence();
@@ -188,15 +191,32 @@ route_count_kernel(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_d
     if (tid == 0) meta[META_TICKET] = 0;
 }
 
+// CTAs [0, ceil(T / 256)): the stable scatter of the slots of 256 tokens.
+// CTAs from ceil(T / 256) on: the shared-expert gate logit z_t = x_t . w_g of
+// eight tokens each, one warp per token (GateLogit's order). Those read only
+// the layer's inputs and skip the wait for the routing launch.
 __global__ void __launch_bounds__(256)
-scatter_kernel(int T, int E, int k, const int* __restrict__ topk_ids,
+scatter_kernel(int T, int H, int E, int k, const int* __restrict__ topk_ids,
                const int* __restrict__ blockhist, const int* __restrict__ offsets,
-               int* __restrict__ perm, int* __restrict__ inv) {
+               int* __restrict__ perm, int* __restrict__ inv,
+               const __nv_bfloat16* __restrict__ hidden, const __nv_bfloat16* __restrict__ w_g,
+               float* __restrict__ gate_logit) {
     extern __shared__ int s_dyn[];
     int* s_sub = s_dyn;           // [8][E]: per-warp counts, then per-warp bases
     int* s_ids = s_dyn + 8 * E;   // [8][32 k]: each warp's slot experts
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ptx::griddep_launch_dependents();
+    const int nb = (T + kCountTokens - 1) / kCountTokens;
+    if (static_cast<int>(blockIdx.x) >= nb) {
+        const int t = (static_cast<int>(blockIdx.x) - nb) * kRouteWarps + warp;
+        if (t < T) {
+            GateLogit gl;
+            gl.load(t, H, hidden, w_g, lane, 0);
+            const float z = gl.finish(t, H, hidden, w_g, lane);
+            if (lane == 0) gate_logit[t] = z;
+        }
+        return;
+    }
     for (int i = tid; i < 8 * E; i += 256) s_sub[i] = 0;
     __syncthreads();
     ptx::griddep_wait();
@@ -469,33 +489,34 @@ cudaError_t launch_route_permute(int T, int H, int E, int k, int score_fn, int b
 #undef MOE_LAUNCH_RP
 }
 
-cudaError_t launch_route_count(int T, int H, int E, int k, int score_fn, int bn_gu, int bn_dn,
-                               const LogitSrc& logits, bool pdl, const __nv_bfloat16* hidden,
-                               const __nv_bfloat16* w_g, int* topk_ids, float* topk_w,
-                               float* gate_logit, int* blockhist, int* counts, int* offsets,
-                               int4* rt_gu, int4* rt_dn, int* meta, int* ids_out, float* w_out,
-                               int* counts_out, cudaStream_t st) {
+cudaError_t launch_route_count(int T, int E, int k, int score_fn, int bn_gu, int bn_dn,
+                               const LogitSrc& logits, bool pdl, int* topk_ids, float* topk_w,
+                               int* blockhist, int* counts, int* offsets, int4* rt_gu, int4* rt_dn,
+                               int* meta, int* ids_out, float* w_out, int* counts_out,
+                               cudaStream_t st) {
     const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
 #define MOE_LAUNCH_RC(N)                                                                        \
     return launch_kernel(route_count_kernel<N>, dim3(blocks), dim3(kRouteWarps * 32), 0, st,  \
-                         pdl, T, H, E, k, score_fn, bn_gu, bn_dn, logits, hidden, w_g,           \
-                         topk_ids, topk_w, gate_logit, blockhist, counts, offsets, rt_gu, rt_dn, \
-                         meta, ids_out, w_out, counts_out)
+                         pdl, T, E, k, score_fn, bn_gu, bn_dn, logits, topk_ids, topk_w,         \
+                         blockhist, counts, offsets, rt_gu, rt_dn, meta, ids_out, w_out,         \
+                         counts_out)
     MOE_EPL_DISPATCH(experts_per_lane(E), MOE_LAUNCH_RC)
 #undef MOE_LAUNCH_RC
 }
 
-cudaError_t launch_scatter(int T, int E, int k, const int* topk_ids, const int* blockhist,
-                           const int* offsets, int* perm, int* inv, cudaStream_t st) {
-    const int blocks = (T + kCountTokens - 1) / kCountTokens;
+cudaError_t launch_scatter(int T, int H, int E, int k, const int* topk_ids, const int* blockhist,
+                           const int* offsets, int* perm, int* inv, const __nv_bfloat16* hidden,
+                           const __nv_bfloat16* w_g, float* gate_logit, cudaStream_t st) {
+    const int blocks =
+        (T + kCountTokens - 1) / kCountTokens + (T + kRouteWarps - 1) / kRouteWarps;
     const size_t smem = (8 * static_cast<size_t>(E) + 8 * 32 * static_cast<size_t>(k)) * sizeof(int);
     if (smem > 48 * 1024) {  // E = 1024 with k = 32 needs 64 KB
         const cudaError_t e = cudaFuncSetAttribute(
             scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    return launch_kernel(scatter_kernel, dim3(blocks), dim3(256), smem, st, true, T, E, k,
-                         topk_ids, blockhist, offsets, perm, inv);
+    return launch_kernel(scatter_kernel, dim3(blocks), dim3(256), smem, st, true, T, H, E, k,
+                         topk_ids, blockhist, offsets, perm, inv, hidden, w_g, gate_logit);
 }
 
 cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,
