@@ -11,7 +11,8 @@ namespace moe {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;                     // pipeline stage barriers
+constexpr int kStageCap = 8;                       // usual pipeline depth cap
 constexpr int kSmemLimit = 232448;
 
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
@@ -248,11 +249,12 @@ __device__ __forceinline__ float matrix_scale(const GemmArgs& a, const Tile& ti)
 }
 
 // One gate_up tile with the tokens on TMEM lanes (tokens on the MMA's M side,
-// 128 gate then 128 up accumulator columns from `slot`), drained by epilogue
+// NF gate then NF up accumulator columns from `slot`), drained by epilogue
 // warp (q, half): it owns the 32 token rows 32q.. and the features
-// [64 half, +64) of the tile, and writes h = silu(gate) * up as bf16 hi/lo
+// [NF/2 half, +NF/2) of the tile, and writes h = silu(gate) * up as bf16 hi/lo
 // pairs (h_hi = bf16(h), h_lo = bf16(h - h_hi)) with 16-byte stores of its
 // own row. Warp-uniform; the whole warp calls it.
+template <int NF = kGemmBM>
 __device__ __forceinline__ void gate_up_ts_epilogue_tile(const Tile& ti, uint32_t slot, int q,
                                                          int half, int lane, const GemmArgs& a) {
     const int r0 = q * 32;  // first token row of this warp's lane quadrant
@@ -264,12 +266,12 @@ __device__ __forceinline__ void gate_up_ts_epilogue_tile(const Tile& ti, uint32_
     __nv_bfloat16* dhi = sh ? a.hs_hi : a.h_hi;
     __nv_bfloat16* dlo = sh ? a.hs_lo : a.h_lo;
     const uint32_t tb = slot + (static_cast<uint32_t>(r0) << 16);
-    for (int c = half * 64; c < half * 64 + 64; c += 32) {
-        const int fb = ti.f * kGemmBM + c;
+    for (int c = half * (NF / 2); c < (half + 1) * (NF / 2); c += 32) {
+        const int fb = ti.f * NF + c;
         if (fb >= n_feat) break;  // I, I_s are multiples of 64
         uint32_t g[32], u[32];
         ptx::tmem_ld_32x32b_x32(tb + c, g);
-        ptx::tmem_ld_32x32b_x32(tb + kGemmBM + c, u);
+        ptx::tmem_ld_32x32b_x32(tb + NF + c, u);
         ptx::tmem_ld_wait();
         if (row_ok) {
             uint32_t hi2[16], lo2[16];

@@ -571,10 +571,13 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         // rows follow I rows later, so a map over the first E*2I - I rows with a plane stride
         // of I rows reaches both (and no address past the tensor); likewise I_s for the
         // shared expert. down: 128-token tiles read 256 weight rows per request.
+        // (the tokens-on-M gate_up kernel reads gu_rows gate and up rows per tile)
+        const uint32_t gu_rows = plan.fused ? static_cast<uint32_t>(kGemmBM)
+                                            : static_cast<uint32_t>(gate_up_ts_features(bn_gu));
         ok = make_pair_map(&gu.w, W.gate_up, H, static_cast<uint64_t>(E) * 2 * I - I,
-                           static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
+                           static_cast<uint64_t>(I) * H * 2, gu_rows) &&
              make_pair_map(&gu.ws, W.s_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2,
-                           kGemmBM) &&
+                           gu_rows) &&
              make_down_maps(&dn, W.down, W.s_down, h_hi, hs_hi, L.h_lo - L.h_hi,
                             L.hs_lo - L.hs_hi, E, H, I, Is, T, tk, bn_dn, plan.fused);
         ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
@@ -615,7 +618,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     gd.sched = meta + META_SCHED_DN;
 
     const size_t routed_min = tk < static_cast<size_t>(E) ? tk : static_cast<size_t>(E);
-    const int F_gu = (I + kGemmBM - 1) / kGemmBM, F_s = (Is + kGemmBM - 1) / kGemmBM;
+    const int gu_nf = W.mx || plan.fused ? kGemmBM : gate_up_ts_features(bn_gu);
+    const int F_gu = (I + gu_nf - 1) / gu_nf, F_s = (Is + gu_nf - 1) / gu_nf;
     // 128-token down tiles use the tokens-on-M kernel with 256 output features per tile.
     const int F_dn = bn_dn == 128 ? (H + 255) / 256 : (H + kGemmBM - 1) / kGemmBM;
     const size_t max_gu = (tk / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
@@ -1057,9 +1061,10 @@ MOE_API moe_status moe_ep_experts(const moe_ep_dims* d, int32_t R, const void* x
 
     GemmMaps gu{}, dn{};
     const uint64_t Rm = R > 0 ? R : 1, Tm = T > 0 ? T : 1;  // maps need non-empty dimensions
+    const uint32_t gu_rows = static_cast<uint32_t>(gate_up_ts_features(bn_gu));
     bool ok = make_pair_map(&gu.w, w_gate_up, H, static_cast<uint64_t>(E_loc) * 2 * I - I,
-                            static_cast<uint64_t>(I) * H * 2, kGemmBM) &&
-              make_pair_map(&gu.ws, ws_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2, kGemmBM) &&
+                            static_cast<uint64_t>(I) * H * 2, gu_rows) &&
+              make_pair_map(&gu.ws, ws_gate_up, H, Is, static_cast<uint64_t>(Is) * H * 2, gu_rows) &&
               make_down_maps(&dn, w_down, ws_down, h_hi, hs_hi, L.h_lo - L.h_hi, L.hs_lo - L.hs_hi,
                              E_loc, H, I, Is, Tm, Rm, bn_dn, false) &&
               make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H,
@@ -1091,7 +1096,8 @@ MOE_API moe_status moe_ep_experts(const moe_ep_dims* d, int32_t R, const void* x
     gd.sched = meta + META_SCHED_DN;
 
     const size_t routed_min = static_cast<size_t>(R) < segs ? static_cast<size_t>(R) : segs;
-    const int F_gu = (I + kGemmBM - 1) / kGemmBM, F_s = (Is + kGemmBM - 1) / kGemmBM;
+    const int F_gu = (I + static_cast<int>(gu_rows) - 1) / static_cast<int>(gu_rows);
+    const int F_s = (Is + static_cast<int>(gu_rows) - 1) / static_cast<int>(gu_rows);
     const int F_dn = (H + kGemmBM - 1) / kGemmBM;
     const size_t max_gu = (R / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
     const size_t max_dn = (R / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;

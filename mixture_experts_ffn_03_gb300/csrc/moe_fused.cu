@@ -61,7 +61,7 @@ struct FusedCfg {
     static constexpr int TAIL_BYTES =
         CTL_BYTES + (EPI_BYTES > TS_SLACK - CTL_BYTES ? EPI_BYTES : TS_SLACK - CTL_BYTES);
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT > kStageCap ? kStageCap : STAGES_FIT;
     static constexpr int A_STAGES = 0;
     static constexpr int CONVERTER_WARPS = 0;
     static constexpr int ACC_COLS = 2 * kGemmBM;  // gate_up: 128 gate + 128 up columns

@@ -42,7 +42,10 @@ struct Cfg {
     // the 128 gate + 128 up weight rows on N = 256: one MMA per K slice.
     // gate_up with BN = 256 and down keep the weights on M.
     static constexpr bool TS = GU && BN <= 128;
-    static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;  // 16 KB weight tile
+    // Weight rows per tile and operand: 128 output features, or for the
+    // tokens-on-M gate_up NF gate and NF up rows.
+    static constexpr int NF = TS ? gate_up_ts_features(BN) : kGemmBM;
+    static constexpr int A_BYTES = NF * kGemmBK * 2;       // 16 KB weight tile (8 KB at NF = 64)
     static constexpr int B_BYTES = BN * kGemmBK * 2;       // token tile
     // down: a stage holds KC consecutive 64-K chunks, loaded as one weight
     // request ([chunk][128 rows]) and one h request ([chunk][h_hi, h_lo][BN
@@ -59,7 +62,7 @@ struct Cfg {
     static constexpr int STAGES_1BUF =
         (kSmemLimit - 1024 - CTL_BYTES - kEpiWarps * kStgBytes) / STAGE_BYTES;
     static constexpr int EPI_BUFS =
-        (GU || (STAGES_1BUF > STAGES_2BUF && STAGES_2BUF < kMaxStages)) ? 1 : 2;
+        (GU || (STAGES_1BUF > STAGES_2BUF && STAGES_2BUF < kStageCap)) ? 1 : 2;
     static constexpr int EPI_BYTES = TS ? 0 : kEpiWarps * EPI_BUFS * kStgBytes;
     // TS: the MMA reads the token tile as 128 rows although only BN are loaded
     // (results of the extra rows are never used), so 16 KB - B_BYTES of
@@ -68,10 +71,13 @@ struct Cfg {
     static constexpr int TAIL_BYTES =
         CTL_BYTES + (EPI_BYTES > TS_SLACK - CTL_BYTES ? EPI_BYTES : TS_SLACK - CTL_BYTES);
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    // the 64-feature gate_up steps are half as large: let them keep as many
+    // bytes in flight as the others
+    static constexpr int STAGE_CAP = NF < kGemmBM ? kMaxStages : kStageCap;
+    static constexpr int STAGES = STAGES_FIT > STAGE_CAP ? STAGE_CAP : STAGES_FIT;
     static constexpr int A_STAGES = 0;                  // no TMEM weight stages
     static constexpr int CONVERTER_WARPS = 0;
-    static constexpr int ACC_COLS = TS ? 2 * kGemmBM : 2 * BN;  // TMEM columns per accumulator set
+    static constexpr int ACC_COLS = TS ? 2 * NF : 2 * BN;  // TMEM columns per accumulator set
     static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
     static constexpr int TMEM_USED = ACC_COLS * ACC_STAGES;
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -109,7 +115,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     ptx::griddep_wait();  // routing, tile lists and the slot order come from earlier kernels
 
     const int R = a.meta[META_RT_GU];
-    const int F = (a.I + kGemmBM - 1) / kGemmBM, F_s = (a.I_s + kGemmBM - 1) / kGemmBM;
+    const int F = (a.I + C::NF - 1) / C::NF, F_s = (a.I_s + C::NF - 1) / C::NF;
     const int shared_tiles = ((a.T + BN - 1) / BN) * F_s;
     const int num_tiles = R * F + shared_tiles;
     const int ksteps = a.H / kGemmBK;
@@ -136,7 +142,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 sch.prefetch(a);
                 const CUtensorMap* tm = ti.shared ? &maps.ws : &maps.w;
                 // gate rows f.. of the expert; the map's second plane is the up rows
-                const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * kGemmBM;
+                const int row_g = (ti.shared ? 0 : ti.e * 2 * a.I) + ti.f * C::NF;
                 for (int ks = 0; ks < ksteps; ++ks) {
                     if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
                         ok = false;
@@ -166,7 +172,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             Tile ti;
             while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
                 const int n_mma = max(16, (ti.n_rows + 15) & ~15);
-                const uint32_t idesc = C::TS ? ptx::idesc_bf16_f32(kGemmBM, 2 * kGemmBM)
+                const uint32_t idesc = C::TS ? ptx::idesc_bf16_f32(kGemmBM, 2 * C::NF)
                                              : ptx::idesc_bf16_f32(kGemmBM, n_mma);
                 if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
                     ok = false;
@@ -282,7 +288,7 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         while (tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
             if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
             ptx::tc_fence_after();
-            gate_up_ts_epilogue_tile(ti, tmem_base + as * C::ACC_COLS, q, half, lane, a);
+            gate_up_ts_epilogue_tile<C::NF>(ti, tmem_base + as * C::ACC_COLS, q, half, lane, a);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
@@ -515,7 +521,7 @@ struct DownTs {
     static constexpr int EPI_BYTES = kEpiWarps * STG_BYTES;
     static constexpr int CTL_BYTES = 1024;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - EPI_BYTES - CTL_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT > kStageCap ? kStageCap : STAGES_FIT;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;    // 1024-byte aligned (swizzled boxes)
     static constexpr int CTL_OFF = EPI_OFF + EPI_BYTES;
     static constexpr int SMEM = 1024 + CTL_OFF + CTL_BYTES;

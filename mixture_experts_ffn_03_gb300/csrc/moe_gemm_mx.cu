@@ -69,7 +69,7 @@ struct MxCfg {
     // leaves its shared memory to one more pipeline stage; down stages y.
     static constexpr int EPI_BYTES = GU ? 0 : kEpiWarps * EPI_BUFS * kStgBytes;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - CTL_BYTES - EPI_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > kMaxStages ? kMaxStages : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT > kStageCap ? kStageCap : STAGES_FIT;
     static constexpr int CTL_OFF = STAGES * STAGE_BYTES;
     static constexpr int EPI_OFF = CTL_OFF + CTL_BYTES;
     static constexpr int SMEM = 1024 + EPI_OFF + EPI_BYTES;

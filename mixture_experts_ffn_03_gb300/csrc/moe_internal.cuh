@@ -59,6 +59,11 @@ constexpr int kSmallSlots = 2048;       // T*k up to which the routing launch al
 constexpr int kCountTokens = 256;       // tokens per histogram block
 constexpr int kGemmBM = 128;            // weight rows (output features) per tile
 constexpr int kGemmBK = 64;             // K elements per pipeline stage
+// Intermediate features per gate_up tile (gate and up rows each) in the
+// tokens-on-M kernel for BN-token tiles: decode-sized tiles take 64, so that
+// the weight stream is cut into twice as many tiles and the last CTAs to run
+// out of work finish closer together; wider tiles take 128.
+constexpr int gate_up_ts_features(int bn) { return bn <= 32 ? 64 : 128; }
 constexpr int kEpiRows = 16;            // token rows per epilogue store box
 constexpr int kEpiCols = 32;            // output columns per epilogue warp (one TMEM lane each)
 
