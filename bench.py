@@ -681,9 +681,10 @@ def main():
     torch.cuda.synchronize(dev)
     e2e_serial_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
     # Serving loop (moe.HostPipeline): each step's input copy overlaps the previous
-    # step's compute and its output copy the next step's. The weights streamed every
-    # step are far larger than L2, so no flush is interleaved; the timed span runs
-    # from before the first input copy to after the last output copy.
+    # step's compute and its output copy the next step's (input and output copies on
+    # streams of their own). The weights streamed every step are far larger than L2,
+    # so no flush is interleaved; the timed span runs from before the first input
+    # copy to after the last output copy.
     pipe = moe.HostPipeline(layer, T, compute_stream=stream)
     for i in range(3):
         pipe.submit(h_host, l_host, o_hosts[i % 2])
@@ -693,7 +694,7 @@ def main():
     pipe.xs.wait_event(p0)
     for i in range(K):
         pipe.submit(h_host, l_host, o_hosts[i % 2])
-    p1.record(pipe.xs)
+    p1.record(pipe.ys)  # after the last output copy
     pipe.drain()
     e2e_ms = p0.elapsed_time(p1)
     del pipe

@@ -438,21 +438,24 @@ class MoELayerRouter(MoELayer):
 
 class HostPipeline:
     """Serving loop from pinned host buffers that overlaps host transfers with
-    compute. Each submit() copies one step's hidden rows and router logits on a
-    copy stream into one of two device staging sets, runs the layer on the
-    compute stream once they have landed, and copies the output back on the
-    copy stream once the layer is done; the next step's input copy overlaps
-    this step's compute. Every byte still crosses between host and device on
-    every step. A caller reuses an out_host buffer only after drain() (or after
-    two further submits). For a layer that computes its own router logits
+    compute. Each submit() copies one step's hidden rows and router logits on an
+    input copy stream into one of two device staging sets, runs the layer on
+    the compute stream once they have landed, and copies the output back on an
+    output copy stream once the layer is done. The two directions use separate
+    streams, so the next step's input copy overlaps this step's compute (it
+    does not queue behind this step's output copy, which waits for the
+    compute). Every byte still crosses between host and device on every step.
+    A caller reuses an out_host buffer only after drain() (or after two
+    further submits). For a layer that computes its own router logits
     (MoELayerRouter) pass logits_host=None: only the hidden rows go in."""
 
-    def __init__(self, layer, T, compute_stream=None, copy_stream=None):
+    def __init__(self, layer, T, compute_stream=None, copy_stream=None, out_stream=None):
         import torch
         self.layer = layer
         dev = layer.device
         self.cs = compute_stream or torch.cuda.current_stream(dev)
-        self.xs = copy_stream or torch.cuda.Stream(dev)
+        self.xs = copy_stream or torch.cuda.Stream(dev)      # host -> device
+        self.ys = out_stream or torch.cuda.Stream(dev)       # device -> host
         self.h = [torch.empty(T, layer.H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.l = [torch.empty(T, layer.E, dtype=torch.float32, device=dev) for _ in range(2)]
         self.o = [torch.empty(T, layer.H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
@@ -464,27 +467,30 @@ class HostPipeline:
     def submit(self, hidden_host, logits_host, out_host):
         import torch
         b = self.i % 2
-        self.xs.wait_event(self.done[b])          # step i-2 no longer reads set b
+        if self.i >= 2:
+            self.xs.wait_event(self.done[b])      # step i-2 no longer reads set b
         with torch.cuda.stream(self.xs):
             self.h[b].copy_(hidden_host, non_blocking=True)
             if logits_host is not None:
                 self.l[b].copy_(logits_host, non_blocking=True)
             self.in_ready[b].record(self.xs)
         self.cs.wait_event(self.in_ready[b])
-        self.cs.wait_event(self.out_read[b])       # step i-2's output has been copied out
+        if self.i >= 2:
+            self.cs.wait_event(self.out_read[b])  # step i-2's output has been copied out
         if logits_host is not None:
             self.layer.forward(self.h[b], self.l[b], out=self.o[b], stream=self.cs)
         else:
             self.layer.forward(self.h[b], out=self.o[b], stream=self.cs)
         self.done[b].record(self.cs)
-        self.xs.wait_event(self.done[b])
-        with torch.cuda.stream(self.xs):
+        self.ys.wait_event(self.done[b])
+        with torch.cuda.stream(self.ys):
             out_host.copy_(self.o[b], non_blocking=True)
-            self.out_read[b].record(self.xs)
+            self.out_read[b].record(self.ys)
         self.i += 1
         return out_host
 
     def drain(self):
         self.xs.synchronize()
         self.cs.synchronize()
+        self.ys.synchronize()
 

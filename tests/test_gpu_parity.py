@@ -246,7 +246,7 @@ def test_nonfinite_logits_stay_in_range(moe):
 
 
 def test_host_pipeline_matches_forward(moe):
-    """The overlapped serving loop (two staging sets, a copy stream) gives the
+    """The overlapped serving loop (two staging sets, input and output copy streams) gives the
     same bytes as plain forward calls, for alternating inputs."""
     cfg = wl.CONFIGS["tiny"].with_tokens(96)
     inps = [wl.make_inputs(cfg, seed=s) for s in (11, 12)]
