@@ -685,7 +685,10 @@ def main():
     # streams of their own). The weights streamed every step are far larger than L2,
     # so no flush is interleaved; the timed span runs from before the first input
     # copy to after the last output copy.
-    pipe = moe.HostPipeline(layer, T, compute_stream=stream)
+    # The plain bf16 layer runs the library's own serving loop (moe_pipeline_submit:
+    # host buffers through the C ABI); the other entry points the binding's loop.
+    native = type(layer) is moe.MoELayer
+    pipe = (moe.NativePipeline if native else moe.HostPipeline)(layer, T, compute_stream=stream)
     for i in range(3):
         pipe.submit(h_host, l_host, o_hosts[i % 2])
     pipe.drain()
@@ -697,6 +700,8 @@ def main():
     p1.record(pipe.ys)  # after the last output copy
     pipe.drain()
     e2e_ms = p0.elapsed_time(p1)
+    if native:
+        pipe.close()
     del pipe
 
     if rank != 0:
@@ -734,7 +739,9 @@ def main():
         down_gbs=None if (m["fused"] or m["layer"]) else work["down_bytes"] / (dn_ms / 1e3) / 1e9,
         e2e=dict(value=world * T * K / (e2e_ms / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h,
-                 mode="serving loop (moe.HostPipeline): transfers overlap neighbouring steps' compute",
+                 mode=("serving loop through the C ABI (moe_pipeline_submit, host buffers)"
+                       if native else "serving loop (moe.HostPipeline)") +
+                      ": transfers overlap neighbouring steps' compute",
                  serial_value=world * T * K / (e2e_serial_ms / 1e3)),
         gpu_launches=m["n_launch"] * K,
         clocks=m["clocks"], cuda_graph=graph)

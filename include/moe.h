@@ -27,7 +27,8 @@
  * Conventions for every entry point:
  *   - Tensor arguments are DEVICE pointers to contiguous row-major arrays,
  *     owned by the caller, 16-byte aligned. The library keeps no pointer
- *     after a call returns and allocates no device memory.
+ *     after a call returns and allocates no device memory (the one
+ *     exception: the host-memory serving loop, moe_pipeline_*, below).
  *   - bf16 arrays are passed as void* (IEEE bfloat16 bit patterns).
  *   - Work is enqueued on the caller's CUDA stream (cudaStream_t passed as
  *     void*; NULL = legacy default stream) without a host synchronisation;
@@ -103,6 +104,56 @@ moe_status moe_forward(const moe_dims* d, const void* hidden, const float* route
                        const void* ws_down, const void* w_g, void* out, int32_t* topk_ids_out,
                        float* topk_w_out, int32_t* expert_counts_out, void* workspace,
                        size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Serving loop from host memory: moe_forward fed from host buffers, with the
+ * output returned into host buffers, and the host<->device copies of
+ * neighbouring steps overlapping the compute. The layer, its arithmetic and
+ * its results are moe_forward's; this is the host-side runtime around it.
+ *
+ * moe_pipeline_create(d, w_gate_up, w_down, ws_gate_up, ws_down, w_g,
+ *                     cuda_stream, &p)
+ *   d and the weight pointers as for moe_forward (device pointers, kept by
+ *   the pipeline until it is destroyed: the weights must outlive it); T >= 1.
+ *   Unlike every other entry point, this one allocates device memory: two
+ *   staging sets of hidden [T, H] bf16, logits [T, E] fp32 and out [T, H]
+ *   bf16, one moe_forward workspace, two copy streams (non-blocking) and six
+ *   events, all on the current device and freed by moe_pipeline_destroy.
+ *   Compute runs on cuda_stream. Returns MOE_ERR_INVALID_ARG (null
+ *   pointers, invalid sizes, T = 0) or MOE_ERR_CUDA (an allocation failed;
+ *   nothing is left allocated), with *p = NULL on any error.
+ * moe_pipeline_submit(p, hidden_host, logits_host, out_host)
+ *   One step. hidden_host [T, H] bf16 and logits_host [T, E] fp32 are host
+ *   buffers (pinned for the copies to be asynchronous) copied in on the
+ *   pipeline's input stream; out_host [T, H] bf16 (host) receives the output
+ *   on its output stream. Step i uses staging set i % 2: its input copy waits
+ *   only for step i - 2's compute, so it overlaps step i - 1's compute; the
+ *   compute waits for its inputs and for step i - 2's output copy; the output
+ *   copy waits for the compute. The host buffers of a step must stay
+ *   unchanged (inputs) and unread (output) until moe_pipeline_drain returns
+ *   or two further steps have been submitted and drained. Returns after
+ *   enqueueing (no host synchronisation): MOE_ERR_INVALID_ARG for null
+ *   buffers, moe_forward's status otherwise, MOE_ERR_CUDA if a copy or event
+ *   call failed.
+ * moe_pipeline_drain(p)
+ *   Waits for every submitted step; returns moe_device_status of the
+ *   workspace (MOE_OK, or MOE_ERR_DEVICE_TIMEOUT), or MOE_ERR_CUDA.
+ * moe_pipeline_streams(p, &in_stream, &out_stream)
+ *   The pipeline's copy streams (cudaStream_t as void*; either output may be
+ *   NULL), e.g. to record timing events after the last output copy.
+ * moe_pipeline_destroy(p)
+ *   Waits for the pipeline's work and frees everything it allocated; NULL is
+ *   a no-op.
+ */
+typedef struct moe_pipeline moe_pipeline;
+moe_status moe_pipeline_create(const moe_dims* d, const void* w_gate_up, const void* w_down,
+                               const void* ws_gate_up, const void* ws_down, const void* w_g,
+                               void* cuda_stream, moe_pipeline** out);
+moe_status moe_pipeline_submit(moe_pipeline* p, const void* hidden_host, const float* logits_host,
+                               void* out_host);
+moe_status moe_pipeline_drain(moe_pipeline* p);
+moe_status moe_pipeline_streams(const moe_pipeline* p, void** in_stream, void** out_stream);
+void moe_pipeline_destroy(moe_pipeline* p);
 
 /*
  * Run the layer with MXFP8 expert weights: the same computation as

@@ -32,7 +32,9 @@ EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_statu
             "moe_selftest_wait_limit", "moe_forward_mxfp8", "moe_mxfp8_dequant",
             "moe_forward_router", "moe_workspace_size_router", "moe_launch_count_router",
             "moe_forward_nvfp4", "moe_nvfp4_dequant", "moe_launch_count_quantized",
-            "moe_set_expert_fusion", "moe_get_expert_fusion"]
+            "moe_set_expert_fusion", "moe_get_expert_fusion", "moe_pipeline_create",
+            "moe_pipeline_submit", "moe_pipeline_drain", "moe_pipeline_streams",
+            "moe_pipeline_destroy"]
 NUM_STAGES = 5
 STAGE_NAMES = ["route", "scatter", "gate_up", "down", "combine"]
 
@@ -104,6 +106,18 @@ def load_library(path: str = LIB_PATH):
     lib.moe_set_expert_fusion.restype = None
     lib.moe_get_expert_fusion.argtypes = []
     lib.moe_get_expert_fusion.restype = ctypes.c_int
+    lib.moe_pipeline_create.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 6 + [
+        ctypes.POINTER(ctypes.c_void_p)]
+    lib.moe_pipeline_create.restype = ctypes.c_int
+    lib.moe_pipeline_submit.argtypes = [P, P, P, P]
+    lib.moe_pipeline_submit.restype = ctypes.c_int
+    lib.moe_pipeline_drain.argtypes = [P]
+    lib.moe_pipeline_drain.restype = ctypes.c_int
+    lib.moe_pipeline_streams.argtypes = [P, ctypes.POINTER(ctypes.c_void_p),
+                                         ctypes.POINTER(ctypes.c_void_p)]
+    lib.moe_pipeline_streams.restype = ctypes.c_int
+    lib.moe_pipeline_destroy.argtypes = [P]
+    lib.moe_pipeline_destroy.restype = None
     _lib = lib
     return lib
 
@@ -434,6 +448,68 @@ class MoELayerRouter(MoELayer):
     def forward(self, hidden, logits=None, out=None, topk_ids=None, topk_w=None, counts=None,
                 stream=None):
         return super().forward(hidden, logits, out, topk_ids, topk_w, counts, stream)
+
+
+class NativePipeline:
+    """The library's serving loop from host memory (moe_pipeline_*) for a bf16
+    MoELayer with router logits as input: two device staging sets, an input
+    and an output copy stream owned by the library, compute on
+    ``compute_stream``. ``submit`` passes pinned host tensors (hidden [T, H]
+    bf16, logits [T, E] fp32, out [T, H] bf16) to the C call; a step's host
+    tensors must stay untouched until ``drain()`` or two further submits.
+    ``xs`` / ``ys`` are the library's input / output copy streams."""
+
+    def __init__(self, layer, T, compute_stream=None):
+        import torch
+        if type(layer) is not MoELayer:
+            raise TypeError("NativePipeline runs the bf16 moe_forward layer (MoELayer)")
+        self.layer, self.T = layer, int(T)
+        self._lib = load_library()
+        dev = layer.device
+        cs = compute_stream or torch.cuda.current_stream(dev)
+        self._dims = layer.dims(self.T)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            st = self._lib.moe_pipeline_create(
+                ctypes.byref(self._dims), _ptr(layer.w_gate_up), _ptr(layer.w_down),
+                _ptr(layer.ws_gate_up), _ptr(layer.ws_down), _ptr(layer.w_g),
+                _stream_handle(cs), ctypes.byref(h))
+        if st != MOE_OK:
+            raise MoEError(st, "moe_pipeline_create")
+        self._h = h
+        ins, outs = ctypes.c_void_p(), ctypes.c_void_p()
+        self._lib.moe_pipeline_streams(self._h, ctypes.byref(ins), ctypes.byref(outs))
+        self.xs = torch.cuda.ExternalStream(ins.value, device=dev)
+        self.ys = torch.cuda.ExternalStream(outs.value, device=dev)
+
+    def _check(self, t, dtype, cols):
+        if t.device.type != "cpu" or t.dtype != dtype or not t.is_contiguous() or \
+                tuple(t.shape) != (self.T, cols):
+            raise ValueError(f"expected a contiguous host tensor [{self.T}, {cols}] of {dtype}")
+
+    def submit(self, hidden_host, logits_host, out_host):
+        import torch
+        self._check(hidden_host, torch.bfloat16, self.layer.H)
+        self._check(logits_host, torch.float32, self.layer.E)
+        self._check(out_host, torch.bfloat16, self.layer.H)
+        st = self._lib.moe_pipeline_submit(self._h, _ptr(hidden_host), _ptr(logits_host),
+                                           _ptr(out_host))
+        if st != MOE_OK:
+            raise MoEError(st, "moe_pipeline_submit")
+        return out_host
+
+    def drain(self):
+        st = self._lib.moe_pipeline_drain(self._h)
+        if st != MOE_OK:
+            raise MoEError(st, "moe_pipeline_drain")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.moe_pipeline_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
 
 
 class HostPipeline:

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["moe_api.cu", "moe_route.cu", "moe_gemm.cu", "moe_gemm_mx.cu", "moe_router.cu", "moe_fused.cu",
-           "moe_static.cu"]
+           "moe_static.cu", "moe_pipeline.cu"]
 HEADERS = ["ptx.cuh", "moe_internal.cuh", "gemm_common.cuh", "mxfp8.cuh", "moe_fused.cuh",
            "routing.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -218,3 +218,29 @@ def test_expert_fusion_setting_is_per_host_thread(lib):
         t.join()
         assert moe.get_expert_fusion()
     assert seen == [False]
+
+
+def test_pipeline_rejects_bad_arguments_on_host(lib):
+    """The host-memory serving loop checks its arguments before allocating or
+    enqueueing anything."""
+    import mixture_experts_ffn_03_gb300 as moe
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced
+    h = P()
+    d = moe.make_dims(16, 128, 16, 4, 64, 64, 0)
+    create = lib.moe_pipeline_create
+    assert create(ctypes.byref(d), fake, fake, fake, fake, fake, None, None) == moe.MOE_ERR_INVALID_ARG
+    for i in range(5):
+        w = [fake] * 5
+        w[i] = None
+        assert create(ctypes.byref(d), *w, None, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+        assert h.value is None
+    for bad in (moe.make_dims(0, 128, 16, 4, 64, 64, 0), moe.make_dims(16, 128, 16, 17, 64, 64, 0)):
+        assert create(ctypes.byref(bad), *([fake] * 5), None, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+        assert h.value is None
+    assert create(None, *([fake] * 5), None, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pipeline_submit(None, fake, fake, fake) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pipeline_drain(None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pipeline_streams(None, None, None) == moe.MOE_ERR_INVALID_ARG
+    lib.moe_pipeline_destroy(None)  # a no-op
+

@@ -265,6 +265,29 @@ def test_host_pipeline_matches_forward(moe):
         assert torch.equal(outs[s], want[s % 2]), s
 
 
+@pytest.mark.gpu
+def test_native_pipeline_matches_forward(moe):
+    """The library's serving loop from host memory (moe_pipeline_*) gives the
+    bytes of plain forward calls, for changing inputs and more steps than
+    staging sets."""
+    cfg = wl.CONFIGS["tiny"].with_tokens(96)
+    inps = [wl.make_inputs(cfg, seed=s) for s in (21, 22, 23)]
+    dev = torch.device("cuda")
+    w = {n: t.to(dev) for n, t in inps[0].items()}
+    layer = moe.MoELayer(w["w_gate_up"], w["w_down"], w["ws_gate_up"], w["ws_down"], w["w_g"],
+                         cfg.k, cfg.score_fn)
+    want = [layer.forward(i["hidden"].to(dev), i["logits"].to(dev)).cpu() for i in inps]
+    hosts = [(i["hidden"].pin_memory(), i["logits"].pin_memory()) for i in inps]
+    outs = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(7)]
+    pipe = moe.NativePipeline(layer, cfg.T)
+    for s in range(7):
+        pipe.submit(hosts[s % 3][0], hosts[s % 3][1], outs[s])
+    pipe.drain()
+    for s in range(7):
+        assert torch.equal(outs[s], want[s % 3]), s
+    pipe.close()
+
+
 def _random_configs(n, seed=2024):
     rng = np.random.default_rng(seed)
     out = []
