@@ -616,6 +616,9 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     }
     ga.sched = meta + META_SCHED_GU;
     gd.sched = meta + META_SCHED_DN;
+    // Decode-sized batches: L2 prefetch of the first tiles' weights while routing
+    // finishes (measured: decode -1.8 us; wider tiles: no gain or slower).
+    if (!W.mx && bn_gu <= 32) ga.w_gu = static_cast<const __nv_bfloat16*>(W.gate_up);
 
     const size_t routed_min = tk < static_cast<size_t>(E) ? tk : static_cast<size_t>(E);
     const int gu_nf = W.mx || plan.fused ? kGemmBM : gate_up_ts_features(bn_gu);

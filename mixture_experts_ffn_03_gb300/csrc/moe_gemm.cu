@@ -112,10 +112,32 @@ gate_up_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         ptx::prefetch_tmap(&maps.ws);
     }
     const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + 2 + kEpiWarps);
+    const int F = (a.I + C::NF - 1) / C::NF, F_s = (a.I_s + C::NF - 1) / C::NF;
+    if (warp == 0 && lane == 0 && a.w_gu != nullptr) {
+        // While routing finishes, HBM is idle: prefetch into L2 the gate and up
+        // rows of routed tile blockIdx.x as it would be if every expert had a
+        // row tile (expert blockIdx.x / F, feature block blockIdx.x % F). Tiles
+        // are claimed in expert order, so the first wave reads about these.
+        const int e = static_cast<int>(blockIdx.x) / F, f = static_cast<int>(blockIdx.x) % F;
+        if (e < a.E) {
+            // this tile's gate rows (and as many up rows); never past the expert
+            const int rows = min(C::NF, a.I - f * C::NF);
+            const size_t plane = static_cast<size_t>(rows) * a.H * 2;
+            const uint8_t* g = reinterpret_cast<const uint8_t*>(a.w_gu) +
+                               (static_cast<size_t>(e) * 2 * a.I + static_cast<size_t>(f) * C::NF) *
+                                   a.H * 2;
+            const uint8_t* u = g + static_cast<size_t>(a.I) * a.H * 2;
+            constexpr uint32_t kChunk = 64 * 1024;
+            for (size_t o = 0; o < plane; o += kChunk) {
+                const uint32_t n = static_cast<uint32_t>(plane - o < kChunk ? plane - o : kChunk);
+                ptx::prefetch_l2_bulk(g + o, n);
+                ptx::prefetch_l2_bulk(u + o, n);
+            }
+        }
+    }
     ptx::griddep_wait();  // routing, tile lists and the slot order come from earlier kernels
 
     const int R = a.meta[META_RT_GU];
-    const int F = (a.I + C::NF - 1) / C::NF, F_s = (a.I_s + C::NF - 1) / C::NF;
     const int shared_tiles = ((a.T + BN - 1) / BN) * F_s;
     const int num_tiles = R * F + shared_tiles;
     const int ksteps = a.H / kGemmBK;

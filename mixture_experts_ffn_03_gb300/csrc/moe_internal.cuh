@@ -140,6 +140,9 @@ struct GemmArgs {
     // of the shared expert [1]; null for bf16 and MXFP8 weights.
     const float* msc;
     const float* msc_s;
+    // gate_up (bf16): the routed gate/up weights [E, 2I, H], read only by an
+    // L2 prefetch issued before the wait for routing (null: no prefetch).
+    const __nv_bfloat16* w_gu;
 };
 
 struct GemmMaps {
