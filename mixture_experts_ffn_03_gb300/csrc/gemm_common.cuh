@@ -26,7 +26,7 @@ struct Tile {
     int m0;      // first row inside the group
     int n_rows;  // valid token rows in this tile (1..BN)
     int p0;      // first row in the sorted slot order (routed) or token index (shared)
-    int f;       // 128-row block of output features
+    int f;       // block of output features (128 rows; gate_up tokens-on-M tiles: NF)
 };
 
 struct Ctl {

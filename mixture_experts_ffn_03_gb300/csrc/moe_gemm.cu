@@ -1,23 +1,29 @@
-// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),// fed by TMA, persistent and warp-specialised.
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA, persistent and warp-specialised.
 //
-// Both GEMMs put the weights on the MMA's M side (128 output features per
-// tile, one TMEM lane each) and the tokens of one expert on the N side (up to
-// BN per tile). Decode-sized groups (a few tokens per expert) then cost one
-// pass over the touched expert weights, and the same kernel serves prefill
-// with BN up to 256. Tiles come from a device-built list of (expert, first
-// row) pairs, so empty experts cost nothing and no host synchronisation is
-// needed; the shared expert is one more group appended to the list.
+// Tiles come from a device-built list of row tiles {expert, first row, rows,
+// first sorted position}, so empty experts cost nothing and no host
+// synchronisation is needed; the shared expert's tiles come first in the
+// list. Each GEMM puts the operand with 128 useful rows on the MMA's M side
+// (one TMEM lane per row) and the other on N; which one depends on the tile
+// width BN (tokens per tile):
 //
-// gate_up: for the tile's 128 intermediate features f..f+127 of expert e,
-//   G = W_gate_up[e][f.., :] X^T and U = W_gate_up[e][I+f.., :] X^T go to two
-//   TMEM accumulators that share the B operand X (the gathered hidden rows of
-//   the expert's tokens), and the epilogue writes h = silu(G) * U as a bf16
-//   high/low pair (h_hi = bf16(h), h_lo = bf16(h - h_hi)).
-// down: y = W_down[e][f.., :] (h_hi + h_lo)^T: the h_hi and h_lo rows of the
-//   tile are adjacent in shared memory and form the N side of one MMA against
-//   the same weight tile; the epilogue adds the two column blocks and writes
-//   fp32 rows of y per (token, slot); the shared expert's rows are scaled by
-//   the per-token gate sigmoid(x . w_g).
+// gate_up, BN <= 128: tokens on M (rows past the tile's end unused), NF gate
+//   rows then NF up rows of the expert on N (NF = 64 for BN <= 32, else 128),
+//   one MMA per K step, two accumulator stages; a thread owns one token in
+//   the epilogue. BN = 160 / 256: weights on M (128 gate rows, 128 up rows:
+//   two MMAs sharing the B operand X, the gathered hidden rows), one
+//   accumulator stage.
+//   The epilogue writes h = silu(G) * U as a bf16 high/low pair (h_hi =
+//   bf16(h), h_lo = bf16(h - h_hi)).
+// down, BN <= 64: weights on M (128 output features); the tile's h_hi and
+//   h_lo rows are adjacent in shared memory and form the N side of one MMA
+//   against the same weight tile; two 64-K chunks per pipeline stage; the
+//   epilogue adds the two column blocks and writes fp32 rows of y per (token,
+//   slot). BN = 128 (down_ts_kernel): tokens on M, 256 output features on N,
+//   h_hi and h_lo as two A operands into one accumulator; y as 24-bit
+//   floats. The shared expert's rows are scaled by the per-token gate
+//   sigmoid(x . w_g).
 // Sources: "Add Qwen3.5-35B-A3B (support vision and text input)", Description
 // (stacked 3D expert weights; per-token sigmoid-gated shared expert); the
 // SwiGLU expert FFN is the plain reading of the stacked gate/up layout.

@@ -151,10 +151,14 @@ struct GemmMaps {
     // together come from one 3D box whose outer dimension (2) selects the
     // member of the pair; the box lands as two consecutive tiles.
     // gate_up: w / ws = W_gate_up as [E*2I - I rows, H] x {gate, up} (plane
-    //   stride I rows), Ws_gate_up as [I_s, H] x {gate, up}; boxes 64 x 128 x 2.
-    // down: w / ws = W_down as [E*H, I] and Ws_down as [H, I_s] (2D, boxes of
-    //   64 x 128 rows, or 64 x 256 rows for 128-token tiles); h / hs = the
-    //   h_hi and h_lo planes of [T*k, I] and [T, I_s], boxes 64 x rows x 2.
+    //   stride I rows), Ws_gate_up as [I_s, H] x {gate, up}; boxes 64 x NF x 2
+    //   (NF = gate_up_ts_features(BN) gate and up rows per tile).
+    // down: w / ws = W_down as [E*H, I] and Ws_down as [H, I_s]; h / hs = the
+    //   h_hi and h_lo planes of [T*k, I] and [T, I_s]. 128-token tiles: 2D
+    //   weight boxes of 64 x 256 rows and h boxes 64 x 128 x 2; the fused
+    //   expert launch: 64 x 128 and 64 x BN x 2; down_kernel: the same boxes
+    //   with kDownChunks 64-column chunks per request (an outer dimension of
+    //   64-column chunks, 128-byte stride).
     CUtensorMap w;
     CUtensorMap ws;
     CUtensorMap h;
