@@ -295,9 +295,13 @@ const char* moe_status_string(moe_status s);
  *   (shared expert activation), y [T k + T, H] (rows [0, T k): routed
  *   expert outputs in sorted order; rows T k + t: gated shared output).
  *   y holds fp32 values, except when the mean expert group is large enough
- *   for 128-token down tiles (1.25 T k / E > 64): then each value is the top
- *   three bytes of its fp32 encoding rounded to nearest even (rows of 3 H
- *   bytes, a 16-bit significand). The region is sized for fp32 either way. */
+ *   for 128-token down tiles (1.25 T k / E > 64): then it holds y16 codes,
+ *   16 bits per value (rows of 2 H bytes) followed by an exponent plane of
+ *   one byte per 32 values of each row (row stride H/32 rounded up to a
+ *   multiple of 4): a value v of a block with exponent byte b is |v| +
+ *   2^(b-127) rounded to a 12-bit significand, stored as 4 exponent bits
+ *   relative to b, 11 fraction bits and the sign. The region is sized for
+ *   fp32 either way. */
 typedef struct {
     size_t topk_ids, topk_w, gate_logit, counts, offsets, perm, inv;
     size_t h_hi, h_lo, hs_hi, hs_lo, y;
@@ -407,7 +411,7 @@ moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream);
  *   5. moe_ep_combine: out = bf16(sum_j w_j y_back[slot j] + shared row),
  *      summed in fp32 in slot order, as in moe_forward (gather, no atomics).
  * moe_forward's results on the same tokens follow from the same arithmetic,
- * except that y is always fp32 here (no 24-bit y) and the tile widths depend
+ * except that y is always fp32 here (no y16 codes) and the tile widths depend
  * on the received rows, so outputs agree with moe_forward within the parity
  * tolerance rather than bit for bit.
  */

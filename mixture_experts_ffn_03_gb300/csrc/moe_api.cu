@@ -228,14 +228,14 @@ bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// y of 128-token down tiles: rows of H 24-bit floats (3 bytes each, byte
-// tensor [outer, 3 * inner]) written in boxes of 96 bytes x 32 rows.
-bool make_y24_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
+// y codes of 128-token down tiles (y16: rows of 2H bytes, byte tensor
+// [outer, 2 * inner]) written in boxes of 64 bytes x 32 rows.
+bool make_y16_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {3 * inner, outer};
-    cuuint64_t strides[1] = {3 * inner};
-    cuuint32_t box[2] = {96, 32};
+    cuuint64_t dims[2] = {2 * inner, outer};
+    cuuint64_t strides[1] = {2 * inner};
+    cuuint32_t box[2] = {64, 32};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -581,7 +581,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
              make_down_maps(&dn, W.down, W.s_down, h_hi, hs_hi, L.h_lo - L.h_hi,
                             L.hs_lo - L.hs_hi, E, H, I, Is, T, tk, bn_dn, plan.fused);
         ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
-             make_y24_store_map(&dn.st[1], y, H, tk + T);
+             make_y16_store_map(&dn.st[1], y, H, tk + T);
     }
     if (!ok) return MOE_ERR_CUDA;
 
@@ -604,6 +604,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     ga.hs_hi = hs_hi;
     ga.hs_lo = hs_lo;
     ga.y = y;
+    // y16 exponent plane of the 128-token down tiles, after the codes
+    ga.yexp = reinterpret_cast<uint8_t*>(y) + (tk + T) * 2 * static_cast<size_t>(H);
     ga.err = reinterpret_cast<unsigned*>(meta + META_ERR);
     GemmArgs gd = ga;
     ga.rowtiles = rt_gu;
@@ -704,7 +706,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
         mark_stage(4, st);
     }
-    // 128-token down tiles leave y as 24-bit floats, the other widths as fp32.
+    // 128-token down tiles leave y as y16 codes, the other widths as fp32.
     if ((launch_combine(T, H, k, y, !W.mx && bn_dn == 128, topk_w, inv,
                         static_cast<__nv_bfloat16*>(out), st)) != cudaSuccess)
         return MOE_ERR_CUDA;

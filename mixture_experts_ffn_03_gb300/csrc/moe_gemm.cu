@@ -21,9 +21,9 @@
 //   against the same weight tile; two 64-K chunks per pipeline stage; the
 //   epilogue adds the two column blocks and writes fp32 rows of y per (token,
 //   slot). BN = 128 (down_ts_kernel): tokens on M, 256 output features on N,
-//   h_hi and h_lo as two A operands into one accumulator; y as 24-bit
-//   floats. The shared expert's rows are scaled by the per-token gate
-//   sigmoid(x . w_g).
+//   h_hi and h_lo as two A operands into one accumulator; y as y16 codes
+//   (16 bits per value and one exponent byte per 32 values). The shared
+//   expert's rows are scaled by the per-token gate sigmoid(x . w_g).
 // Sources: "Add Qwen3.5-35B-A3B (support vision and text input)", Description
 // (stacked 3D expert weights; per-token sigmoid-gated shared expert); the
 // SwiGLU expert FFN is the plain reading of the stacked gate/up layout.
@@ -523,14 +523,6 @@ down_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     gemm_teardown<C>(tmem_base, warp);
 }
 
-// y of the 128-token down tiles is stored with a 16-bit significand: the top
-// three bytes of the fp32 encoding, rounded to nearest even on the dropped
-// byte (NaN stays NaN). The result's low byte is dropped by the caller.
-__device__ __forceinline__ uint32_t y24_round(uint32_t b) {
-    if ((b & 0x7FFFFFFFu) > 0x7F800000u) return b | 0x00400000u;
-    return b + 0x7Fu + ((b >> 8) & 1u);
-}
-
 // ====================================================== down, tokens on M
 // Tiles of up to 128 tokens of one expert against 256 output features:
 // D[token, 0:N] = h_hi W^T + h_lo W^T, where the h_hi and h_lo tiles are two A
@@ -545,7 +537,7 @@ struct DownTs {
     static constexpr int A_BYTES = BM * kGemmBK * 2;        // 16 KB: h_hi or h_lo tile
     static constexpr int W_BYTES = NF * kGemmBK * 2;        // 32 KB: weight tile (two boxes)
     static constexpr int STAGE_BYTES = 2 * A_BYTES + W_BYTES;
-    static constexpr int STG_BYTES = 32 * 32 * 4;           // one warp's store box (32 rows x 96 B used)
+    static constexpr int STG_BYTES = 32 * 32 * 4;           // one warp's store box (32 rows x 64 B used)
     static constexpr int EPI_BYTES = kEpiWarps * STG_BYTES;
     static constexpr int CTL_BYTES = 1024;
     static constexpr int STAGES_FIT = (kSmemLimit - 1024 - EPI_BYTES - CTL_BYTES) / STAGE_BYTES;
@@ -687,13 +679,15 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     } else if (warp >= 4) {  // ------------------------------ epilogue (warps 4-11)
         // Tokens on TMEM lanes: warp we owns the token rows 32*(warp % 4).. and
         // the features [128*(we / 4), +128) of the tile, drained 32 at a time.
-        // Each thread packs 32 consecutive features of its token's y row (24-bit
-        // floats, 96 bytes) into the warp's staging box, which goes out as one
-        // 96-byte x 32-row TMA store; a warp whose token rows are only partly
-        // valid stores its valid rows directly.
+        // Each thread turns 32 consecutive features of its token's y row into
+        // y16 codes (64 bytes; its own block exponent) in the warp's staging
+        // box, which goes out as one 64-byte x 32-row TMA store; a warp whose
+        // token rows are only partly valid stores its valid rows directly. The
+        // thread's four exponent bytes go out as one 4-byte store per tile.
         const int we = warp - 4, q = warp & 3, half = we >> 2;
         uint8_t* stg = smem + C::EPI_OFF + we * C::STG_BYTES;
         const uint32_t stg_u32 = ptx::smem_u32(stg);
+        const int es = y16_exp_stride(a.H);
         int as = 0;
         uint32_t aph = 0;
         const int shared_row0 = a.P;
@@ -705,56 +699,61 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             ptx::tc_fence_after();
             const int r0 = q * 32;
             const int rows_valid = ti.n_rows - r0;  // token rows of this warp that are real
-            if (rows_valid > 0) {
-                const int n_f = min(C::NF, a.H - ti.f * C::NF);
+            const int c_begin = half * (C::NF / 2);
+            const int n_f = min(C::NF, a.H - ti.f * C::NF);
+            if (rows_valid > 0 && c_begin < n_f) {
                 const int row0 = (ti.shared ? shared_row0 + ti.m0 : ti.p0) + r0;
                 float scale = 1.f;
                 if (ti.shared && lane < rows_valid)
                     scale = 1.f / (1.f + expf(-a.gate_logit[ti.m0 + r0 + lane]));
                 const uint32_t tb =
                     tmem_base + (static_cast<uint32_t>(r0) << 16) + as * C::ACC_COLS;
-                for (int col = half * (C::NF / 2); col < half * (C::NF / 2) + C::NF / 2; col += 32) {
+                uint32_t eb = 0;  // the thread's block exponents, one byte per chunk
+                for (int col = c_begin; col < c_begin + C::NF / 2; col += 32) {
                     if (col >= n_f) break;
                     const int f0 = ti.f * C::NF + col;
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(tb + col, v);
-                    // The thread's 32 values of its token's y row, rounded to 24-bit
-                    // floats and packed into 96 bytes (24 words).
                     ptx::tmem_ld_wait();
-                    uint32_t w[24];
+                    uint32_t mx = 0;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t r0 = y24_round(__float_as_uint(__uint_as_float(v[4 * q]) * scale));
-                        const uint32_t r1 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 1]) * scale));
-                        const uint32_t r2 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 2]) * scale));
-                        const uint32_t r3 = y24_round(__float_as_uint(__uint_as_float(v[4 * q + 3]) * scale));
-                        w[3 * q] = __byte_perm(r0, r1, 0x5321);
-                        w[3 * q + 1] = __byte_perm(r1, r2, 0x6532);
-                        w[3 * q + 2] = __byte_perm(r2, r3, 0x7653);
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] = __float_as_uint(__uint_as_float(v[i]) * scale);
+                        mx = max(mx, v[i] & 0x7FFFFFFFu);
                     }
+                    const uint32_t b = y16_block_exp(mx);
+                    eb |= b << (((col - c_begin) / 32) * 8);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = y16_encode(v[2 * i], b) | (y16_encode(v[2 * i + 1], b) << 16);
                     if (rows_valid >= 32) {
                         if (lane == 0) ptx::bulk_wait_read<0>();  // staging box free again
                         __syncwarp();
-                        const uint32_t row_addr = stg_u32 + lane * 96;
+                        const uint32_t row_addr = stg_u32 + lane * 64;
 #pragma unroll
-                        for (int j = 0; j < 6; ++j)
+                        for (int j = 0; j < 4; ++j)
                             ptx::st_shared_v4u(row_addr + 16 * j, w[4 * j], w[4 * j + 1], w[4 * j + 2],
                                                w[4 * j + 3]);
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&maps.st[1], stg_u32, 3 * f0, row0);
+                            ptx::tma_store_2d(&maps.st[1], stg_u32, 2 * f0, row0);
                             ptx::bulk_commit();
                         }
                     } else if (lane < rows_valid) {
                         uint4* dst = reinterpret_cast<uint4*>(
-                            reinterpret_cast<uint8_t*>(a.y) + static_cast<size_t>(row0 + lane) * 3 * a.H +
-                            3 * f0);
+                            reinterpret_cast<uint8_t*>(a.y) + static_cast<size_t>(row0 + lane) * 2 * a.H +
+                            2 * f0);
 #pragma unroll
-                        for (int j = 0; j < 6; ++j)
+                        for (int j = 0; j < 4; ++j)
                             dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                     }
                 }
+                // bytes past the row's last block fall into the padding of the stride
+                if (lane < rows_valid)
+                    *reinterpret_cast<uint32_t*>(a.yexp + static_cast<size_t>(row0 + lane) * es +
+                                                 (ti.f * C::NF + c_begin) / kY16Block) = eb;
             }
             ptx::tc_fence_before();
             __syncwarp();

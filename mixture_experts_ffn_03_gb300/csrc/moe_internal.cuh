@@ -67,6 +67,46 @@ constexpr int gate_up_ts_features(int bn) { return bn <= 32 ? 64 : 128; }
 constexpr int kEpiRows = 16;            // token rows per epilogue store box
 constexpr int kEpiCols = 32;            // output columns per epilogue warp (one TMEM lane each)
 
+// y rows of the tokens-on-M down GEMM, read by the combine ("y16"): each
+// block of 32 consecutive values of a row has one exponent byte b, the
+// biased fp32 exponent of the block's largest magnitude minus 13, clamped to
+// [1, 240]. With D = 2^(b - 127), a value v is stored as 16 bits: its sign
+// and |v| + D rounded to a 12-bit significand (nearest even), as 4 exponent
+// bits counted from b and 11 fraction bits. Decoding adds b back and
+// subtracts D, exactly. The error is at most 2^-12 (|v| + D) (a 12-bit
+// significand; D is 2^-13 to 2^-14 of the block's largest magnitude, so
+// small values get an absolute step of at most 2^-11 D), and zero is
+// exact. A block holding an infinity
+// or a NaN gets b = 240: those decode as themselves, its finite values
+// below 2^114 as zero. Layout: the codes [rows][H] (2H-byte rows), then the
+// exponent plane [rows][y16_exp_stride(H)] bytes.
+constexpr int kY16Block = 32;
+__host__ __device__ constexpr int y16_exp_stride(int H) { return (H / kY16Block + 3) & ~3; }
+
+#ifdef __CUDACC__
+// Exponent byte of a block whose largest |value| has the fp32 bits
+// `max_abs_bits` (an integer maximum of the values' bits without the sign,
+// so infinities and NaNs rank highest).
+__device__ __forceinline__ uint32_t y16_block_exp(uint32_t max_abs_bits) {
+    const int e = static_cast<int>(max_abs_bits >> 23) - 13;
+    return static_cast<uint32_t>(e < 1 ? 1 : (e > 240 ? 240 : e));
+}
+// 16-bit code of the fp32 value with bits x in a block with exponent byte b.
+__device__ __forceinline__ uint32_t y16_encode(uint32_t x, uint32_t b) {
+    const uint32_t ax = x & 0x7FFFFFFFu;
+    // |v| + D rounded to fp32, then to 12 significant bits (the first
+    // rounding moves it by at most 2^-13 of the second one's step)
+    const uint32_t c = __float_as_uint(__uint_as_float(ax) + __uint_as_float(b << 23));
+    uint32_t em = ((c + 0x7FFu + ((c >> 12) & 1u)) >> 12) - (b << 11);
+    if (ax > 0x7F800000u) em = 0x7C00u;  // NaN: all-ones exponent, nonzero fraction
+    return em | ((x >> 16) & 0x8000u);
+}
+__device__ __forceinline__ float y16_decode(uint32_t u, uint32_t b) {
+    const float f = __uint_as_float(((u & 0x7FFFu) << 12) + (b << 23)) - __uint_as_float(b << 23);
+    return __uint_as_float(__float_as_uint(f) | ((u & 0x8000u) << 16));
+}
+#endif
+
 // Where the routing kernels read the logits: the sum, in order, of `parts`
 // fp32 arrays [T, E] spaced part_stride floats apart (parts = 1: the caller's
 // logits; more: the router GEMM's split-K partial sums). `out` (optional)
@@ -100,7 +140,9 @@ cudaError_t launch_route_count(int T, int E, int k, int score_fn, int bn_gu, int
 cudaError_t launch_scatter(int T, int H, int E, int k, const int* topk_ids, const int* blockhist,
                            const int* offsets, int* perm, int* inv, const __nv_bfloat16* hidden,
                            const __nv_bfloat16* w_g, float* gate_logit, cudaStream_t st);
-cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,
+// y: fp32 rows [T*k + T, H], or with `y16` the codes and exponent plane of
+// the y16 format starting at y.
+cudaError_t launch_combine(int T, int H, int k, const float* y, bool y16, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st);
 // Expert parallelism: the fp32 combine with the routed rows y_routed [T*k, H]
 // (sorted order) and the gated shared rows y_shared [T, H] in separate arrays;
@@ -135,6 +177,7 @@ struct GemmArgs {
     __nv_bfloat16* hs_hi;
     __nv_bfloat16* hs_lo;
     float* y;
+    uint8_t* yexp;          // y16 exponent plane (tokens-on-M down tiles)
     unsigned* err;
     // NVFP4 weights: fp32 matrix scales of this GEMM's routed experts [E] and
     // of the shared expert [1]; null for bf16 and MXFP8 weights.
@@ -164,8 +207,8 @@ struct GemmMaps {
     CUtensorMap h;
     CUtensorMap hs;
     // Epilogue stores of the down GEMM: st[0] = y [T*k + T, H] fp32 in boxes of
-    // 32 columns x kEpiRows rows (no swizzle); with tokens on M, st[1] = y as
-    // 24-bit floats in boxes of 96 bytes x 32 rows. (The gate_up epilogues
+    // 32 columns x kEpiRows rows (no swizzle); with tokens on M, st[1] = the
+    // y16 codes of y in boxes of 64 bytes x 32 rows. (The gate_up epilogues
     // write h with plain stores.)
     CUtensorMap st[4];
 };

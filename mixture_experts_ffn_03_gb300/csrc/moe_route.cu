@@ -279,63 +279,38 @@ combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __
     *reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * H + h) = packed;
 }
 
-// The same combine over y stored as 24-bit floats (the top three bytes of an
-// fp32, rows of 3H bytes). A warp owns 512 consecutive outputs (lane = 16 of
-// them, 48 bytes of each y row): it reads the warp's 1536-byte row segment
-// with three fully coalesced 16-byte loads per lane and redistributes the
-// chunks with shuffles so that each lane holds its own 48 bytes; the fp32 sum
-// runs in slot order as above.
-__device__ __forceinline__ void y24_unpack(const uint4 q[3], float (&f)[16]) {
-    const uint32_t wv[12] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y,
-                             q[1].z, q[1].w, q[2].x, q[2].y, q[2].z, q[2].w};
+// The same combine over y stored as y16 codes (2H-byte rows, then one
+// exponent byte per 32 values of each row in the exponent plane). A thread
+// owns 16 consecutive outputs: per row it reads 32 contiguous bytes of codes
+// (a warp: 1 KB) and the exponent byte of their block, and the fp32 sum runs
+// in slot order as above.
+__device__ __forceinline__ void y16_row16(const uint8_t* __restrict__ codes,
+                                          const uint8_t* __restrict__ exps, float (&f)[16]) {
+    const uint4* c = reinterpret_cast<const uint4*>(codes);
+    const uint4 c0 = __ldcs(c), c1 = __ldcs(c + 1);
+    const uint32_t b = __ldcs(exps);
+    const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint32_t w0 = wv[3 * g], w1 = wv[3 * g + 1], w2 = wv[3 * g + 2];
-        f[4 * g] = __uint_as_float(__byte_perm(w0, 0u, 0x2104));
-        f[4 * g + 1] = __uint_as_float(__byte_perm(w0, w1, 0x5433) & 0xFFFFFF00u);
-        f[4 * g + 2] = __uint_as_float(__byte_perm(w1, w2, 0x4322) & 0xFFFFFF00u);
-        f[4 * g + 3] = __uint_as_float(w2 & 0xFFFFFF00u);
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = y16_decode(wv[i] & 0xFFFFu, b);
+        f[2 * i + 1] = y16_decode(wv[i] >> 16, b);
     }
-}
-
-__device__ __forceinline__ uint4 shfl_u4(const uint4& v, int src) {
-    return make_uint4(__shfl_sync(0xFFFFFFFFu, v.x, src), __shfl_sync(0xFFFFFFFFu, v.y, src),
-                      __shfl_sync(0xFFFFFFFFu, v.z, src), __shfl_sync(0xFFFFFFFFu, v.w, src));
-}
-
-// Lane l's 16 values of one y row: the warp loads chunks l, l + 32, l + 64 of
-// its segment (chunks of lanes past the row end read as zero) and lane l
-// takes chunks 3l, 3l + 1, 3l + 2.
-__device__ __forceinline__ void y24_row(const uint8_t* __restrict__ seg, int lane, int lanes_valid,
-                                        float (&f)[16]) {
-    const uint4* c = reinterpret_cast<const uint4*>(seg);
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 c0 = lane / 3 < lanes_valid ? __ldcs(c + lane) : z;
-    const uint4 c1 = (lane + 32) / 3 < lanes_valid ? __ldcs(c + 32 + lane) : z;
-    const uint4 c2 = (lane + 64) / 3 < lanes_valid ? __ldcs(c + 64 + lane) : z;
-    uint4 q[3];
-#pragma unroll
-    for (int m = 0; m < 3; ++m) {
-        const int chunk = 3 * lane + m;  // 0 .. 95
-        const int src = chunk & 31, which = chunk >> 5;
-        const uint4 a0 = shfl_u4(c0, src), a1 = shfl_u4(c1, src), a2 = shfl_u4(c2, src);
-        q[m] = which == 0 ? a0 : (which == 1 ? a1 : a2);
-    }
-    y24_unpack(q, f);
 }
 
 __global__ void __launch_bounds__(128)
-combine_y24_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
+combine_y16_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
                    const float* __restrict__ topk_w, const int* __restrict__ inv,
                    __nv_bfloat16* __restrict__ out) {
     const int t = blockIdx.x;
-    const int lane = threadIdx.x & 31;
-    const int hw = (blockIdx.y * 128 + (threadIdx.x & ~31)) * 16;  // warp's first output
+    const int h = (blockIdx.y * 128 + threadIdx.x) * 16;  // thread's first output
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    if (hw >= H) return;  // whole warp past the row end
-    const int lanes_valid = min(32, (H - hw) / 16);  // H is a multiple of 64
-    const size_t row_bytes = static_cast<size_t>(3) * H;
+    if (h >= H) return;  // H is a multiple of 64
+    const size_t rows = static_cast<size_t>(T) * k + T;
+    const uint8_t* exps = y + rows * 2 * H + h / kY16Block;
+    const size_t es = static_cast<size_t>(y16_exp_stride(H));
+    const uint8_t* codes = y + 2 * static_cast<size_t>(h);
+    const size_t row_bytes = 2 * static_cast<size_t>(H);
     const size_t tk = static_cast<size_t>(t) * k;
     float acc[16];
 #pragma unroll
@@ -343,26 +318,26 @@ combine_y24_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
 #pragma unroll 4
     for (int j = 0; j < k; ++j) {
         const float w = topk_w[tk + j];
-        const int p = inv[tk + j];
+        const size_t p = static_cast<size_t>(inv[tk + j]);
         float f[16];
-        y24_row(y + static_cast<size_t>(p) * row_bytes + 3 * hw, lane, lanes_valid, f);
+        y16_row16(codes + p * row_bytes, exps + p * es, f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, f[i], acc[i]);
     }
     {
+        const size_t p = static_cast<size_t>(T) * k + t;
         float f[16];
-        y24_row(y + (static_cast<size_t>(T) * k + t) * row_bytes + 3 * hw, lane, lanes_valid, f);
+        y16_row16(codes + p * row_bytes, exps + p * es, f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] += f[i];
     }
-    if (lane >= lanes_valid) return;
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
         o[i] = *reinterpret_cast<const uint32_t*>(&b);
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + hw + 16 * lane);
+    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + h);
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
@@ -519,11 +494,11 @@ cudaError_t launch_scatter(int T, int H, int E, int k, const int* topk_ids, cons
                          topk_ids, blockhist, offsets, perm, inv, hidden, w_g, gate_logit);
 }
 
-cudaError_t launch_combine(int T, int H, int k, const float* y, bool y24, const float* topk_w,
+cudaError_t launch_combine(int T, int H, int k, const float* y, bool y16, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st) {
-    if (y24) {
+    if (y16) {
         dim3 grid(T, (H / 16 + 127) / 128);
-        return launch_kernel(combine_y24_kernel, grid, dim3(128), 0, st, true, T, H, k,
+        return launch_kernel(combine_y16_kernel, grid, dim3(128), 0, st, true, T, H, k,
                              reinterpret_cast<const uint8_t*>(y), topk_w, inv, out);
     }
     dim3 grid(T, (H / 4 + 255) / 256);

@@ -185,7 +185,7 @@ def test_full_size_workloads(moe, name):
 # 1 + exp(-g) overflows fp32 for g < -88.7 and exceeds 2^126 just above it.
 # Scaling W_down and Ws_down by 2^+-100 (exact in bf16) moves every expert
 # output and the layer output to ~1e30 or ~1e-30 with the same relative
-# rounding, through the fp32 and the 24-bit y paths (large groups: 128-token
+# rounding, through the fp32 and the y16 paths (large groups: 128-token
 # down tiles; small groups: fp32 y).
 MAGNITUDE_CASES = [
     ("saturating_small_groups", 60, 16, 4, 1.0),
