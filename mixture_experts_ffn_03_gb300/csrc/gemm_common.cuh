@@ -301,10 +301,13 @@ __device__ __forceinline__ void gate_up_ts_epilogue_tile(const Tile& ti, uint32_
 // One down tile with the weights on M (W h_hi in accumulator columns [0, BN)
 // and W h_lo in [BN, 2 BN) from `slot`), drained by epilogue warp (q, half):
 // it owns 32 output features (TMEM lanes 32q..) and every other 16-column
-// chunk. Full chunks go out as fp32 TMA box stores of y through st_y, staged
-// in the warp's BUFS buffers at stg (nbuf counts the buffers used); ragged
-// tails as plain stores. Shared-expert rows are scaled by their token's gate
-// sigmoid(x . w_g), NVFP4 tiles by the matrix scale. Warp-uniform.
+// chunk. Shared-expert rows are scaled by their token's gate sigmoid(x .
+// w_g), NVFP4 tiles by the matrix scale. y is written as y16 codes when
+// a.yexp is set (the warp's 32 features of a row are one block: a warp-wide
+// maximum gives its exponent byte), else as fp32. Full chunks go out as TMA
+// box stores through st_y[2] (y16 codes, 64 bytes x 16 rows) or st_y[0]
+// (fp32), staged in the warp's BUFS buffers at stg (nbuf counts the buffers
+// used); ragged tails as plain stores. Warp-uniform.
 template <int BN, int BUFS>
 __device__ __forceinline__ void down_epilogue_tile(const Tile& ti, uint32_t slot, int q, int half,
                                                    int lane, uint8_t* stg, uint32_t& nbuf,
@@ -328,7 +331,39 @@ __device__ __forceinline__ void down_epilogue_tile(const Tile& ti, uint32_t slot
             val[n] = msc * (__uint_as_float(v[n]) + __uint_as_float(vl[n]));
             if (sh && n < rows) val[n] *= 1.f / (1.f + expf(-a.gate_logit[ti.m0 + c0 + n]));
         }
-        if (rows == kEpiRows) {
+        if (a.yexp) {
+            uint32_t code[kEpiRows], b_row = 0;  // lane n keeps row n's exponent byte
+#pragma unroll
+            for (int n = 0; n < kEpiRows; ++n) {
+                const uint32_t x = __float_as_uint(val[n]);
+                const uint32_t b = y16_block_exp(__reduce_max_sync(0xFFFFFFFFu, x & 0x7FFFFFFFu));
+                code[n] = y16_encode(x, b);
+                if (lane == n) b_row = b;
+            }
+            if (rows == kEpiRows) {
+                const uint32_t bb = nbuf++ % BUFS;
+                uint16_t* sc = reinterpret_cast<uint16_t*>(stg + bb * kStgBytes);
+                if (lane == 0) ptx::bulk_wait_read<BUFS - 1>();  // buffer bb is free
+                __syncwarp();
+#pragma unroll
+                for (int n = 0; n < kEpiRows; ++n) sc[n * kEpiCols + lane] = static_cast<uint16_t>(code[n]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(st_y + 2, ptx::smem_u32(sc), 2 * h0, row0 + c0);
+                    ptx::bulk_commit();
+                }
+            } else {
+                uint16_t* yc = reinterpret_cast<uint16_t*>(a.y);
+#pragma unroll
+                for (int n = 0; n < kEpiRows; ++n)
+                    if (n < rows)
+                        yc[static_cast<size_t>(row0 + c0 + n) * a.H + h0 + lane] = static_cast<uint16_t>(code[n]);
+            }
+            if (lane < rows)
+                a.yexp[static_cast<size_t>(row0 + c0 + lane) * y16_exp_stride(a.H) + h0 / kY16Block] =
+                    static_cast<uint8_t>(b_row);
+        } else if (rows == kEpiRows) {
             const uint32_t b = nbuf++ % BUFS;
             float* sy = reinterpret_cast<float*>(stg + b * kStgBytes);
             if (lane == 0) ptx::bulk_wait_read<BUFS - 1>();  // buffer b is free

@@ -228,14 +228,15 @@ bool make_store_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// y codes of 128-token down tiles (y16: rows of 2H bytes, byte tensor
-// [outer, 2 * inner]) written in boxes of 64 bytes x 32 rows.
-bool make_y16_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer) {
+// y16 codes of y (rows of 2H bytes, byte tensor [outer, 2 * inner]) written
+// in boxes of 64 bytes (32 values) x box_rows rows.
+bool make_y16_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {2 * inner, outer};
     cuuint64_t strides[1] = {2 * inner};
-    cuuint32_t box[2] = {64, 32};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -439,7 +440,8 @@ bool make_mx_maps(const moe_dims& d, const ExpertWeights& W, const Layout& L, ch
         ok = ok && make_map_nd(&dn->h, BF16, ws + L.h_hi, 4, dr, sr, box, SW) &&
              make_map_nd(&dn->hs, BF16, ws + L.hs_hi, 4, dsh, ssh, box, SW);
     }
-    ok = ok && make_store_map(&dn->st[0], ws + L.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T);
+    ok = ok && make_store_map(&dn->st[0], ws + L.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
+         make_y16_store_map(&dn->st[2], ws + L.y, H, tk + T, kEpiRows);
     return ok;
 }
 
@@ -581,7 +583,8 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
              make_down_maps(&dn, W.down, W.s_down, h_hi, hs_hi, L.h_lo - L.h_hi,
                             L.hs_lo - L.hs_hi, E, H, I, Is, T, tk, bn_dn, plan.fused);
         ok = ok && make_store_map(&dn.st[0], y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tk + T) &&
-             make_y16_store_map(&dn.st[1], y, H, tk + T);
+             make_y16_store_map(&dn.st[1], y, H, tk + T, 32) &&
+             make_y16_store_map(&dn.st[2], y, H, tk + T, kEpiRows);
     }
     if (!ok) return MOE_ERR_CUDA;
 
@@ -604,8 +607,12 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     ga.hs_hi = hs_hi;
     ga.hs_lo = hs_lo;
     ga.y = y;
-    // y16 exponent plane of the 128-token down tiles, after the codes
-    ga.yexp = reinterpret_cast<uint8_t*>(y) + (tk + T) * 2 * static_cast<size_t>(H);
+    // y as y16 codes (the exponent plane after them) where its bytes matter:
+    // the tokens-on-M down tiles always, the others when fp32 y would exceed
+    // 64 MB. Decode-sized batches keep fp32 y, whose combine has more threads
+    // in flight per output.
+    const bool y16 = (!W.mx && bn_dn == 128) || (tk + T) * static_cast<size_t>(H) * 4 > (64u << 20);
+    if (y16) ga.yexp = reinterpret_cast<uint8_t*>(y) + (tk + T) * 2 * static_cast<size_t>(H);
     ga.err = reinterpret_cast<unsigned*>(meta + META_ERR);
     GemmArgs gd = ga;
     ga.rowtiles = rt_gu;
@@ -706,8 +713,7 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
         if (e_dn != cudaSuccess) return MOE_ERR_CUDA;
         mark_stage(4, st);
     }
-    // 128-token down tiles leave y as y16 codes, the other widths as fp32.
-    if ((launch_combine(T, H, k, y, !W.mx && bn_dn == 128, topk_w, inv,
+    if ((launch_combine(T, H, k, y, y16, topk_w, inv,
                         static_cast<__nv_bfloat16*>(out), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
     mark_stage(5, st);

@@ -188,7 +188,8 @@ __device__ __noinline__ bool layer_prologue(uint8_t* smem, const GemmArgs& a, co
 // Whole-layer launch, after the expert phase (and after TMEM is released):
 // the CTA counts itself done (its epilogue warps have waited for their y
 // stores), waits (bounded) until every CTA is, then combines tokens b, b +
-// grid, ... with the combine kernel's arithmetic. No combine after an abort.
+// grid, ... with the combine kernel's arithmetic (over y16 or fp32 rows). No
+// combine after an abort.
 __device__ __noinline__ void layer_epilogue(const GemmArgs& a, const LayerArgs& l,
                                             volatile int* abort_flag, unsigned code) {
     __shared__ int s_ok;
@@ -203,9 +204,16 @@ __device__ __noinline__ void layer_epilogue(const GemmArgs& a, const LayerArgs& 
     }
     __syncthreads();
     if (!s_ok) return;
-    for (int t = blockIdx.x; t < a.T; t += gridDim.x)
-        combine_token(t, a.H, a.k, a.y, a.y + static_cast<size_t>(a.P) * a.H, l.topk_w, l.inv,
-                      l.out, tid, blockDim.x);
+    if (a.yexp) {
+        const uint8_t* y = reinterpret_cast<const uint8_t*>(a.y);
+        for (int t = blockIdx.x; t < a.T; t += gridDim.x)
+            for (int h = tid * 16; h < a.H; h += blockDim.x * 16)
+                combine16_y16(t, h, a.T, a.H, a.k, y, l.topk_w, l.inv, l.out);
+    } else {
+        for (int t = blockIdx.x; t < a.T; t += gridDim.x)
+            combine_token(t, a.H, a.k, a.y, a.y + static_cast<size_t>(a.P) * a.H, l.topk_w, l.inv,
+                          l.out, tid, blockDim.x);
+    }
 }
 
 template <int BN, bool LAYER>

@@ -281,65 +281,18 @@ combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __
 
 // The same combine over y stored as y16 codes (2H-byte rows, then one
 // exponent byte per 32 values of each row in the exponent plane). A thread
-// owns 16 consecutive outputs: per row it reads 32 contiguous bytes of codes
-// (a warp: 1 KB) and the exponent byte of their block, and the fp32 sum runs
-// in slot order as above.
-__device__ __forceinline__ void y16_row16(const uint8_t* __restrict__ codes,
-                                          const uint8_t* __restrict__ exps, float (&f)[16]) {
-    const uint4* c = reinterpret_cast<const uint4*>(codes);
-    const uint4 c0 = __ldcs(c), c1 = __ldcs(c + 1);
-    const uint32_t b = __ldcs(exps);
-    const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[2 * i] = y16_decode(wv[i] & 0xFFFFu, b);
-        f[2 * i + 1] = y16_decode(wv[i] >> 16, b);
-    }
-}
-
+// owns 16 consecutive outputs (combine16_y16): per row it reads 32
+// contiguous bytes of codes (a warp: 1 KB) and the exponent byte of their
+// block.
 __global__ void __launch_bounds__(128)
 combine_y16_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
                    const float* __restrict__ topk_w, const int* __restrict__ inv,
                    __nv_bfloat16* __restrict__ out) {
-    const int t = blockIdx.x;
     const int h = (blockIdx.y * 128 + threadIdx.x) * 16;  // thread's first output
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
     if (h >= H) return;  // H is a multiple of 64
-    const size_t rows = static_cast<size_t>(T) * k + T;
-    const uint8_t* exps = y + rows * 2 * H + h / kY16Block;
-    const size_t es = static_cast<size_t>(y16_exp_stride(H));
-    const uint8_t* codes = y + 2 * static_cast<size_t>(h);
-    const size_t row_bytes = 2 * static_cast<size_t>(H);
-    const size_t tk = static_cast<size_t>(t) * k;
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-        const float w = topk_w[tk + j];
-        const size_t p = static_cast<size_t>(inv[tk + j]);
-        float f[16];
-        y16_row16(codes + p * row_bytes, exps + p * es, f);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, f[i], acc[i]);
-    }
-    {
-        const size_t p = static_cast<size_t>(T) * k + t;
-        float f[16];
-        y16_row16(codes + p * row_bytes, exps + p * es, f);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] += f[i];
-    }
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        o[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + h);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    combine16_y16(blockIdx.x, h, T, H, k, y, topk_w, inv, out);
 }
 
 // ---------------------------------------------------- expert parallelism

@@ -438,6 +438,66 @@ __device__ __forceinline__ void permute_small(int T, int E, int k, int bn_gu, in
     ordered_scatter(s_ids + a0, a0, a1, s_sub + warp * E, perm, inv, lane);
 }
 
+// 16 consecutive values of one y16 row (codes at `codes`, their block's
+// exponent byte at `exps`).
+__device__ __forceinline__ void y16_row16(const uint8_t* __restrict__ codes,
+                                          const uint8_t* __restrict__ exps, float (&f)[16]) {
+    const uint4* c = reinterpret_cast<const uint4*>(codes);
+    const uint4 c0 = __ldcs(c), c1 = __ldcs(c + 1);
+    const uint32_t b = __ldcs(exps);
+    const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = y16_decode(wv[i] & 0xFFFFu, b);
+        f[2 * i + 1] = y16_decode(wv[i] >> 16, b);
+    }
+}
+
+// out[t, h .. h+15] = bf16(sum_j w_tj y[inv(t,j)] + y[T k + t]) over y16
+// rows (T k routed rows in sorted order, then T gated shared rows; codes
+// from y, then the exponent plane), summed in fp32 in slot order with one
+// rounding. h is a multiple of 16 below H (a multiple of 64).
+__device__ __forceinline__ void combine16_y16(int t, int h, int T, int H, int k,
+                                              const uint8_t* __restrict__ y,
+                                              const float* __restrict__ topk_w,
+                                              const int* __restrict__ inv,
+                                              __nv_bfloat16* __restrict__ out) {
+    const size_t rows = static_cast<size_t>(T) * k + T;
+    const size_t row_bytes = 2 * static_cast<size_t>(H);
+    const uint8_t* codes = y + 2 * static_cast<size_t>(h);
+    const uint8_t* exps = y + rows * row_bytes + h / kY16Block;
+    const size_t es = static_cast<size_t>(y16_exp_stride(H));
+    const size_t tk = static_cast<size_t>(t) * k;
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < k; ++j) {
+        const float w = topk_w[tk + j];
+        const size_t p = static_cast<size_t>(inv[tk + j]);
+        float f[16];
+        y16_row16(codes + p * row_bytes, exps + p * es, f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+    }
+    {
+        const size_t p = static_cast<size_t>(T) * k + t;
+        float f[16];
+        y16_row16(codes + p * row_bytes, exps + p * es, f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] += f[i];
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + h);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // out_t = bf16(sum_j w_tj y[inv(t,j)] + y_shared[t]) for one token, summed in
 // fp32 in slot order; thread i of nthreads takes 4 columns at a time from 4i.
 // The arithmetic is the combine kernel's (fp32 y).

@@ -133,6 +133,8 @@ def test_fusion_launch_counts(moe):
 LAYER_CASES = [c for c in CASES if c.E <= 256] + [
     # 256 tokens: more tokens than CTAs, so CTAs route and combine several each
     wl.MoEConfig("l_many_tokens", T=256, H=256, E=256, k=8, I=128, I_s=128, score_fn=wl.SOFTMAX),
+    # fp32 y rows would take more than 64 MB: y16 rows and their combine
+    wl.MoEConfig("l_y16_rows", T=256, H=7296, E=256, k=8, I=64, I_s=64, score_fn=wl.SIGMOID),
 ]
 
 
