@@ -243,6 +243,10 @@ bool make_y16_store_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t out
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Bytes of y16 rows the tokens-on-M down GEMM stores with an L2 evict-last
+// policy (the last routed rows it writes), for the combine to read from L2.
+constexpr size_t kYKeepBytes = size_t(64) << 20;
+
 int sm_count() {
     static int cache[kMaxDevices] = {0};
     int dev = 0;
@@ -613,6 +617,12 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     // in flight per output.
     const bool y16 = (!W.mx && bn_dn == 128) || (tk + T) * static_cast<size_t>(H) * 4 > (64u << 20);
     if (y16) ga.yexp = reinterpret_cast<uint8_t*>(y) + (tk + T) * 2 * static_cast<size_t>(H);
+    // The routed y rows written last (tiles are claimed in expert order) stay in
+    // L2 for the combine, up to kYKeepBytes of them.
+    {
+        const size_t keep_rows = kYKeepBytes / (2 * static_cast<size_t>(H));
+        ga.y_keep_row = static_cast<int>(tk > keep_rows ? tk - keep_rows : 0);
+    }
     ga.err = reinterpret_cast<unsigned*>(meta + META_ERR);
     GemmArgs gd = ga;
     ga.rowtiles = rt_gu;

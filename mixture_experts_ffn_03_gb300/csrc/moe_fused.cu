@@ -512,7 +512,8 @@ cudaError_t launch_fused_bn(const GemmMaps& gu, const GemmMaps& dn, const GemmAr
 }
 
 // One CTA per SM: every CTA routes, waits for the permute, takes expert
-// tiles (or none) and combines, so the grid never exceeds what is resident.
+// tiles (or none) and combines. Its CTAs wait on one another (the permute
+// flag, the done count), so the launch is cooperative: all of them resident.
 template <int BN>
 cudaError_t launch_layer_bn(const GemmMaps& gu, const GemmMaps& dn, const GemmArgs& a, int* ready,
                             const LayerArgs& l, int num_sms, cudaStream_t st) {
@@ -520,8 +521,8 @@ cudaError_t launch_layer_bn(const GemmMaps& gu, const GemmMaps& dn, const GemmAr
     cudaError_t e = cudaFuncSetAttribute(expert_fused_kernel<BN, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_kernel(expert_fused_kernel<BN, true>, dim3(num_sms), dim3(kFusedThreads), C::SMEM,
-                         st, false, gu, dn, a, ready, l);
+    return launch_kernel_cooperative(expert_fused_kernel<BN, true>, dim3(num_sms),
+                                     dim3(kFusedThreads), C::SMEM, st, gu, dn, a, ready, l);
 }
 
 }  // namespace

@@ -688,6 +688,7 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         uint8_t* stg = smem + C::EPI_OFF + we * C::STG_BYTES;
         const uint32_t stg_u32 = ptx::smem_u32(stg);
         const int es = y16_exp_stride(a.H);
+        const uint64_t pol_keep = ptx::policy_evict_last();
         int as = 0;
         uint32_t aph = 0;
         const int shared_row0 = a.P;
@@ -738,7 +739,10 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&maps.st[1], stg_u32, 2 * f0, row0);
+                            if (row0 >= a.y_keep_row && row0 < a.P)
+                                ptx::tma_store_2d_hint(&maps.st[1], stg_u32, 2 * f0, row0, pol_keep);
+                            else
+                                ptx::tma_store_2d(&maps.st[1], stg_u32, 2 * f0, row0);
                             ptx::bulk_commit();
                         }
                     } else if (lane < rows_valid) {

@@ -29,6 +29,25 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Launch `kern` on `st` as a cooperative launch: every CTA of the grid is
+// resident at once (the launch fails rather than queueing CTAs behind others),
+// which a kernel whose CTAs wait on one another needs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cooperative(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Device status word bits (workspace status block, word 0).
 enum : unsigned {
     ERR_GATE_UP_TIMEOUT = 1u << 0,
@@ -178,6 +197,9 @@ struct GemmArgs {
     __nv_bfloat16* hs_lo;
     float* y;
     uint8_t* yexp;          // y16 exponent plane (tokens-on-M down tiles)
+    // routed y rows from this one on are stored with an L2 evict-last policy
+    // (the rows written last, which the combine can then read from L2)
+    int y_keep_row;
     unsigned* err;
     // NVFP4 weights: fp32 matrix scales of this GEMM's routed experts [E] and
     // of the shared expert [1]; null for bf16 and MXFP8 weights.

@@ -108,6 +108,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
                  "r"(src), "r"(x), "r"(y)
                  : "memory");
 }
+// tma_store_2d with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, uint32_t src, int32_t x,
+                                                  int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+        ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
 // 3D tiled store of one box from shared memory; completion as for tma_store_2d.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int32_t x,
                                              int32_t y, int32_t z) {
