@@ -283,16 +283,18 @@ combine_kernel(int T, int H, int k, const float* __restrict__ y, const float* __
 // exponent byte per 32 values of each row in the exponent plane). A thread
 // owns 16 consecutive outputs (combine16_y16): per row it reads 32
 // contiguous bytes of codes (a warp: 1 KB) and the exponent byte of their
-// block.
-__global__ void __launch_bounds__(128)
+// block. CTAs of 256 threads cover 256 / (H/16) whole tokens (two at H =
+// 2048), or with H/16 > 256 one token's outputs over gridDim.y CTAs.
+__global__ void __launch_bounds__(256)
 combine_y16_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
                    const float* __restrict__ topk_w, const int* __restrict__ inv,
                    __nv_bfloat16* __restrict__ out) {
-    const int h = (blockIdx.y * 128 + threadIdx.x) * 16;  // thread's first output
-    ptx::griddep_launch_dependents();
-    ptx::griddep_wait();
-    if (h >= H) return;  // H is a multiple of 64
-    combine16_y16(blockIdx.x, h, T, H, k, y, topk_w, inv, out);
+    const int per = min(H / 16, 256);  // threads per token and CTA (H is a multiple of 64)
+    const int tpc = 256 / per;         // tokens per CTA
+    const int t = blockIdx.x * tpc + static_cast<int>(threadIdx.x) / per;
+    const int h = (blockIdx.y * 256 + static_cast<int>(threadIdx.x) % per) * 16;
+    if (t >= T || static_cast<int>(threadIdx.x) >= tpc * per || h >= H) return;
+    combine16_y16(t, h, T, H, k, y, topk_w, inv, out);
 }
 
 // ---------------------------------------------------- expert parallelism
@@ -450,8 +452,13 @@ cudaError_t launch_scatter(int T, int H, int E, int k, const int* topk_ids, cons
 cudaError_t launch_combine(int T, int H, int k, const float* y, bool y16, const float* topk_w,
                            const int* inv, __nv_bfloat16* out, cudaStream_t st) {
     if (y16) {
-        dim3 grid(T, (H / 16 + 127) / 128);
-        return launch_kernel(combine_y16_kernel, grid, dim3(128), 0, st, true, T, H, k,
+        // An ordinary launch, after the down GEMM has finished: as a programmatic
+        // dependent its CTAs would sit resident beside the down GEMM's CTAs for
+        // all of that kernel, and the step measured 1-3 % slower (prefill, skewed,
+        // wide) than with this launch.
+        const int per = H / 16 < 256 ? H / 16 : 256, tpc = 256 / per;
+        dim3 grid((T + tpc - 1) / tpc, (H / 16 + 255) / 256);
+        return launch_kernel(combine_y16_kernel, grid, dim3(256), 0, st, false, T, H, k,
                              reinterpret_cast<const uint8_t*>(y), topk_w, inv, out);
     }
     dim3 grid(T, (H / 4 + 255) / 256);
