@@ -172,14 +172,16 @@ bool make_pair_chunk_map(CUtensorMap* m, const void* base, uint64_t inner, uint6
 
 // Operand maps of the bf16 down GEMM (GemmMaps w, ws, h, hs): W_down [E*H, I],
 // Ws_down [H, I_s] and the h_hi / h_lo planes of [P, I] and [T, I_s]. The
-// 128-token tokens-on-M kernel reads 256 weight rows per request; the fused
-// expert launch 64-K steps; down_kernel kDownChunks 64-K chunks per request.
+// tokens-on-M kernels (128-token tiles; stacked 64-token tiles) read 256
+// weight rows per request; the fused expert launch 64-K steps; down_kernel
+// kDownChunks 64-K chunks per request.
 bool make_down_maps(GemmMaps* dn, const void* w_down, const void* ws_down, const void* h_hi,
                     const void* hs_hi, uint64_t h_plane, uint64_t hs_plane, uint64_t E, uint64_t H,
                     uint64_t I, uint64_t Is, uint64_t T, uint64_t P, int bn_dn, bool fused) {
     const uint32_t bn = static_cast<uint32_t>(bn_dn);
-    if (bn_dn == 128 || fused) {
-        const uint32_t w_rows = bn_dn == 128 ? 256u : static_cast<uint32_t>(kGemmBM);
+    if (bn_dn >= 64 || fused) {
+        // 128-token and stacked 64-token tiles: 256 weight rows per request
+        const uint32_t w_rows = (!fused && bn_dn >= 64) ? 256u : static_cast<uint32_t>(kGemmBM);
         return make_map(&dn->w, w_down, I, E * H, w_rows) &&
                make_map(&dn->ws, ws_down, Is, H, w_rows) &&
                make_pair_map(&dn->h, h_hi, I, P, h_plane, bn) &&
@@ -643,7 +645,9 @@ moe_status forward_impl(const moe_dims* d, const void* hidden, const float* rout
     const int gu_nf = W.mx || plan.fused ? kGemmBM : gate_up_ts_features(bn_gu);
     const int F_gu = (I + gu_nf - 1) / gu_nf, F_s = (Is + gu_nf - 1) / gu_nf;
     // 128-token down tiles use the tokens-on-M kernel with 256 output features per tile.
-    const int F_dn = bn_dn == 128 ? (H + 255) / 256 : (H + kGemmBM - 1) / kGemmBM;
+    // 128-token and (unfused bf16) 64-token down tiles take 256 output features.
+    const bool dn256 = bn_dn == 128 || (bn_dn == 64 && !plan.fused && !W.mx);
+    const int F_dn = dn256 ? (H + 255) / 256 : (H + kGemmBM - 1) / kGemmBM;
     const size_t max_gu = (tk / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
     const size_t max_dn = (tk / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
     const int cap = 1 << 30;
@@ -1119,7 +1123,7 @@ MOE_API moe_status moe_ep_experts(const moe_ep_dims* d, int32_t R, const void* x
     const size_t routed_min = static_cast<size_t>(R) < segs ? static_cast<size_t>(R) : segs;
     const int F_gu = (I + static_cast<int>(gu_rows) - 1) / static_cast<int>(gu_rows);
     const int F_s = (Is + static_cast<int>(gu_rows) - 1) / static_cast<int>(gu_rows);
-    const int F_dn = (H + kGemmBM - 1) / kGemmBM;
+    const int F_dn = bn_dn == 64 ? (H + 255) / 256 : (H + kGemmBM - 1) / kGemmBM;
     const size_t max_gu = (R / bn_gu + routed_min) * F_gu + ((T + bn_gu - 1) / bn_gu) * F_s;
     const size_t max_dn = (R / bn_dn + routed_min) * F_dn + ((T + bn_dn - 1) / bn_dn) * F_dn;
     const size_t cap = 1u << 30;

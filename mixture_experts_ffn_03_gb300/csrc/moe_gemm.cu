@@ -772,6 +772,301 @@ down_ts_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     gemm_teardown<C>(tmem_base, warp);
 }
 
+// =========================================== down, stacked h_hi / h_lo rows
+// Tiles of up to 64 tokens of one expert against 256 output features (groups
+// too small for 128-token tiles): the MMA's M side stacks the tile's 64 h_hi
+// rows over its 64 h_lo rows (one TMA box of the h_hi / h_lo pair) and the
+// 256 weight rows are the N side, so one MMA of M = 128, N = 256 covers both
+// halves for 256 x 16 weights: half the MMA instructions per weight of the
+// weights-on-M form (one MMA of N = BN + rows per 128 x 16 weights), whose
+// pace at these widths the MMA instruction rate sets. TMEM lanes 0-63 hold
+// W h_hi of the tokens and lanes 64-127 W h_lo: the epilogue warp of lanes
+// 64 + 32j.. hands its 32 x 32 values per chunk to the warp of lanes 32j..
+// through shared memory (mbarrier hand-offs with bounded waits), which adds
+// the two halves in fp32, as the weights-on-M epilogue does, and writes y.
+struct DownStk {
+    static constexpr int BN = 64;                            // tokens per tile (each half)
+    static constexpr int NF = 256;                           // output features per tile (MMA N)
+    static constexpr int A_BYTES = 2 * BN * kGemmBK * 2;     // 16 KB: h_hi rows, then h_lo rows
+    static constexpr int W_BYTES = NF * kGemmBK * 2;         // 32 KB: weight tile
+    static constexpr int STAGE_BYTES = A_BYTES + W_BYTES;
+    static constexpr int XCH_BYTES = 32 * 32 * 4;            // one warp pair's hand-off block
+    static constexpr int STG_BYTES = 32 * 32 * 4;            // one storing warp's y box (64 B rows used)
+    static constexpr int XBAR_OFF = 4 * XCH_BYTES + 4 * STG_BYTES;  // hand-off mbarriers
+    static constexpr int EPI_BYTES = XBAR_OFF + 1024;
+    static constexpr int CTL_BYTES = 1024;
+    static constexpr int STAGES_FIT = (kSmemLimit - 1024 - EPI_BYTES - CTL_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > kStageCap ? kStageCap : STAGES_FIT;
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+    static constexpr int CTL_OFF = EPI_OFF + EPI_BYTES;
+    static constexpr int SMEM = 1024 + CTL_OFF + CTL_BYTES;
+    static constexpr int ACC_COLS = NF;
+    static constexpr int A_STAGES = 0;
+    static constexpr int CONVERTER_WARPS = 0;
+    static constexpr int ACC_STAGES = 2;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(STAGES >= 3, "pipeline depth");
+    static_assert(SMEM <= kSmemLimit, "shared memory budget");
+    static_assert(EPI_OFF % 1024 == 0 && STG_BYTES % 1024 == 0, "swizzled staging alignment");
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+down_stk_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    using C = DownStk;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::CTL_OFF);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + C::EPI_OFF + C::XBAR_OFF);  // [4] full, [4] empty
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&maps.w);
+        ptx::prefetch_tmap(&maps.ws);
+        ptx::prefetch_tmap(&maps.h);
+        ptx::prefetch_tmap(&maps.hs);
+        ptx::prefetch_tmap(&maps.st[1]);
+    }
+    if (threadIdx.x == 0)
+        for (int i = 0; i < 8; ++i) ptx::mbar_init(bar_addr(&xbar[i]), 1);  // fenced in gemm_setup
+    const uint32_t tmem_base = gemm_setup<C>(ctl, warp, 1 + kEpiWarps);
+    ptx::griddep_wait();  // h, tile lists and the gate logits come from earlier kernels
+
+    const int R = a.meta[META_RT_DN];
+    const int F = (a.H + C::NF - 1) / C::NF;
+    const int shared_tiles = ((a.T + C::BN - 1) / C::BN) * F;
+    const int num_tiles = R * F + shared_tiles;
+    volatile int* abort_flag = &ctl->abort;
+    unsigned* err = a.err;
+    const unsigned code = ERR_DOWN_TIMEOUT;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------------------------- TMA producer
+            const uint64_t pol_w = ptx::policy_evict_normal();
+            const uint64_t pol_h = ptx::policy_evict_last();  // h rows are re-read per feature block
+            int s = 0;
+            uint32_t ph = 0, armed = 0, parity_bits = 0;
+            bool ok = true;
+            TileSched<C::BN> sch;
+            Tile ti = sch.start(num_tiles, shared_tiles, F, F, a);
+            int qs = 0;
+            uint32_t qph = 0;
+            ok = tq_publish(ctl, qs, qph, ti, abort_flag, err, code);
+            for (; ok && ti.n_rows >= 0;
+                 ok = ok && sch.next(ti, a) && tq_publish(ctl, qs, qph, ti, abort_flag, err, code)) {
+                sch.prefetch(a);
+                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const CUtensorMap* tw = ti.shared ? &maps.ws : &maps.w;
+                const CUtensorMap* th = ti.shared ? &maps.hs : &maps.h;
+                // Rows past this expert's H (a ragged last block) read the next
+                // expert's rows or zero fill; their columns are never stored.
+                const int row_w = (ti.shared ? 0 : ti.e * a.H) + ti.f * C::NF;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint32_t fb = bar_addr(&ctl->full_a[s]);
+                    ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    // the tile's 64 h_hi rows, then its 64 h_lo rows (one request);
+                    // then 256 weight rows (one request)
+                    ptx::tma_load_3d(sa, th, fb, ks * kGemmBK, ti.p0, 0, pol_h);
+                    ptx::tma_load_2d(sa + C::A_BYTES, tw, fb, ks * kGemmBK, row_w, pol_w);
+                    armed |= 1u << s;
+                    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) drain_tma<C::STAGES>(ctl, armed, parity_bits);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------------------------- MMA issuer
+            int s = 0, as = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            int qs = 0;
+            uint32_t qph = 0;
+            Tile ti;
+            while (ok && tq_read(ctl, qs, qph, ti, true, abort_flag, err, code)) {
+                const int ksteps = (ti.shared ? a.I_s : a.I) / kGemmBK;
+                const int n_f = min(C::NF, a.H - ti.f * C::NF);  // a multiple of 64
+                const uint32_t idesc = ptx::idesc_bf16_f32(128, n_f);
+                if (!wait_bar(bar_addr(&ctl->tempty[as]), aph ^ 1u, abort_flag, err, code)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + as * C::ACC_COLS;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!wait_bar(bar_addr(&ctl->full_a[s]), ph, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+                    const uint64_t dh = ptx::smem_desc_sw128(sa);
+                    const uint64_t dw = ptx::smem_desc_sw128(sa + C::A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk)
+                        ptx::mma_bf16_ss(d, dh + 2 * kk, dw + 2 * kk, idesc, (ks | kk) != 0 ? 1u : 0u);
+                    ptx::mma_commit(bar_addr(&ctl->empty[s]));
+                    if (++s == C::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar_addr(&ctl->tfull[as]));
+                if (++as == C::ACC_STAGES) {
+                    as = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) {
+                ptx::mma_commit(bar_addr(&ctl->drain));
+                wait_bounded(bar_addr(&ctl->drain), 0);
+            }
+        }
+    } else if (warp >= 4) {  // ------------------------------ epilogue (warps 4-11)
+        // Warp (q, half) reads TMEM lanes 32q.. over the columns [128 half, +128)
+        // in 32-column chunks. q = 0, 1 (lanes 0-63: W h_hi of tokens 32q..)
+        // store; q = 2, 3 (W h_lo of the same tokens) hand their chunk to the
+        // warp of q - 2 through block p (its mbarriers xbar[p] full, xbar[4 + p]
+        // empty). The storing warp adds the halves, scales shared-expert rows by
+        // the gate, and writes y: y16 codes (its own staging box, one TMA store
+        // per chunk of 32 full rows, the four exponent bytes of the tile as one
+        // 4-byte store) or fp32 rows.
+        const int we = warp - 4, q = warp & 3, half = we >> 2;
+        const bool store = q < 2;
+        const int p = (q & 1) + 2 * half;
+        float* xb = reinterpret_cast<float*>(smem + C::EPI_OFF + p * C::XCH_BYTES);
+        uint8_t* stg = smem + C::EPI_OFF + 4 * C::XCH_BYTES + p * C::STG_BYTES;
+        const uint32_t stg_u32 = ptx::smem_u32(stg);
+        const uint32_t xfull = bar_addr(&xbar[p]), xempty = bar_addr(&xbar[4 + p]);
+        const int es = y16_exp_stride(a.H);
+        uint32_t xph = 0;
+        int as = 0;
+        uint32_t aph = 0;
+        const int shared_row0 = a.P;
+        int qs = 0;
+        uint32_t qph = 0;
+        bool ok = true;
+        Tile ti;
+        while (ok && tq_read(ctl, qs, qph, ti, false, abort_flag, err, code)) {
+            if (!wait_bar(bar_addr(&ctl->tfull[as]), aph, abort_flag, err, code)) break;
+            ptx::tc_fence_after();
+            const int r0 = (q & 1) * 32;            // this pair's first token row of the tile
+            const int rows_valid = ti.n_rows - r0;  // the pair's token rows that are real
+            const int c_begin = half * (C::NF / 2);
+            const int n_f = min(C::NF, a.H - ti.f * C::NF);
+            if (rows_valid > 0 && c_begin < n_f) {
+                const int row0 = (ti.shared ? shared_row0 + ti.m0 : ti.p0) + r0;
+                float scale = 1.f;
+                if (store && ti.shared && lane < rows_valid)
+                    scale = 1.f / (1.f + expf(-a.gate_logit[ti.m0 + r0 + lane]));
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * C::ACC_COLS;
+                uint32_t eb = 0;
+                for (int col = c_begin; col < c_begin + C::NF / 2; col += 32) {
+                    if (col >= n_f) break;
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(tb + col, v);
+                    ptx::tmem_ld_wait();
+                    if (!store) {
+                        if (!wait_bar(xempty, xph ^ 1u, abort_flag, err, code)) {
+                            ok = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) xb[c * 32 + lane] = __uint_as_float(v[c]);
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(xfull);
+                        xph ^= 1u;
+                        continue;
+                    }
+                    if (!wait_bar(xfull, xph, abort_flag, err, code)) {
+                        ok = false;
+                        break;
+                    }
+                    float f[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) f[c] = (__uint_as_float(v[c]) + xb[c * 32 + lane]) * scale;
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(xempty);
+                    xph ^= 1u;
+                    const int f0 = ti.f * C::NF + col;
+                    if (a.yexp) {
+                        uint32_t mx = 0;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) mx = max(mx, __float_as_uint(f[c]) & 0x7FFFFFFFu);
+                        const uint32_t b = y16_block_exp(mx);
+                        eb |= b << (((col - c_begin) / 32) * 8);
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = y16_encode(__float_as_uint(f[2 * i]), b) |
+                                   (y16_encode(__float_as_uint(f[2 * i + 1]), b) << 16);
+                        if (rows_valid >= 32) {
+                            if (lane == 0) ptx::bulk_wait_read<0>();  // staging box free again
+                            __syncwarp();
+                            const uint32_t row_addr = stg_u32 + lane * 64;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                ptx::st_shared_v4u(row_addr + 16 * j, w[4 * j], w[4 * j + 1],
+                                                   w[4 * j + 2], w[4 * j + 3]);
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_2d(&maps.st[1], stg_u32, 2 * f0, row0);
+                                ptx::bulk_commit();
+                            }
+                        } else if (lane < rows_valid) {
+                            uint4* dst = reinterpret_cast<uint4*>(
+                                reinterpret_cast<uint8_t*>(a.y) + static_cast<size_t>(row0 + lane) * 2 * a.H +
+                                2 * f0);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        }
+                    } else if (lane < rows_valid) {
+                        float4* dst = reinterpret_cast<float4*>(a.y + static_cast<size_t>(row0 + lane) * a.H + f0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+                    }
+                }
+                // bytes past the row's last block fall into the padding of the stride
+                if (ok && store && a.yexp && lane < rows_valid)
+                    *reinterpret_cast<uint32_t*>(a.yexp + static_cast<size_t>(row0 + lane) * es +
+                                                 (ti.f * C::NF + c_begin) / kY16Block) = eb;
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(&ctl->tempty[as]));
+            if (++as == C::ACC_STAGES) {
+                as = 0;
+                aph ^= 1u;
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_all();
+    }
+    gemm_teardown<C>(tmem_base, warp);
+}
+
+cudaError_t launch_down_stk(const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
+                            cudaStream_t st) {
+    using C = DownStk;
+    cudaError_t e = cudaFuncSetAttribute(down_stk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = max_tiles < num_sms ? max_tiles : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    return launch_kernel(down_stk_kernel, dim3(grid), dim3(kThreads), C::SMEM, st, true, maps, a);
+}
+
 template <int BN, bool GU>
 cudaError_t launch_bn(const GemmMaps& maps, const GemmArgs& a, int max_tiles, int num_sms,
                       cudaStream_t st) {
@@ -805,7 +1100,9 @@ cudaError_t dispatch(int bn, const GemmMaps& maps, const GemmArgs& a, int max_ti
     switch (bn) {
         case 16: return launch_bn<16, GU>(maps, a, max_tiles, num_sms, st);
         case 32: return launch_bn<32, GU>(maps, a, max_tiles, num_sms, st);
-        case 64: return launch_bn<64, GU>(maps, a, max_tiles, num_sms, st);
+        case 64:
+            if constexpr (GU) return launch_bn<64, GU>(maps, a, max_tiles, num_sms, st);
+            return launch_down_stk(maps, a, max_tiles, num_sms, st);
         case 128:
             if constexpr (GU) return launch_bn<128, GU>(maps, a, max_tiles, num_sms, st);
             return launch_down_ts(maps, a, max_tiles, num_sms, st);
