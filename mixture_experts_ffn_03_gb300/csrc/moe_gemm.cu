@@ -16,14 +16,17 @@
 //   accumulator stage.
 //   The epilogue writes h = silu(G) * U as a bf16 high/low pair (h_hi =
 //   bf16(h), h_lo = bf16(h - h_hi)).
-// down, BN <= 64: weights on M (128 output features); the tile's h_hi and
+// down, BN <= 32: weights on M (128 output features); the tile's h_hi and
 //   h_lo rows are adjacent in shared memory and form the N side of one MMA
 //   against the same weight tile; two 64-K chunks per pipeline stage; the
-//   epilogue adds the two column blocks and writes fp32 rows of y per (token,
-//   slot). BN = 128 (down_ts_kernel): tokens on M, 256 output features on N,
-//   h_hi and h_lo as two A operands into one accumulator; y as y16 codes
-//   (16 bits per value and one exponent byte per 32 values). The shared
-//   expert's rows are scaled by the per-token gate sigmoid(x . w_g).
+//   epilogue adds the two column blocks and writes y rows per (token, slot)
+//   (fp32, or y16 codes where fp32 y would be large). BN = 64
+//   (down_stk_kernel): the tile's h_hi rows stacked over its h_lo rows on M,
+//   256 output features on N, the two halves added in the epilogue. BN = 128
+//   (down_ts_kernel): tokens on M, 256 output features on N, h_hi and h_lo as
+//   two A operands into one accumulator; y as y16 codes (16 bits per value
+//   and one exponent byte per 32 values). The shared expert's rows are scaled
+//   by the per-token gate sigmoid(x . w_g).
 // Sources: "Add Qwen3.5-35B-A3B (support vision and text input)", Description
 // (stacked 3D expert weights; per-token sigmoid-gated shared expert); the
 // SwiGLU expert FFN is the plain reading of the stacked gate/up layout.
