@@ -383,6 +383,13 @@ int moe_get_expert_fusion(void);
  * Returns MOE_ERR_WORKSPACE for a missing or misaligned workspace. */
 moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream);
 
+/* Test hook of the y16 format in which the down GEMMs hand large expert
+ * outputs to the combine (see the workspace layout above): out[i] = the
+ * value in[i] decodes to after encoding, each block of 32 consecutive values
+ * taking one exponent byte from its largest magnitude. n (a multiple of 32,
+ * else MOE_ERR_INVALID_ARG) device fp32 values; enqueued on cuda_stream. */
+moe_status moe_y16_roundtrip(const float* in, float* out, int64_t n, void* cuda_stream);
+
 /*
  * Expert parallelism: the layer spread over G ranks (one GPU each), rank g
  * owning the contiguous block of routed experts [g E/G, (g+1) E/G) and a copy

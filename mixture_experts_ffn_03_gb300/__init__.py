@@ -34,7 +34,7 @@ EXPORTED = ["moe_workspace_size", "moe_forward", "moe_device_status", "moe_statu
             "moe_forward_nvfp4", "moe_nvfp4_dequant", "moe_launch_count_quantized",
             "moe_set_expert_fusion", "moe_get_expert_fusion", "moe_pipeline_create",
             "moe_pipeline_submit", "moe_pipeline_drain", "moe_pipeline_streams",
-            "moe_pipeline_destroy"]
+            "moe_pipeline_destroy", "moe_y16_roundtrip"]
 NUM_STAGES = 5
 STAGE_NAMES = ["route", "scatter", "gate_up", "down", "combine"]
 
@@ -88,6 +88,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_selftest_wait_limit.restype = ctypes.c_int
     lib.moe_forward_mxfp8.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 15 + [P, ctypes.c_size_t, P]
     lib.moe_forward_mxfp8.restype = ctypes.c_int
+    lib.moe_y16_roundtrip.argtypes = [P, P, ctypes.c_int64, P]
+    lib.moe_y16_roundtrip.restype = ctypes.c_int
     lib.moe_mxfp8_dequant.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
     lib.moe_mxfp8_dequant.restype = ctypes.c_int
     lib.moe_forward_router.argtypes = [ctypes.POINTER(MoEDims)] + [P] * 12 + [P, ctypes.c_size_t, P]
@@ -270,6 +272,19 @@ def mxfp8_dequant(codes, scales, out=None, stream=None):
                                           _ptr(out), _stream_handle(stream))
     if st != MOE_OK:
         raise MoEError(st, "moe_mxfp8_dequant")
+    return out
+
+
+def y16_roundtrip(x, out=None, stream=None):
+    """fp32 values through the y16 format (moe_y16_roundtrip): x float32 on the
+    GPU with a multiple of 32 elements, each block of 32 consecutive values
+    sharing one exponent byte; returns the decoded values."""
+    import torch
+    if out is None:
+        out = torch.empty_like(x)
+    st = load_library().moe_y16_roundtrip(_ptr(x), _ptr(out), int(x.numel()), _stream_handle(stream))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_y16_roundtrip")
     return out
 
 

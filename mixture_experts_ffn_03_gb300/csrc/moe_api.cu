@@ -887,6 +887,21 @@ MOE_API moe_status moe_set_stage_events(void* const* events, int n_events) {
     return MOE_OK;
 }
 
+namespace moe {
+// moe_route.cu: n (a multiple of 32) fp32 values through the y16 format.
+cudaError_t launch_y16_roundtrip(long n, const float* in, float* out, cudaStream_t st);
+}  // namespace moe
+
+MOE_API moe_status moe_y16_roundtrip(const float* in, float* out, int64_t n, void* cuda_stream) {
+    if (n < 0 || n % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!in || !out) return MOE_ERR_INVALID_ARG;
+    if (launch_y16_roundtrip(static_cast<long>(n), in, out, static_cast<cudaStream_t>(cuda_stream)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 MOE_API moe_status moe_selftest_wait_limit(void* workspace, void* cuda_stream) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return MOE_ERR_WORKSPACE;

@@ -297,6 +297,21 @@ combine_y16_kernel(int T, int H, int k, const uint8_t* __restrict__ y,
     combine16_y16(t, h, T, H, k, y, topk_w, inv, out);
 }
 
+// fp32 values through the y16 format (the down GEMMs' encoder, the combine's
+// decoder): warp w takes blocks w, w + warps, ... of 32 values, lane i value
+// i; the block's exponent byte comes from a warp-wide maximum, as in the
+// weights-on-M down epilogue.
+__global__ void __launch_bounds__(256)
+y16_roundtrip_kernel(long n, const float* __restrict__ in, float* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const long warps = static_cast<long>(gridDim.x) * 8;
+    for (long blk = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5); blk * 32 < n; blk += warps) {
+        const uint32_t x = __float_as_uint(in[blk * 32 + lane]);
+        const uint32_t b = y16_block_exp(__reduce_max_sync(0xFFFFFFFFu, x & 0x7FFFFFFFu));
+        out[blk * 32 + lane] = y16_decode(y16_encode(x, b), b);
+    }
+}
+
 // ---------------------------------------------------- expert parallelism
 // Rows of the (token, slot) pairs in expert-sorted order: rows[p] =
 // hidden[perm[p] / k]. The rows bound for one rank's block of experts are
@@ -464,6 +479,12 @@ cudaError_t launch_combine(int T, int H, int k, const float* y, bool y16, const 
     dim3 grid(T, (H / 4 + 255) / 256);
     return launch_kernel(combine_kernel, grid, dim3(256), 0, st, true, T, H, k, y,
                          y + static_cast<size_t>(T) * k * H, topk_w, inv, out);
+}
+
+cudaError_t launch_y16_roundtrip(long n, const float* in, float* out, cudaStream_t st) {
+    const long blocks = (n / 32 + 7) / 8;
+    y16_roundtrip_kernel<<<static_cast<unsigned>(blocks < 1184 ? blocks : 1184), 256, 0, st>>>(n, in, out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine_split(int T, int H, int k, const float* y_routed, const float* y_shared,
