@@ -10,7 +10,8 @@
 // products and the fp32 accumulation are the bf16 path's.
 //
 // The layer's arithmetic is that of moe_gemm.cu (weights on the MMA's M
-// side, tokens on N, h as a bf16 hi/lo pair, fp32 y), with the weights
+// side, tokens on N, h as a bf16 hi/lo pair, y as fp32 or, where fp32 y would
+// be large, as y16 codes), with the weights
 // arriving as one byte (MXFP8) or half a byte (NVFP4) per value:
 //   TMA -> shared memory: codes (128-byte swizzle; 64-byte for the NVFP4
 //     gate_up rows of 128 values) and their block scales;
