@@ -294,8 +294,10 @@ const char* moe_status_string(moe_status s);
  *   in sorted order, as a high + low bf16 pair), hs_hi / hs_lo [T, I_s] bf16
  *   (shared expert activation), y [T k + T, H] (rows [0, T k): routed
  *   expert outputs in sorted order; rows T k + t: gated shared output).
- *   y holds fp32 values, except when the mean expert group is large enough
- *   for 128-token down tiles (1.25 T k / E > 64): then it holds y16 codes,
+ *   y holds fp32 values, except when fp32 y ((T k + T) H 4 bytes) would
+ *   exceed 64 MiB or, with bf16 expert weights, when the mean expert group
+ *   is large enough for 128-token down tiles (1.25 T k / E > 64): then it
+ *   holds y16 codes,
  *   16 bits per value (rows of 2 H bytes) followed by an exponent plane of
  *   one byte per 32 values of each row (row stride H/32 rounded up to a
  *   multiple of 4): a value v of a block with exponent byte b is |v| +
